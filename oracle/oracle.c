@@ -1,0 +1,255 @@
+/*
+ * oracle.c — plain FP64 CPU oracle for the GEMM and fused-SwiGLU hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link
+ * or call this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline use it.  It shares no code, header, table or helper with the CUDA
+ * library under swiglu_mlp_gb300/.
+ *
+ * What it computes (sources, by page title and section):
+ *
+ *   GEMM   D[i][j] = alpha * sum_p opA(i,p) * opB(p,j) + beta * C_old[i][j]
+ *          "GEMM o Coração Matemático", §1 (the BLAS GEMM statement and its
+ *          element-wise form; op(X) is X or its transpose) and §2 (row-major
+ *          linearisation, position i*N + j).  The sum over p runs in ascending
+ *          order, one element at a time, in double precision.
+ *          When beta == 0, C is not read at all (§2.1, the ikj kernel fills C
+ *          with zeros instead of scaling it), so NaN in C cannot leak out.
+ *
+ *   SwiGLU Y = SiLU(A*W1) (.) (A*W2), with SiLU(x) = x * sigmoid(x)
+ *          = x / (1 + exp(-x))
+ *          "Sobreposição de Ativação em Nível de Tile para Inferência
+ *          Eficiente de LLM", Definição do Problema (the gated MLP) and
+ *          Metodologia, Kernel-2 (SiLU applied to the Gate column, multiplied
+ *          by the Up column).  The oracle takes W1 and W2 SEPARATELY, so the
+ *          column interleave used by the product is checked independently.
+ *
+ *   Interleave  W_fused[k][2n] = W1[k][n], W_fused[k][2n+1] = W2[k][n]
+ *          Same page, Metodologia, Kernel-2 (even columns Gate, odd Up).
+ *
+ * Inputs arrive as the stored, already-rounded values: IEEE binary16 bits,
+ * bfloat16 bits, or binary32.  Each is widened to double exactly (every
+ * binary16, bfloat16 and binary32 value is a double).  Outputs are double and
+ * are NOT rounded to the product's output type.
+ *
+ * Speed comes only from splitting rows across threads and from visiting
+ * (p, j) in the ikj order ("GEMM o Coração Matemático", §2.1), which keeps the
+ * per-element summation order p = 0, 1, ..., K-1.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_F32 = 2 };
+
+/* ---- exact widening of the stored formats ---------------------------- */
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double orc_f16_to_f64(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0)            /* zero or subnormal: f * 2^-24 */
+        v = ldexp((double)f, -24);
+    else if (e == 31)      /* infinity or NaN */
+        v = f ? NAN : INFINITY;
+    else                   /* normal: (1024 + f) * 2^(e - 15 - 10) */
+        v = ldexp((double)(1024 + f), e - 25);
+    return sign ? -v : v;
+}
+
+/* bfloat16 is the upper half of an IEEE binary32: 1 sign, 8 exponent bits
+ * (bias 127), 7 fraction bits.  Decoded from the fields, not by a bit cast. */
+double orc_bf16_to_f64(uint16_t b)
+{
+    int sign = (b >> 15) & 1;
+    int e = (b >> 7) & 0xff;
+    int f = b & 0x7f;
+    double v;
+    if (e == 0)            /* zero or subnormal: f * 2^-133 */
+        v = ldexp((double)f, -133);
+    else if (e == 255)
+        v = f ? NAN : INFINITY;
+    else                   /* (128 + f) * 2^(e - 127 - 7) */
+        v = ldexp((double)(128 + f), e - 134);
+    return sign ? -v : v;
+}
+
+static double load_elem(const void *base, int64_t idx, int type)
+{
+    switch (type) {
+    case ORC_F16:  return orc_f16_to_f64(((const uint16_t *)base)[idx]);
+    case ORC_BF16: return orc_bf16_to_f64(((const uint16_t *)base)[idx]);
+    default:       return (double)((const float *)base)[idx];
+    }
+}
+
+/* SiLU(x) = x * sigmoid(x) = x / (1 + e^-x). */
+double orc_silu(double x)
+{
+    return x / (1.0 + exp(-x));
+}
+
+/* ---- GEMM ------------------------------------------------------------ */
+
+typedef struct {
+    int transA, transB;
+    int64_t M, N, K;
+    double alpha, beta;
+    const void *A; int64_t lda; int a_type;
+    const double *opB;            /* op(B) widened, K x N, row-major */
+    const void *C; int64_t ldc; int c_type;
+    const int64_t *rows; int64_t n_rows;
+    double *D;                    /* n_rows x N */
+    int64_t r_begin, r_end;
+} gemm_job;
+
+/* opA(i,p): row-major A is M x K (op = N) or K x M (op = T), row stride lda. */
+static double opA_at(const gemm_job *g, int64_t i, int64_t p)
+{
+    int64_t idx = g->transA ? p * g->lda + i : i * g->lda + p;
+    return load_elem(g->A, idx, g->a_type);
+}
+
+static void *gemm_rows(void *arg)
+{
+    gemm_job *g = (gemm_job *)arg;
+    const int64_t N = g->N, K = g->K;
+    double *arow = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+    for (int64_t r = g->r_begin; r < g->r_end; ++r) {
+        int64_t i = g->rows ? g->rows[r] : r;
+        double *acc = g->D + r * N;
+        for (int64_t j = 0; j < N; ++j)
+            acc[j] = 0.0;
+        for (int64_t p = 0; p < K; ++p)
+            arow[p] = opA_at(g, i, p);
+        /* ikj: acc[j] += a_ip * b_pj for p = 0..K-1; each acc[j] still sums
+         * its K products in ascending p. */
+        for (int64_t p = 0; p < K; ++p) {
+            const double a = arow[p];
+            const double *brow = g->opB + p * N;
+            for (int64_t j = 0; j < N; ++j)
+                acc[j] += a * brow[j];
+        }
+        for (int64_t j = 0; j < N; ++j) {
+            double y = g->alpha * acc[j];
+            if (g->beta != 0.0)
+                y += g->beta * load_elem(g->C, i * g->ldc + j, g->c_type);
+            acc[j] = y;
+        }
+    }
+    free(arow);
+    return NULL;
+}
+
+static int pick_threads(int n_threads, int64_t n_rows)
+{
+    if (n_threads <= 0) {
+        long c = sysconf(_SC_NPROCESSORS_ONLN);
+        n_threads = c > 0 ? (int)c : 1;
+    }
+    if (n_threads > 256) n_threads = 256;
+    if ((int64_t)n_threads > n_rows) n_threads = (int)(n_rows > 0 ? n_rows : 1);
+    return n_threads;
+}
+
+/* Widen op(B) into a dense K x N double matrix: opB(p,j) = B[p*ldb + j]
+ * (op = N, B stored K x N) or B[j*ldb + p] (op = T, B stored N x K). */
+static double *widen_opB(int transB, int64_t N, int64_t K, const void *B,
+                         int64_t ldb, int b_type)
+{
+    double *opB = (double *)malloc(sizeof(double) * (size_t)(K * N > 0 ? K * N : 1));
+    if (!opB) return NULL;
+    for (int64_t p = 0; p < K; ++p)
+        for (int64_t j = 0; j < N; ++j)
+            opB[p * N + j] = load_elem(B, transB ? j * ldb + p : p * ldb + j, b_type);
+    return opB;
+}
+
+/* Computes rows[0..n_rows) of D (all rows 0..M-1 when rows == NULL, and then
+ * n_rows must equal M).  D is n_rows x N doubles, row-major.  Returns 0 on
+ * success, -1 on bad arguments or allocation failure. */
+int orc_gemm(int transA, int transB, int64_t M, int64_t N, int64_t K,
+             double alpha, const void *A, int64_t lda, int a_type,
+             const void *B, int64_t ldb, int b_type, double beta,
+             const void *C, int64_t ldc, int c_type,
+             const int64_t *rows, int64_t n_rows, double *D, int n_threads)
+{
+    if (M < 0 || N < 0 || K < 0 || n_rows < 0 || !D) return -1;
+    if (!rows && n_rows != M) return -1;
+    if (n_rows == 0 || N == 0) return 0;
+    double *opB = widen_opB(transB, N, K, B, ldb, b_type);
+    if (!opB) return -1;
+    int T = pick_threads(n_threads, n_rows);
+    pthread_t th[256];
+    gemm_job jobs[256];
+    for (int t = 0; t < T; ++t) {
+        gemm_job *g = &jobs[t];
+        g->transA = transA; g->transB = transB;
+        g->M = M; g->N = N; g->K = K;
+        g->alpha = alpha; g->beta = beta;
+        g->A = A; g->lda = lda; g->a_type = a_type;
+        g->opB = opB;
+        g->C = C; g->ldc = ldc; g->c_type = c_type;
+        g->rows = rows; g->n_rows = n_rows; g->D = D;
+        g->r_begin = n_rows * t / T;
+        g->r_end = n_rows * (t + 1) / T;
+        pthread_create(&th[t], NULL, gemm_rows, g);
+    }
+    for (int t = 0; t < T; ++t)
+        pthread_join(th[t], NULL);
+    free(opB);
+    return 0;
+}
+
+/* ---- SwiGLU ---------------------------------------------------------- */
+
+/* Y[i][n] = SiLU(G[i][n]) * U[i][n] with G = A*W1, U = A*W2; A is M x K
+ * bfloat16 (row stride lda), W1 and W2 are K x N bfloat16 (row stride ldw).
+ * Both products come from orc_gemm with alpha = 1, beta = 0. */
+int orc_swiglu(const uint16_t *A, int64_t lda, const uint16_t *W1,
+               const uint16_t *W2, int64_t ldw, int64_t M, int64_t N,
+               int64_t K, const int64_t *rows, int64_t n_rows, double *Y,
+               int n_threads)
+{
+    if (!rows && n_rows != M) return -1;
+    if (n_rows == 0 || N == 0) return 0;
+    double *G = (double *)malloc(sizeof(double) * (size_t)(n_rows * N));
+    double *U = (double *)malloc(sizeof(double) * (size_t)(n_rows * N));
+    int rc = (G && U) ? 0 : -1;
+    if (rc == 0)
+        rc = orc_gemm(0, 0, M, N, K, 1.0, A, lda, ORC_BF16, W1, ldw, ORC_BF16,
+                      0.0, NULL, 0, ORC_BF16, rows, n_rows, G, n_threads);
+    if (rc == 0)
+        rc = orc_gemm(0, 0, M, N, K, 1.0, A, lda, ORC_BF16, W2, ldw, ORC_BF16,
+                      0.0, NULL, 0, ORC_BF16, rows, n_rows, U, n_threads);
+    if (rc == 0)
+        for (int64_t e = 0; e < n_rows * N; ++e)
+            Y[e] = orc_silu(G[e]) * U[e];
+    free(G);
+    free(U);
+    return rc;
+}
+
+/* W_fused (K x 2N, row stride 2N) from W1, W2 (K x N, row stride N):
+ * column 2n is W1's column n (Gate), column 2n+1 is W2's column n (Up). */
+void orc_interleave(const uint16_t *W1, const uint16_t *W2, uint16_t *Wf,
+                    int64_t K, int64_t N)
+{
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t n = 0; n < N; ++n) {
+            Wf[k * 2 * N + 2 * n] = W1[k * N + n];
+            Wf[k * 2 * N + 2 * n + 1] = W2[k * N + n];
+        }
+}
+
+int orc_num_cores(void)
+{
+    long c = sysconf(_SC_NPROCESSORS_ONLN);
+    return c > 0 ? (int)c : 1;
+}
