@@ -1,0 +1,164 @@
+/*
+ * swiglu_mlp.h — C ABI of the GB300 (sm_103a) GEMM and fused-SwiGLU library.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Matrices are ROW-MAJOR: element (i, j) of a matrix with row stride ld
+ *   sits at offset i*ld + j ("GEMM o Coração Matemático", §2, row-major
+ *   linearisation).  ld counts elements, not bytes.
+ * - op(X) is X (SWG_OP_N) or its transpose (SWG_OP_T) of the STORED row-major
+ *   matrix ("GEMM o Coração Matemático", §1: reading a matrix as transposed
+ *   needs no copy).
+ * - All pointers except alpha/beta scalars are DEVICE pointers on the current
+ *   CUDA device.  The caller owns every tensor; the library never frees them.
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   Calls are asynchronous: SWG_OK means the work was validated and enqueued.
+ * - Every argument is validated BEFORE any CUDA call; a rejected call writes
+ *   nothing and launches nothing.
+ * - Accumulation is always FP32, in tensor memory; outputs are rounded once,
+ *   round-to-nearest-even, at the store.
+ * - There is no CPU fallback: an unsupported case returns an error.
+ * - Device-side waits are bounded: a kernel that cannot make progress within
+ *   about two seconds stops, records SWG_ERR_DEVICE_TIMEOUT in a device error
+ *   word, and exits; read it with swg_get_device_error().
+ */
+#ifndef SWIGLU_MLP_H
+#define SWIGLU_MLP_H
+
+#include <stdint.h>
+
+/* Exported with default visibility even when the library is built with
+ * -fvisibility=hidden. */
+#if defined(__GNUC__)
+#define SWG_API __attribute__((visibility("default")))
+#else
+#define SWG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SWG_OK = 0,
+    SWG_ERR_INVALID_ARG = 1,    /* negative size, null pointer, ld too small, bad enum */
+    SWG_ERR_MISALIGNED = 2,     /* a pointer or row stride breaks the 16-byte rule */
+    SWG_ERR_UNSUPPORTED = 3,    /* valid request this library does not implement */
+    SWG_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed */
+    SWG_ERR_NO_MEMORY = 5,      /* library workspace allocation failed */
+    SWG_ERR_DEVICE_TIMEOUT = 6  /* a kernel gave up on a bounded wait */
+} swg_status;
+
+typedef enum { SWG_OP_N = 0, SWG_OP_T = 1 } swg_op;
+
+/* Storage types.  A and B share one input type; C and D share one output type. */
+typedef enum {
+    SWG_F16_F32OUT = 0,   /* A, B binary16;  C, D binary32 */
+    SWG_BF16 = 1,         /* A, B, C, D bfloat16            */
+    SWG_F16 = 2,          /* A, B, C, D binary16            */
+    SWG_BF16_F32OUT = 3   /* A, B bfloat16;  C, D binary32  */
+} swg_dtype;
+
+/*
+ * gemm — D = alpha * op(A) * op(B) + beta * C, written in place over C.
+ *
+ * Defined by "GEMM o Coração Matemático", §1 (the BLAS GEMM statement, element
+ * by element: D_ij = alpha * sum_p op(A)_ip op(B)_pj + beta * C_ij) and by
+ * "为什么 GEMM 是 CUDA 的必修课" (the opening definition C = A B with 2K flops
+ * per element).
+ *
+ *   transA, transB  SWG_OP_N or SWG_OP_T.
+ *   M, N, K         op(A) is M x K, op(B) is K x N, C/D is M x N.  All >= 0.
+ *                   M == 0 or N == 0: nothing to do, returns SWG_OK.
+ *                   K == 0: D = beta * C (D = 0 when beta == 0).
+ *   alpha, beta     host scalars.  When beta == 0, C is NOT read (so NaN or
+ *                   garbage in C does not reach D).
+ *   A, lda          stored M x K (op N) or K x M (op T); lda >= stored columns.
+ *   B, ldb          stored K x N (op N) or N x K (op T); ldb >= stored columns.
+ *   C, ldc          M x N, ldc >= N; read (when beta != 0) and overwritten.
+ *   dtype           a swg_dtype.
+ *   Alignment       A, B, C must be 16-byte aligned and lda, ldb, ldc times
+ *                   the element size must be multiples of 16 bytes (tensor
+ *                   memory accelerator rule); otherwise SWG_ERR_MISALIGNED.
+ *   Sizes           M, N, K, lda, ldb, ldc <= 2^31 - 1, else SWG_ERR_UNSUPPORTED.
+ *   Aliasing        A or B overlapping C is undefined.
+ *   Split-K         chosen automatically when the output has too few tiles to
+ *                   fill the GPU ("为什么 GEMM 是 CUDA 的必修课", 关键技术 item 5);
+ *                   the partial sums are reduced in a fixed order, so repeated
+ *                   calls give bit-identical results.  The FP32 partials live
+ *                   in a library-owned workspace, allocated on first use per
+ *                   (device, stream) and freed by swg_shutdown().
+ */
+SWG_API int gemm(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
+         const void *A, int64_t lda, const void *B, int64_t ldb, float beta,
+         void *C, int64_t ldc, int dtype, void *stream);
+
+/*
+ * gemm_ex — gemm with an explicit split-K factor.
+ *   split_k == 0  automatic choice (what gemm does);
+ *   split_k == 1  no split;
+ *   split_k >= 2  split the K loop into at most split_k contiguous ranges
+ *                 (fewer when K has fewer 64-wide blocks).
+ * Every other argument and rule is that of gemm.
+ */
+SWG_API int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,
+            float alpha, const void *A, int64_t lda, const void *B,
+            int64_t ldb, float beta, void *C, int64_t ldc, int dtype,
+            int split_k, void *stream);
+
+/*
+ * swiglu_mlp — Y = SiLU(A * W1) (.) (A * W2) as ONE GEMM over the interleaved
+ * weight W_fused, with SiLU(x) = x / (1 + e^-x).
+ *
+ * Defined by "Sobreposição de Ativação em Nível de Tile para Inferência
+ * Eficiente de LLM": Definição do Problema (the SwiGLU MLP) and Metodologia,
+ * Kernel-2 (one GEMM over W_fused in R^{K x 2N} whose even columns are Gate
+ * and odd columns Up; the epilogue reads each column pair of the accumulator
+ * and stores SiLU(gate) * up).  Gate and Up stay in tensor memory and
+ * registers; neither is written to global memory.
+ *
+ *   A        bfloat16, M x K, row stride K.
+ *   W_fused  bfloat16, K x 2N, row stride 2N: W_fused[k][2n] = W1[k][n],
+ *            W_fused[k][2n+1] = W2[k][n] (see swiglu_interleave).
+ *   Y        bfloat16, M x N, row stride N (written).
+ *   Alignment  all three pointers 16-byte aligned, K % 8 == 0 and
+ *            N % 8 == 0; otherwise SWG_ERR_MISALIGNED.
+ *   M == 0 or N == 0: nothing to do.  K == 0: Y = SiLU(0) * 0 = 0.
+ */
+SWG_API int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M,
+               int64_t N, int64_t K, void *stream);
+
+/*
+ * swiglu_interleave — builds W_fused (K x 2N, row stride 2N) from W1 and W2
+ * (each K x N, row stride N), bfloat16: column 2n <- W1 column n (Gate),
+ * column 2n+1 <- W2 column n (Up).  Same page and section as swiglu_mlp.
+ * A one-off weight-layout step, not part of the per-token hot path.
+ * Pointers 16-byte aligned and N % 4 == 0, else SWG_ERR_MISALIGNED.
+ */
+SWG_API int swiglu_interleave(const void *W1, const void *W2, void *W_fused,
+                      int64_t K, int64_t N, void *stream);
+
+/* Human-readable name of a swg_status value (static string, never NULL). */
+SWG_API const char *swg_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns SWG_OK when no kernel reported a problem since the last call,
+ * SWG_ERR_DEVICE_TIMEOUT when a bounded wait ran out, SWG_ERR_CUDA when the
+ * synchronisation itself failed.  After a timeout the library's split-K
+ * tickets for this stream are cleared, so later calls start clean.
+ */
+SWG_API int swg_get_device_error(void *stream);
+
+/* Number of kernels this library has launched in this process (all devices). */
+SWG_API uint64_t swg_launch_count(void);
+
+/* Frees every library-owned workspace on every device.  Safe to call twice;
+ * later calls allocate afresh.  Call only when no library work is in flight. */
+SWG_API void swg_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWIGLU_MLP_H */

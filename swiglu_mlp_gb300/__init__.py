@@ -1,0 +1,205 @@
+"""Python binding of ``libswiglu_mlp.so`` (C ABI in ``include/swiglu_mlp.h``).
+
+Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels.  There is no fallback of any kind; if the shared
+library has not been built this module raises on first use.
+
+Functions with the C names take the C arguments (pointers may be given as
+ints or as tensors, whose ``data_ptr()`` is used; ``stream`` may be a
+``torch.cuda.Stream``, a raw handle, or None for the current torch stream).
+Each raises :class:`SwgError` when the library returns a non-zero status.
+The ``*_into`` helpers derive sizes and strides from row-major torch tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "SwgError", "OP_N", "OP_T", "F16_F32OUT", "BF16", "F16", "BF16_F32OUT",
+    "gemm", "gemm_ex", "swiglu_mlp", "swiglu_interleave", "status_string",
+    "get_device_error", "launch_count", "shutdown", "gemm_into",
+    "swiglu_mlp_into", "interleave_weights", "library_path", "load",
+]
+
+OP_N, OP_T = 0, 1
+F16_F32OUT, BF16, F16, BF16_F32OUT = 0, 1, 2, 3
+STATUS = {0: "SWG_OK", 1: "SWG_ERR_INVALID_ARG", 2: "SWG_ERR_MISALIGNED",
+          3: "SWG_ERR_UNSUPPORTED", 4: "SWG_ERR_CUDA", 5: "SWG_ERR_NO_MEMORY",
+          6: "SWG_ERR_DEVICE_TIMEOUT"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libswiglu_mlp.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class SwgError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {STATUS.get(self.status, 'SWG_ERR_UNKNOWN')} ({self.status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Loads the shared library (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(_LIB_PATH)
+        i64, i32, f32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+        lib.gemm.argtypes = [i32, i32, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, i32, vp]
+        lib.gemm.restype = i32
+        lib.gemm_ex.argtypes = [i32, i32, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, i32,
+                                i32, vp]
+        lib.gemm_ex.restype = i32
+        lib.swiglu_mlp.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+        lib.swiglu_mlp.restype = i32
+        lib.swiglu_interleave.argtypes = [vp, vp, vp, i64, i64, vp]
+        lib.swiglu_interleave.restype = i32
+        lib.swg_status_string.argtypes = [i32]
+        lib.swg_status_string.restype = ctypes.c_char_p
+        lib.swg_get_device_error.argtypes = [vp]
+        lib.swg_get_device_error.restype = i32
+        lib.swg_launch_count.argtypes = []
+        lib.swg_launch_count.restype = ctypes.c_uint64
+        lib.swg_shutdown.argtypes = []
+        lib.swg_shutdown.restype = None
+        _lib = lib
+        return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        if torch.cuda.is_available():
+            return torch.cuda.current_stream().cuda_stream
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(rc: int, where: str) -> int:
+    if rc != 0:
+        raise SwgError(rc, where)
+    return rc
+
+
+def gemm(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtype, stream=None):
+    """D = alpha * op(A) op(B) + beta * C, in place over C (see the C header)."""
+    return _check(load().gemm(int(transA), int(transB), int(M), int(N), int(K), float(alpha),
+                              _ptr(A), int(lda), _ptr(B), int(ldb), float(beta), _ptr(C),
+                              int(ldc), int(dtype), _stream(stream)), "gemm")
+
+
+def gemm_ex(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtype, split_k,
+            stream=None):
+    return _check(load().gemm_ex(int(transA), int(transB), int(M), int(N), int(K), float(alpha),
+                                 _ptr(A), int(lda), _ptr(B), int(ldb), float(beta), _ptr(C),
+                                 int(ldc), int(dtype), int(split_k), _stream(stream)), "gemm_ex")
+
+
+def swiglu_mlp(A, W_fused, Y, M, N, K, stream=None):
+    """Y = SiLU(A W1) (.) (A W2) over the interleaved W_fused (see the C header)."""
+    return _check(load().swiglu_mlp(_ptr(A), _ptr(W_fused), _ptr(Y), int(M), int(N), int(K),
+                                    _stream(stream)), "swiglu_mlp")
+
+
+def swiglu_interleave(W1, W2, W_fused, K, N, stream=None):
+    return _check(load().swiglu_interleave(_ptr(W1), _ptr(W2), _ptr(W_fused), int(K), int(N),
+                                           _stream(stream)), "swiglu_interleave")
+
+
+def status_string(status: int) -> str:
+    return load().swg_status_string(int(status)).decode()
+
+
+def get_device_error(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device error word."""
+    return load().swg_get_device_error(_stream(stream))
+
+
+def launch_count() -> int:
+    return int(load().swg_launch_count())
+
+
+def shutdown() -> None:
+    load().swg_shutdown()
+
+
+# ---------------------------------------------------------------- tensor helpers
+
+def _dtype_code(in_dtype, out_dtype) -> int:
+    import torch
+    table = {(torch.float16, torch.float32): F16_F32OUT, (torch.bfloat16, torch.bfloat16): BF16,
+             (torch.float16, torch.float16): F16, (torch.bfloat16, torch.float32): BF16_F32OUT}
+    try:
+        return table[(in_dtype, out_dtype)]
+    except KeyError:
+        raise SwgError(3, f"gemm_into: unsupported dtypes {in_dtype} -> {out_dtype}") from None
+
+
+def _row_major_ld(t, name):
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise SwgError(1, f"{name} must be a 2-D row-major tensor (unit column stride)")
+    return t.stride(0)
+
+
+def gemm_into(C, A, B, transA=0, transB=0, alpha=1.0, beta=0.0, split_k=None, stream=None):
+    """C <- alpha * op(A) op(B) + beta * C for 2-D row-major tensors."""
+    M = A.shape[1] if transA else A.shape[0]
+    K = A.shape[0] if transA else A.shape[1]
+    N = B.shape[0] if transB else B.shape[1]
+    Kb = B.shape[1] if transB else B.shape[0]
+    if Kb != K or tuple(C.shape) != (M, N) or A.dtype != B.dtype:
+        raise SwgError(1, "gemm_into: inconsistent shapes or dtypes")
+    code = _dtype_code(A.dtype, C.dtype)
+    args = (transA, transB, M, N, K, alpha, A, _row_major_ld(A, "A"), B, _row_major_ld(B, "B"),
+            beta, C, _row_major_ld(C, "C"), code)
+    if split_k is None:
+        gemm(*args, stream=stream)
+    else:
+        gemm_ex(*args, split_k, stream=stream)
+    return C
+
+
+def swiglu_mlp_into(Y, A, W_fused, stream=None):
+    """Y <- SiLU(A W1) (.) (A W2) with W_fused the interleaved [K, 2N] weight."""
+    M, K = A.shape
+    N = W_fused.shape[1] // 2
+    if W_fused.shape[0] != K or tuple(Y.shape) != (M, N):
+        raise SwgError(1, "swiglu_mlp_into: inconsistent shapes")
+    for t, n in ((A, "A"), (W_fused, "W_fused"), (Y, "Y")):
+        if not t.is_contiguous():
+            raise SwgError(1, f"swiglu_mlp_into: {n} must be contiguous")
+    swiglu_mlp(A, W_fused, Y, M, N, K, stream=stream)
+    return Y
+
+
+def interleave_weights(W1, W2, stream=None):
+    """W_fused[K, 2N] with even columns W1 (Gate) and odd columns W2 (Up)."""
+    import torch
+    K, N = W1.shape
+    if tuple(W2.shape) != (K, N) or not (W1.is_contiguous() and W2.is_contiguous()):
+        raise SwgError(1, "interleave_weights: W1, W2 must be contiguous and the same shape")
+    Wf = torch.empty((K, 2 * N), dtype=W1.dtype, device=W1.device)
+    swiglu_interleave(W1, W2, Wf, K, N, stream=stream)
+    return Wf

@@ -1,0 +1,503 @@
+// api.cu — the C ABI declared in include/swiglu_mlp.h: argument validation,
+// tile/split selection, tensor-map encoding, library-owned workspace, and the
+// two small auxiliary kernels (K == 0 scaling, weight interleave).
+//
+// Validation happens before any CUDA call, so a rejected call has no side
+// effects and the checks run on machines without a GPU.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <map>
+#include <mutex>
+#include <vector>
+
+#include "../../include/swiglu_mlp.h"
+#include "launch.h"
+
+namespace {
+
+using swg::TileParams;
+
+std::atomic<uint64_t> g_launches{0};
+std::mutex g_mu;
+
+// Device error word: written by kernels whose bounded waits ran out.
+__device__ int g_err_word;
+
+constexpr int64_t kMaxDim = 0x7fffffff;
+
+// ----------------------------------------------------------------- dtypes
+
+struct TypeInfo {
+    bool in_bf16;    // A, B bfloat16 (else binary16)
+    int out_kind;    // swg::OutKind
+    int out_bytes;
+};
+
+bool type_info(int dtype, TypeInfo &t)
+{
+    switch (dtype) {
+    case SWG_F16_F32OUT: t = {false, swg::OUT_F32, 4}; return true;
+    case SWG_BF16: t = {true, swg::OUT_BF16, 2}; return true;
+    case SWG_F16: t = {false, swg::OUT_F16, 2}; return true;
+    case SWG_BF16_F32OUT: t = {true, swg::OUT_F32, 4}; return true;
+    default: return false;
+    }
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ----------------------------------------------------------------- per device
+
+struct Workspace {
+    void *base = nullptr;   // [tickets | partials]
+    size_t bytes = 0;
+    size_t ticket_bytes = 0;
+};
+
+struct DeviceState {
+    bool ready = false;
+    int sms = 0;
+    int *err = nullptr;                          // address of g_err_word
+    std::map<cudaStream_t, Workspace> ws;
+};
+
+std::map<int, DeviceState> g_dev;
+
+int device_state(DeviceState *&out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SWG_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState &d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SWG_ERR_CUDA;
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return SWG_ERR_CUDA;
+        d.err = static_cast<int *>(p);
+        d.ready = true;
+    }
+    out = &d;
+    return SWG_OK;
+}
+
+// Grow-only split-K workspace for (device, stream).  Tickets are zeroed on
+// allocation and every reducing CTA resets its own ticket.
+int workspace(DeviceState *d, cudaStream_t s, size_t ticket_bytes, size_t part_bytes,
+              Workspace *&out)
+{
+    if (std::getenv("SWG_TEST_FAIL_ALLOC")) return SWG_ERR_NO_MEMORY;
+    std::lock_guard<std::mutex> lk(g_mu);
+    Workspace &w = d->ws[s];
+    ticket_bytes = (ticket_bytes + 255) & ~size_t(255);
+    const size_t need = ticket_bytes + part_bytes;
+    if (w.base == nullptr || w.ticket_bytes < ticket_bytes || w.bytes < need) {
+        const size_t tb = std::max(ticket_bytes, w.ticket_bytes);
+        const size_t total = tb + std::max(part_bytes, w.bytes - w.ticket_bytes);
+        if (w.base) {
+            if (cudaStreamSynchronize(s) != cudaSuccess) return SWG_ERR_CUDA;
+            cudaFree(w.base);
+            w.base = nullptr;
+        }
+        void *p = nullptr;
+        if (cudaMalloc(&p, total) != cudaSuccess) {
+            cudaGetLastError();
+            w = Workspace{};
+            return SWG_ERR_NO_MEMORY;
+        }
+        if (cudaMemsetAsync(p, 0, tb, s) != cudaSuccess) {
+            cudaFree(p);
+            w = Workspace{};
+            return SWG_ERR_CUDA;
+        }
+        w.base = p;
+        w.bytes = total;
+        w.ticket_bytes = tb;
+    }
+    out = &w;
+    return SWG_OK;
+}
+
+// ----------------------------------------------------------------- tensor maps
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Row-major matrix of `outer` rows x `inner` contiguous 16-bit elements with
+// row stride `ld`, read in boxes of 64 x box_outer with the 128-byte swizzle.
+// Rows/columns past the matrix read as zero.
+bool make_tmap(CUtensorMap *m, const void *ptr, bool bf16, int64_t inner, int64_t outer,
+               int64_t ld, int box_outer)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {64u, (cuuint32_t)box_outer};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                    const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// tcgen05 instruction descriptor, kind::f16: D=F32 (bits 4-5 = 1), A/B type
+// (bits 7-9, 10-12: 0 = f16, 1 = bf16), A/B major (bits 15, 16: 1 = MN-major),
+// N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+uint32_t make_idesc(bool bf16, bool a_mn, bool b_mn, int m, int n)
+{
+    const uint32_t t = bf16 ? 1u : 0u;
+    return (1u << 4) | (t << 7) | (t << 10) | ((a_mn ? 1u : 0u) << 15) |
+           ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Tile width with the best last-wave fill; ties and near-ties keep the wider
+// tile (more operand reuse per byte loaded).
+int pick_bn(int64_t M, int64_t N, int sms, const int *cands, int ncand)
+{
+    int best = cands[0];
+    double best_score = -1.0;
+    for (int i = 0; i < ncand; ++i) {
+        const int bn = cands[i];
+        const int64_t tiles = cdiv(M, swg::BM) * cdiv(N, bn);
+        const int64_t waves = cdiv(tiles, sms);
+        double eff = double(tiles) / double(waves * sms);
+        // Narrow tiles re-read A more often; only take one for a clear gain.
+        const double penalty = bn == 256 ? 1.0 : bn == 128 ? 0.90 : 0.80;
+        const double score = eff * penalty;
+        if (score > best_score + 1e-9) {
+            best_score = score;
+            best = bn;
+        }
+    }
+    return best;
+}
+
+// ----------------------------------------------------------------- small kernels
+
+__global__ void scale_kernel(void *D, long long ldd, int M, int N, float beta, int out_kind)
+{
+    const long long total = (long long)M * N;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long r = i / N, c = i - r * N;
+        const long long o = r * ldd + c;
+        if (out_kind == swg::OUT_F32) {
+            float *d = static_cast<float *>(D);
+            d[o] = beta == 0.0f ? 0.0f : beta * d[o];
+        } else if (out_kind == swg::OUT_F16) {
+            __half *d = static_cast<__half *>(D);
+            d[o] = __float2half_rn(beta == 0.0f ? 0.0f : beta * __half2float(d[o]));
+        } else {
+            __nv_bfloat16 *d = static_cast<__nv_bfloat16 *>(D);
+            d[o] = __float2bfloat16_rn(beta == 0.0f ? 0.0f : beta * __bfloat162float(d[o]));
+        }
+    }
+}
+
+// Four output column pairs per thread: 8-byte loads from W1 and W2, one
+// 16-byte store of (g0,u0,g1,u1,g2,u2,g3,u3).
+__global__ void interleave_kernel(const uint16_t *W1, const uint16_t *W2, uint16_t *Wf, long long K,
+                                  long long N)
+{
+    const long long quads = N / 4;
+    const long long total = K * quads;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long k = i / quads, n = (i - k * quads) * 4;
+        const uint2 g = *reinterpret_cast<const uint2 *>(W1 + k * N + n);
+        const uint2 u = *reinterpret_cast<const uint2 *>(W2 + k * N + n);
+        uint4 o;
+        o.x = (g.x & 0xffffu) | (u.x << 16);
+        o.y = (g.x >> 16) | (u.x & 0xffff0000u);
+        o.z = (g.y & 0xffffu) | (u.y << 16);
+        o.w = (g.y >> 16) | (u.y & 0xffff0000u);
+        *reinterpret_cast<uint4 *>(Wf + k * 2 * N + 2 * n) = o;
+    }
+}
+
+int grid_for(long long work, int sms)
+{
+    long long g = cdiv(work, 256);
+    const long long cap = (long long)sms * 8;
+    if (g > cap) g = cap;
+    if (g < 1) g = 1;
+    return (int)g;
+}
+
+}  // namespace
+
+// =================================================================== C ABI
+
+extern "C" {
+
+const char *swg_status_string(int status)
+{
+    switch (status) {
+    case SWG_OK: return "SWG_OK";
+    case SWG_ERR_INVALID_ARG: return "SWG_ERR_INVALID_ARG";
+    case SWG_ERR_MISALIGNED: return "SWG_ERR_MISALIGNED";
+    case SWG_ERR_UNSUPPORTED: return "SWG_ERR_UNSUPPORTED";
+    case SWG_ERR_CUDA: return "SWG_ERR_CUDA";
+    case SWG_ERR_NO_MEMORY: return "SWG_ERR_NO_MEMORY";
+    case SWG_ERR_DEVICE_TIMEOUT: return "SWG_ERR_DEVICE_TIMEOUT";
+    default: return "SWG_ERR_UNKNOWN";
+    }
+}
+
+uint64_t swg_launch_count(void) { return g_launches.load(); }
+
+int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha, const void *A,
+            int64_t lda, const void *B, int64_t ldb, float beta, void *C, int64_t ldc, int dtype,
+            int split_k, void *stream)
+{
+    TypeInfo ti;
+    if (!type_info(dtype, ti)) return SWG_ERR_UNSUPPORTED;
+    if ((transA != SWG_OP_N && transA != SWG_OP_T) || (transB != SWG_OP_N && transB != SWG_OP_T))
+        return SWG_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0 || split_k < 0) return SWG_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return SWG_OK;
+    const int64_t a_cols = transA ? M : K, b_cols = transB ? K : N;
+    if (C == nullptr || ldc < N) return SWG_ERR_INVALID_ARG;
+    if (K > 0 && (A == nullptr || B == nullptr || lda < a_cols || ldb < b_cols))
+        return SWG_ERR_INVALID_ARG;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim || ldc > kMaxDim || lda > kMaxDim ||
+        ldb > kMaxDim)
+        return SWG_ERR_UNSUPPORTED;
+    if (!aligned16(C) || (ldc * ti.out_bytes) % 16 != 0) return SWG_ERR_MISALIGNED;
+    if (K > 0 && (!aligned16(A) || !aligned16(B) || (lda * 2) % 16 != 0 || (ldb * 2) % 16 != 0))
+        return SWG_ERR_MISALIGNED;
+
+    DeviceState *d = nullptr;
+    if (int rc = device_state(d)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    if (K == 0) {
+        scale_kernel<<<grid_for(M * N, d->sms), 256, 0, s>>>(C, ldc, (int)M, (int)N, beta,
+                                                              ti.out_kind);
+        g_launches++;
+        return cudaGetLastError() == cudaSuccess ? SWG_OK : SWG_ERR_CUDA;
+    }
+
+    const int64_t kb = cdiv(K, swg::BK);
+    const int64_t mblk = cdiv(M, swg::BM);
+    int splits = 1;
+    int bn = 256;
+    if (split_k == 0) {
+        const int64_t tiles256 = mblk * cdiv(N, 256);
+        if (tiles256 * 2 <= d->sms && kb >= 8) {
+            splits = (int)std::min<int64_t>(d->sms / tiles256, kb / 4);
+            if (splits < 2) splits = 1;
+        }
+    } else if (split_k > 1) {
+        splits = (int)std::min<int64_t>(split_k, kb);
+    }
+    int kbps = (int)kb;
+    if (splits > 1) {
+        kbps = (int)cdiv(kb, splits);
+        splits = (int)cdiv(kb, kbps);
+    }
+    if (splits <= 1) {
+        static const int cands[] = {256, 128};
+        bn = pick_bn(M, N, d->sms, cands, 2);
+    }
+
+    const bool a_mn = transA == SWG_OP_T;
+    const bool b_mn = transB == SWG_OP_N;
+    CUtensorMap ta, tb;
+    bool ok = a_mn ? make_tmap(&ta, A, ti.in_bf16, M, K, lda, 64)
+                   : make_tmap(&ta, A, ti.in_bf16, K, M, lda, swg::BM);
+    ok = ok && (b_mn ? make_tmap(&tb, B, ti.in_bf16, N, K, ldb, 64)
+                     : make_tmap(&tb, B, ti.in_bf16, K, N, ldb, bn));
+    if (!ok) return SWG_ERR_CUDA;
+
+    TileParams p{};
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.m_blocks = (int)mblk;
+    p.n_blocks = (int)cdiv(N, bn);
+    p.k_blocks = (int)kb;
+    p.tiles = p.m_blocks * p.n_blocks;
+    p.splits = splits;
+    p.kb_per_split = kbps;
+    p.units = p.tiles * splits;
+    p.group_m = 16;
+    p.idesc = make_idesc(ti.in_bf16, a_mn, b_mn, swg::BM, bn);
+    p.a_mn_major = a_mn;
+    p.b_mn_major = b_mn;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.D = C;
+    p.ldd = ldc;
+    p.out_kind = ti.out_kind;
+    p.err = d->err;
+
+    const int grid = (int)std::min<int64_t>(p.units, d->sms);
+    cudaError_t e;
+    if (splits > 1) {
+        const int64_t ld_ws = cdiv(N, 4) * 4;
+        Workspace *w = nullptr;
+        if (int rc = workspace(d, s, sizeof(int) * (size_t)p.tiles,
+                               sizeof(float) * (size_t)splits * (size_t)M * (size_t)ld_ws, w))
+            return rc;
+        p.tickets = static_cast<int *>(w->base);
+        p.ws = reinterpret_cast<float *>(static_cast<char *>(w->base) + w->ticket_bytes);
+        p.ld_ws = ld_ws;
+        e = swg::launch_tc_splitk(bn, ta, tb, p, grid, s);
+    } else {
+        e = swg::launch_tc_store(bn, ta, tb, p, grid, s);
+    }
+    if (e != cudaSuccess) return SWG_ERR_CUDA;
+    g_launches++;
+    return SWG_OK;
+}
+
+int gemm(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha, const void *A,
+         int64_t lda, const void *B, int64_t ldb, float beta, void *C, int64_t ldc, int dtype,
+         void *stream)
+{
+    return gemm_ex(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtype, 0,
+                   stream);
+}
+
+int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M, int64_t N, int64_t K,
+               void *stream)
+{
+    if (M < 0 || N < 0 || K < 0) return SWG_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return SWG_OK;
+    if (Y == nullptr || (K > 0 && (A == nullptr || W_fused == nullptr)))
+        return SWG_ERR_INVALID_ARG;
+    if (M > kMaxDim || 2 * N > kMaxDim || K > kMaxDim) return SWG_ERR_UNSUPPORTED;
+    if (!aligned16(Y) || N % 8 != 0) return SWG_ERR_MISALIGNED;
+    if (K > 0 && (!aligned16(A) || !aligned16(W_fused) || K % 8 != 0)) return SWG_ERR_MISALIGNED;
+
+    DeviceState *d = nullptr;
+    if (int rc = device_state(d)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    if (K == 0) {   // Gate = Up = 0, so Y = SiLU(0) * 0 = 0.
+        scale_kernel<<<grid_for(M * N, d->sms), 256, 0, s>>>(Y, N, (int)M, (int)N, 0.0f,
+                                                              swg::OUT_BF16);
+        g_launches++;
+        return cudaGetLastError() == cudaSuccess ? SWG_OK : SWG_ERR_CUDA;
+    }
+
+    const int64_t N2 = 2 * N;
+    static const int cands[] = {256, 128, 64};
+    const int bn = pick_bn(M, N2, d->sms, cands, 3);
+    CUtensorMap ta, tb;
+    if (!make_tmap(&ta, A, true, K, M, K, swg::BM) || !make_tmap(&tb, W_fused, true, N2, K, N2, 64))
+        return SWG_ERR_CUDA;
+
+    TileParams p{};
+    p.M = (int)M;
+    p.N = (int)N2;
+    p.K = (int)K;
+    p.m_blocks = (int)cdiv(M, swg::BM);
+    p.n_blocks = (int)cdiv(N2, bn);
+    p.k_blocks = (int)cdiv(K, swg::BK);
+    p.tiles = p.m_blocks * p.n_blocks;
+    p.splits = 1;
+    p.kb_per_split = p.k_blocks;
+    p.units = p.tiles;
+    p.group_m = 16;
+    p.idesc = make_idesc(true, false, true, swg::BM, bn);
+    p.a_mn_major = 0;
+    p.b_mn_major = 1;
+    p.alpha = 1.0f;
+    p.beta = 0.0f;
+    p.D = Y;
+    p.ldd = N;
+    p.out_kind = swg::OUT_BF16;
+    p.err = d->err;
+    const int grid = (int)std::min<int64_t>(p.units, d->sms);
+    if (swg::launch_tc_swiglu(bn, ta, tb, p, grid, s) != cudaSuccess) return SWG_ERR_CUDA;
+    g_launches++;
+    return SWG_OK;
+}
+
+int swiglu_interleave(const void *W1, const void *W2, void *W_fused, int64_t K, int64_t N,
+                      void *stream)
+{
+    if (K < 0 || N < 0) return SWG_ERR_INVALID_ARG;
+    if (K == 0 || N == 0) return SWG_OK;
+    if (!W1 || !W2 || !W_fused) return SWG_ERR_INVALID_ARG;
+    if (K > kMaxDim || 2 * N > kMaxDim) return SWG_ERR_UNSUPPORTED;
+    if (!aligned16(W1) || !aligned16(W2) || !aligned16(W_fused) || N % 4 != 0)
+        return SWG_ERR_MISALIGNED;
+    DeviceState *d = nullptr;
+    if (int rc = device_state(d)) return rc;
+    interleave_kernel<<<grid_for(K * N / 4, d->sms), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(W1), static_cast<const uint16_t *>(W2),
+        static_cast<uint16_t *>(W_fused), K, N);
+    g_launches++;
+    return cudaGetLastError() == cudaSuccess ? SWG_OK : SWG_ERR_CUDA;
+}
+
+int swg_get_device_error(void *stream)
+{
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SWG_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_err_word, sizeof(int)) != cudaSuccess) return SWG_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_err_word, &zero, sizeof(int)) != cudaSuccess) return SWG_ERR_CUDA;
+        int dev = 0;
+        cudaGetDevice(&dev);
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_dev.find(dev);
+        if (it != g_dev.end())
+            for (auto &kv : it->second.ws)
+                if (kv.second.base) cudaMemset(kv.second.base, 0, kv.second.ticket_bytes);
+        return v;
+    }
+    return SWG_OK;
+}
+
+void swg_shutdown(void)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    int cur = 0;
+    const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+    for (auto &dv : g_dev) {
+        bool any = false;
+        for (auto &kv : dv.second.ws) any = any || kv.second.base != nullptr;
+        if (!any) continue;
+        if (cudaSetDevice(dv.first) != cudaSuccess) continue;
+        for (auto &kv : dv.second.ws)
+            if (kv.second.base) cudaFree(kv.second.base);
+        dv.second.ws.clear();
+    }
+    if (have_cur) cudaSetDevice(cur);
+}
+
+}  // extern "C"

@@ -1,0 +1,543 @@
+// tc_gemm.cuh — persistent, warp-specialised tcgen05 GEMM for sm_103a.
+//
+// One CTA per SM walks a static list of output tiles (BM x BN, BM = 128).
+// Roles inside a CTA (192 threads):
+//   warp 0, lane 0 : TMA producer.  For every 64-wide K block it waits for a
+//                    free shared-memory stage, arms the stage's "full" barrier
+//                    with the byte count and issues the tile loads of op(A)
+//                    and op(B) (128-byte swizzle; the tensor map's box and the
+//                    operand's major-ness realise op = N / T without copies).
+//   warp 1         : allocates tensor memory (TMEM); lane 0 issues
+//                    tcgen05.mma (M=128, N=BN, K=16, FP32 accumulate) into one
+//                    of two TMEM accumulators and commits each stage back to
+//                    its "empty" barrier, each finished tile to "acc_full".
+//   warps 2..5     : epilogue.  Each thread owns one accumulator row (TMEM
+//                    lane), reads it 32 columns at a time with tcgen05.ld and
+//                    applies the fused epilogue:
+//                      EPI_STORE  D = alpha*acc + beta*C, cast, 16-byte stores;
+//                      EPI_SWIGLU Y = SiLU(acc[2j]) * acc[2j+1] per column pair;
+//                      EPI_SPLITK FP32 partial to the workspace, then the last
+//                                 arriving CTA of the tile sums all partials in
+//                                 split order and stores alpha*sum + beta*C.
+// The double TMEM accumulator lets the epilogue of tile t overlap the main
+// loop of tile t+1.
+//
+// Every barrier wait is bounded (about two seconds): on expiry the thread
+// records SWG_ERR_DEVICE_TIMEOUT in the error word, raises a CTA-wide abort
+// flag that makes every other role leave its loop, the producer waits (again
+// bounded) for its own loads in flight, the MMA thread for its own MMAs, and
+// the CTA frees its TMEM and exits.
+//
+// Method sources: the GEMM statement of "GEMM o Coração Matemático" §1; the
+// tiling, multi-buffering, split-K and epilogue fusion of
+// "为什么 GEMM 是 CUDA 的必修课" (多级分块, 关键技术 items 3, 5, 6); the
+// interleaved-weight SwiGLU epilogue of "Sobreposição de Ativação em Nível de
+// Tile para Inferência Eficiente de LLM", Metodologia, Kernel-2.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace swg {
+
+enum EpiKind { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SPLITK = 2 };
+enum OutKind { OUT_BF16 = 0, OUT_F16 = 1, OUT_F32 = 2 };
+
+constexpr int BM = 128;
+constexpr int BK = 64;               // 64 x 16-bit = one 128-byte swizzle row
+constexpr int UMMA_K = 16;           // K of one kind::f16 MMA
+constexpr int NUM_THREADS = 192;
+constexpr int NUM_EPI_THREADS = 128;
+constexpr int EPI_WARP0 = 2;
+constexpr int ERR_TIMEOUT = 6;       // == SWG_ERR_DEVICE_TIMEOUT
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+
+struct TileParams {
+    int M, N, K;                 // N is the 2N-space width for SwiGLU
+    int m_blocks, n_blocks, k_blocks;
+    int tiles;                   // m_blocks * n_blocks
+    int splits;                  // K ranges per tile (1 = no split)
+    int kb_per_split;            // K blocks per range (last may be shorter)
+    int units;                   // tiles * splits
+    int group_m;                 // raster: m-blocks per group
+    uint32_t idesc;              // tcgen05 instruction descriptor
+    int a_mn_major;              // op(A) stored M-contiguous (transA = T)
+    int b_mn_major;              // op(B) stored N-contiguous (transB = N)
+    float alpha, beta;
+    void *D;                     // output (also C when beta != 0)
+    long long ldd;
+    int out_kind;                // OutKind
+    float *ws;                   // split-K partials [splits][M][ld_ws]
+    long long ld_ws;
+    int *tickets;                // split-K arrival counters, one per tile
+    int *err;                    // device error word
+};
+
+template <int BN>
+struct Cfg {
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES_RAW = (192 * 1024) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int TMEM_COLS = (2 * BN) <= 32 ? 32 : (2 * BN) <= 64 ? 64
+                                   : (2 * BN) <= 128 ? 128 : (2 * BN) <= 256 ? 256 : 512;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 64;
+    static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64, 128, 192 or 256");
+};
+
+// Tile coordinates of work unit u (grouped raster: walk GROUP m-blocks down a
+// column of tiles before moving right, so concurrently running CTAs share A
+// and B panels in L2).
+__device__ __forceinline__ void unit_coords(const TileParams &p, int u, int &mb, int &nb,
+                                            int &split, int &tile)
+{
+    split = u / p.tiles;
+    tile = u - split * p.tiles;
+    const int per_group = p.group_m * p.n_blocks;
+    const int group = tile / per_group;
+    const int first_m = group * p.group_m;
+    int gm = p.m_blocks - first_m;
+    gm = gm < p.group_m ? gm : p.group_m;
+    const int local = tile - group * per_group;
+    mb = first_m + local % gm;
+    nb = local / gm;
+}
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                             int *err, bool honour_abort = true)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 31) == 0) {
+            if (honour_abort && *abort_flag) return false;
+            if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+                *abort_flag = 1;
+                atomicCAS(err, 0, ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading
+// and stride byte offsets (all >> 4), version 1 at bit 46, 128-byte swizzle
+// (layout type 2) at bits 61-63.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ float silu_f32(float x)
+{
+    return x / (1.0f + __expf(-x));
+}
+
+__device__ __forceinline__ uint32_t pack2(float a, float b, int out_kind)
+{
+    if (out_kind == OUT_F16) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ float load_out(const void *base, long long idx, int out_kind)
+{
+    if (out_kind == OUT_F32) return reinterpret_cast<const float *>(base)[idx];
+    if (out_kind == OUT_F16) return __half2float(reinterpret_cast<const __half *>(base)[idx]);
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[idx]);
+}
+
+__device__ __forceinline__ void store_out(void *base, long long idx, float v, int out_kind)
+{
+    if (out_kind == OUT_F32)
+        reinterpret_cast<float *>(base)[idx] = v;
+    else if (out_kind == OUT_F16)
+        reinterpret_cast<__half *>(base)[idx] = __float2half_rn(v);
+    else
+        reinterpret_cast<__nv_bfloat16 *>(base)[idx] = __float2bfloat16_rn(v);
+}
+
+// alpha*acc + beta*C for `cnt` (<= 32) consecutive outputs of one row,
+// starting at element offset `off` of D.  `full` = all 32 in range and the
+// row chunk is 16-byte aligned (guaranteed by the host's alignment rules).
+__device__ __forceinline__ void store_row_chunk(const TileParams &p, long long off, const float *acc,
+                                                int cnt)
+{
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = p.alpha * acc[j];
+    const bool full = cnt == 32;
+    if (p.beta != 0.0f) {
+        if (full && p.out_kind != OUT_F32) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                reinterpret_cast<const uint16_t *>(p.D) + off);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint4 w = src[q];
+                uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    float lo, hi;
+                    if (p.out_kind == OUT_F16) {
+                        __half2 c2 = *reinterpret_cast<__half2 *>(&ww[h]);
+                        lo = __low2float(c2);
+                        hi = __high2float(c2);
+                    } else {
+                        __nv_bfloat162 c2 = *reinterpret_cast<__nv_bfloat162 *>(&ww[h]);
+                        lo = __low2float(c2);
+                        hi = __high2float(c2);
+                    }
+                    v[q * 8 + h * 2] += p.beta * lo;
+                    v[q * 8 + h * 2 + 1] += p.beta * hi;
+                }
+            }
+        } else if (full) {
+            const float4 *src = reinterpret_cast<const float4 *>(
+                reinterpret_cast<const float *>(p.D) + off);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                float4 c4 = src[q];
+                v[q * 4 + 0] += p.beta * c4.x;
+                v[q * 4 + 1] += p.beta * c4.y;
+                v[q * 4 + 2] += p.beta * c4.z;
+                v[q * 4 + 3] += p.beta * c4.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (j < cnt) v[j] += p.beta * load_out(p.D, off + j, p.out_kind);
+        }
+    }
+    if (full && p.out_kind != OUT_F32) {
+        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.D) + off);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            w.x = pack2(v[q * 8 + 0], v[q * 8 + 1], p.out_kind);
+            w.y = pack2(v[q * 8 + 2], v[q * 8 + 3], p.out_kind);
+            w.z = pack2(v[q * 8 + 4], v[q * 8 + 5], p.out_kind);
+            w.w = pack2(v[q * 8 + 6], v[q * 8 + 7], p.out_kind);
+            dst[q] = w;
+        }
+    } else if (full) {
+        float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.D) + off);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(v[q * 4], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j < cnt) store_out(p.D, off + j, v[j], p.out_kind);
+    }
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const TileParams p)
+{
+    using C = Cfg<BN>;
+    constexpr int S = C::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    // 128-byte swizzled stages need 1024-byte alignment.
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + S * C::A_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + S * C::B_BYTES);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + S;
+    uint64_t *acc_full = bars + 2 * S;
+    uint64_t *acc_empty = bars + 2 * S + 2;
+    uint64_t *mma_done = bars + 2 * S + 4;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + C::NUM_BARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    volatile int *last_flag = reinterpret_cast<volatile int *>(tmem_holder + 2);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&acc_full[b]), 1);
+            mbar_init(smem_u32(&acc_empty[b]), NUM_EPI_THREADS);
+        }
+        mbar_init(smem_u32(mma_done), 1);
+        *abort_flag = 0;
+        *last_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed = 0, armed_parity = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+                int mb, nb, split, tile;
+                unit_coords(p, u, mb, nb, split, tile);
+                const int kb0 = split * p.kb_per_split;
+                int kb1 = kb0 + p.kb_per_split;
+                kb1 = kb1 < p.k_blocks ? kb1 : p.k_blocks;
+                const int m0 = mb * BM, n0 = nb * BN;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!wait_bounded(smem_u32(&empty[stage]), phase ^ 1, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&full[stage]);
+                    mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                    armed |= 1u << stage;
+                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    const uint32_t a_dst = smem_u32(sA + stage * C::A_BYTES);
+                    const uint32_t b_dst = smem_u32(sB + stage * C::B_BYTES);
+                    const int k0 = kb * BK;
+                    if (!p.a_mn_major) {
+                        tma_load_2d(a_dst, &tmA, fb, k0, m0);               // box {64 K, 128 M}
+                    } else {
+                        tma_load_2d(a_dst, &tmA, fb, m0, k0);               // box {64 M, 64 K}
+                        tma_load_2d(a_dst + 8192, &tmA, fb, m0 + 64, k0);
+                    }
+                    if (!p.b_mn_major) {
+                        tma_load_2d(b_dst, &tmB, fb, k0, n0);               // box {64 K, BN N}
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < BN / 64; ++c)                   // box {64 N, 64 K}
+                            tma_load_2d(b_dst + c * 8192, &tmB, fb, n0 + c * 64, k0);
+                    }
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            // Never leave with loads in flight into this CTA's shared memory.
+            for (int s = 0; s < S; ++s)
+                if (armed & (1u << s))
+                    wait_bounded(smem_u32(&full[s]), (armed_parity >> s) & 1, abort_flag, p.err,
+                                 false);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            // K-major operand: next K=16 slice is 32 bytes further in the
+            // swizzled row; MN-major: two 8-row K groups (2 x 1024 bytes) further.
+            const uint32_t a_kstep = p.a_mn_major ? 2048u : 32u;
+            const uint32_t b_kstep = p.b_mn_major ? 2048u : 32u;
+            const uint32_t a_lbo = p.a_mn_major ? 8192u : 16u;
+            const uint32_t b_lbo = p.b_mn_major ? 8192u : 16u;
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int t = 0;
+            for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++t) {
+                int mb, nb, split, tile;
+                unit_coords(p, u, mb, nb, split, tile);
+                const int kb0 = split * p.kb_per_split;
+                int kb1 = kb0 + p.kb_per_split;
+                kb1 = kb1 < p.k_blocks ? kb1 : p.k_blocks;
+                const int acc = t & 1;
+                const uint32_t acc_phase = (t >> 1) & 1;
+                if (!wait_bounded(smem_u32(&acc_empty[acc]), acc_phase ^ 1, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!wait_bounded(smem_u32(&full[stage]), phase, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(sA + stage * C::A_BYTES);
+                    const uint32_t b_base = smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        const uint64_t ad = smem_desc(a_base + kk * a_kstep, a_lbo, 1024);
+                        const uint64_t bd = smem_desc(b_base + kk * b_kstep, b_lbo, 1024);
+                        tc_mma_f16(d_tmem, ad, bd, p.idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(smem_u32(&empty[stage]));
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(smem_u32(&acc_full[acc]));
+            }
+            // Never free TMEM under a running MMA.
+            tc_commit(smem_u32(mma_done));
+            wait_bounded(smem_u32(mma_done), 0, abort_flag, p.err, false);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                 // TMEM lane quarter of this warp
+        const int row = q * 32 + lane;
+        const int et = threadIdx.x - EPI_WARP0 * 32;
+        int t = 0;
+        for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++t) {
+            int mb, nb, split, tile;
+            unit_coords(p, u, mb, nb, split, tile);
+            const int acc = t & 1;
+            const uint32_t acc_phase = (t >> 1) & 1;
+            bool ok = wait_bounded(smem_u32(&acc_full[acc]), acc_phase, abort_flag, p.err);
+            ok = __all_sync(0xffffffffu, ok);
+            if (EPI == EPI_SPLITK) ok = named_bar_and(1, NUM_EPI_THREADS, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+            const int m = mb * BM + row;
+            const bool row_ok = m < p.M;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32cols(t_row + c * 32, r);
+                tmem_ld_wait();
+                const int n = nb * BN + c * 32;
+                if (!row_ok || n >= p.N) continue;
+                const int cnt = (p.N - n) < 32 ? (p.N - n) : 32;
+                if (EPI == EPI_STORE) {
+                    float a[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) a[j] = __uint_as_float(r[j]);
+                    store_row_chunk(p, (long long)m * p.ldd + n, a, cnt);
+                } else if (EPI == EPI_SWIGLU) {
+                    // Column pair (2j, 2j+1) of the 2N-space = (Gate_j, Up_j).
+                    const long long off = (long long)m * p.ldd + n / 2;
+                    uint32_t w[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float y0 = silu_f32(__uint_as_float(r[4 * j])) *
+                                         __uint_as_float(r[4 * j + 1]);
+                        const float y1 = silu_f32(__uint_as_float(r[4 * j + 2])) *
+                                         __uint_as_float(r[4 * j + 3]);
+                        w[j] = pack2(y0, y1, OUT_BF16);
+                    }
+                    if (cnt == 32) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(
+                            reinterpret_cast<__nv_bfloat16 *>(p.D) + off);
+                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    } else {
+                        __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.D) + off;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            if (2 * j < cnt) {
+                                const float y = silu_f32(__uint_as_float(r[2 * j])) *
+                                                __uint_as_float(r[2 * j + 1]);
+                                dst[j] = __float2bfloat16_rn(y);
+                            }
+                        }
+                    }
+                } else {
+                    float *dst = p.ws + ((long long)split * p.M + m) * p.ld_ws + n;
+                    if (cnt == 32) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            reinterpret_cast<float4 *>(dst)[j] =
+                                make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                            __uint_as_float(r[4 * j + 2]),
+                                            __uint_as_float(r[4 * j + 3]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < cnt) dst[j] = __uint_as_float(r[j]);
+                    }
+                }
+            }
+            // Accumulator drained: hand it back to the MMA warp.
+            tc_fence_before();
+            mbar_arrive(smem_u32(&acc_empty[acc]));
+
+            if (EPI == EPI_SPLITK) {
+                // Publish this split's partial; the last of p.splits arrivals
+                // reduces all of them in split order 0..splits-1.
+                __threadfence();
+                named_bar_sync(1, NUM_EPI_THREADS);
+                if (et == 0) {
+                    const int old = atomicAdd(&p.tickets[tile], 1);
+                    const int last = old == p.splits - 1;
+                    if (last) p.tickets[tile] = 0;   // ready for the next call
+                    *last_flag = last;
+                }
+                named_bar_sync(1, NUM_EPI_THREADS);
+                if (*last_flag) {
+                    __threadfence();
+                    const int m0 = mb * BM, n0 = nb * BN;
+                    const int rows = (p.M - m0) < BM ? (p.M - m0) : BM;
+                    const int cols = (p.N - n0) < BN ? (p.N - n0) : BN;
+                    const int quads = (cols + 3) / 4;
+                    for (int idx = et; idx < rows * quads; idx += NUM_EPI_THREADS) {
+                        const int rr = idx / quads;
+                        const int cc = (idx - rr * quads) * 4;
+                        const int mm = m0 + rr, nn = n0 + cc;
+                        const int cnt = (cols - cc) < 4 ? (cols - cc) : 4;
+                        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+                        for (int s = 0; s < p.splits; ++s) {
+                            const float *src = p.ws + ((long long)s * p.M + mm) * p.ld_ws + nn;
+                            if (cnt == 4) {
+                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
+                                s4[0] += v.x;
+                                s4[1] += v.y;
+                                s4[2] += v.z;
+                                s4[3] += v.w;
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 4; ++j)
+                                    if (j < cnt) s4[j] += __ldcg(src + j);
+                            }
+                        }
+                        const long long off = (long long)mm * p.ldd + nn;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            if (j < cnt) {
+                                float v = p.alpha * s4[j];
+                                if (p.beta != 0.0f)
+                                    v += p.beta * load_out(p.D, off + j, p.out_kind);
+                                store_out(p.D, off + j, v, p.out_kind);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+}  // namespace swg

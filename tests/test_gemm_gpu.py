@@ -1,0 +1,198 @@
+"""GEMM parity: the CUDA path (through the C ABI) against the FP64 oracle.
+
+D = alpha op(A) op(B) + beta C ("GEMM o Coração Matemático", §1), all four
+op combinations, every storage type, ragged tails, padded row strides, the
+beta = 0 / K = 0 special cases, the 256^3 fp16 case in full, and sampled
+rows of the square 4096 / 8192 bf16 cases in the launch configuration the
+benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import swiglu_mlp_gb300 as swg
+import synth
+from helpers import check_f32, check_half, padded, round_up, to_f64
+
+pytestmark = pytest.mark.gpu
+
+DT = {  # code -> (input torch dtype, output torch dtype, oracle in, oracle out)
+    swg.F16_F32OUT: (torch.float16, torch.float32, "f16", "f32"),
+    swg.BF16: (torch.bfloat16, torch.bfloat16, "bf16", "bf16"),
+    swg.F16: (torch.float16, torch.float16, "f16", "f16"),
+    swg.BF16_F32OUT: (torch.bfloat16, torch.float32, "bf16", "f32"),
+}
+
+
+def run_case(M, N, K, tA, tB, code, alpha, beta, seed, pad=(0, 0, 0), c_fill=None,
+             split_k=None, rows=None):
+    """Runs one GEMM on the GPU and on the oracle; returns (y, yhat)."""
+    tin, tout, oin, oout = DT[code]
+    g = synth.generator(seed)
+    A = synth.normal(synth.stored_shape(tA, M, K), g, dtype=tin)
+    B = synth.normal(synth.stored_shape(tB, K, N), g, dtype=tin)
+    C = synth.normal((M, N), g, dtype=tout)
+    esz_out = 4 if tout == torch.float32 else 2
+    lda = round_up(A.shape[1], 8) + pad[0]
+    ldb = round_up(B.shape[1], 8) + pad[1]
+    ldc = round_up(N, 16 // esz_out) + pad[2]
+    Ap, Bp = padded(A, lda, 3.0), padded(B, ldb, 3.0)
+    Cp = padded(C, ldc, 5.0)
+    if c_fill is not None:
+        Cp.fill_(c_fill)
+    Cd = Cp.cuda()
+    Ad, Bd = Ap.cuda(), Bp.cuda()
+    if split_k is None:
+        swg.gemm(tA, tB, M, N, K, alpha, Ad, lda, Bd, ldb, beta, Cd, ldc, code)
+    else:
+        swg.gemm_ex(tA, tB, M, N, K, alpha, Ad, lda, Bd, ldb, beta, Cd, ldc, code, split_k)
+    assert swg.get_device_error() == 0
+    out = Cd.cpu()
+    # the padding columns of C must be untouched
+    if ldc > N:
+        assert torch.equal(out[:, N:], Cp[:, N:])
+    y = to_f64(out[:, :N])
+    yhat = oracle.gemm(tA, tB, M, N, K, alpha, Ap, lda, Bp, ldb, beta, Cp, ldc,
+                       in_type=oin, c_type=oout, rows=rows)
+    if rows is not None:
+        y = y[np.asarray(rows)]
+    return y, yhat
+
+
+def check(y, yhat, code, K, what):
+    if DT[code][1] == torch.float32:
+        return check_f32(y, yhat, K, what)
+    return check_half(y, yhat, what)
+
+
+def test_config_f16_256_cubed_full():
+    """FP16 in, FP32 out: C = 1.5 A B + 0.5 C, 256^3, U(-1,1) inputs, seed 0."""
+    M = N = K = 256
+    A, B, C = synth.gemm_f16_small(seed=0)
+    Ad, Bd, Cd = A.cuda(), B.cuda(), C.cuda()
+    swg.gemm(0, 0, M, N, K, 1.5, Ad, K, Bd, N, 0.5, Cd, N, swg.F16_F32OUT)
+    assert swg.get_device_error() == 0
+    yhat = oracle.gemm(0, 0, M, N, K, 1.5, A, K, B, N, 0.5, C, N, in_type="f16", c_type="f32")
+    check_f32(to_f64(Cd), yhat, K, "f16 256^3")
+
+
+@pytest.mark.parametrize("tA", [0, 1])
+@pytest.mark.parametrize("tB", [0, 1])
+@pytest.mark.parametrize("shape", [(128, 256, 64), (256, 512, 320), (300, 520, 200),
+                                   (129, 257, 72), (1, 8, 8), (7, 13, 5), (640, 384, 1000)])
+def test_bf16_all_ops(tA, tB, shape):
+    M, N, K = shape
+    y, yhat = run_case(M, N, K, tA, tB, swg.BF16, 1.0, 0.0, seed=100 + M + N + K + tA * 2 + tB)
+    check_half(y, yhat, f"bf16 {shape} tA={tA} tB={tB}")
+
+
+@pytest.mark.parametrize("code", [swg.F16_F32OUT, swg.F16, swg.BF16_F32OUT])
+@pytest.mark.parametrize("tA,tB", [(0, 0), (1, 1), (0, 1), (1, 0)])
+def test_other_dtypes(code, tA, tB):
+    M, N, K = 200, 264, 136
+    y, yhat = run_case(M, N, K, tA, tB, code, 0.75, 0.0, seed=7 + code * 4 + tA * 2 + tB)
+    check(y, yhat, code, K, f"code={code} tA={tA} tB={tB}")
+
+
+@pytest.mark.parametrize("code", [swg.BF16, swg.F16_F32OUT, swg.F16])
+def test_beta_nonzero_and_padding(code):
+    M, N, K = 190, 300, 256
+    y, yhat = run_case(M, N, K, 0, 0, code, 1.5, -0.5, seed=31, pad=(8, 16, 8))
+    check(y, yhat, code, K, f"beta code={code}")
+
+
+def test_beta_zero_ignores_nan_c():
+    M, N, K = 160, 272, 96
+    y, yhat = run_case(M, N, K, 0, 1, swg.BF16, 1.0, 0.0, seed=5, c_fill=float("nan"))
+    check_half(y, yhat, "beta=0 NaN C")
+
+
+@pytest.mark.parametrize("code", [swg.BF16, swg.F16_F32OUT])
+def test_k_zero_scales_c(code):
+    M, N = 70, 40
+    for beta in (0.0, 2.0):
+        y, yhat = run_case(M, N, 0, 0, 0, code, 1.0, beta, seed=9)
+        check(y, yhat, code, 1, f"K=0 beta={beta}")
+
+
+def test_m_or_n_zero_is_noop():
+    C = torch.full((4, 8), 7.0, dtype=torch.bfloat16, device="cuda")
+    before = swg.launch_count()
+    swg.gemm(0, 0, 0, 8, 16, 1.0, 0, 16, 0, 8, 0.0, C, 8, swg.BF16)
+    swg.gemm(0, 0, 4, 0, 16, 1.0, 0, 16, 0, 8, 0.0, C, 8, swg.BF16)
+    assert swg.launch_count() == before
+    assert torch.all(C == 7.0)
+
+
+def test_identity_product_exact():
+    """A I = A exactly: every output is one bf16 value times 1."""
+    M, K = 300, 256
+    g = synth.generator(41)
+    A = synth.normal((M, K), g).cuda()
+    eye = torch.eye(K, dtype=torch.bfloat16, device="cuda")
+    D = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    swg.gemm(0, 0, M, K, K, 1.0, A, K, eye, K, 0.0, D, K, swg.BF16)
+    torch.cuda.synchronize()
+    assert torch.equal(D, A)
+
+
+def test_transpose_identity_gpu():
+    """(A B)^T = B^T A^T: computing D^T with both operands transposed gives the
+    transpose of D (to within rounding of the same FP32 sums)."""
+    M, N, K = 256, 384, 512
+    A, B, _ = synth.gemm_bf16(M, N, K, seed=43)
+    Ad, Bd = A.cuda(), B.cuda()
+    D = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    Dt = torch.empty((N, M), dtype=torch.float32, device="cuda")
+    swg.gemm(0, 0, M, N, K, 1.0, Ad, K, Bd, N, 0.0, D, N, swg.BF16_F32OUT)
+    swg.gemm(1, 1, N, M, K, 1.0, Bd, N, Ad, K, 0.0, Dt, M, swg.BF16_F32OUT)
+    torch.cuda.synchronize()
+    yhat = oracle.gemm(0, 0, M, N, K, 1.0, A, K, B, N, 0.0)
+    check_f32(to_f64(D), yhat, K, "D")
+    check_f32(to_f64(Dt).T, yhat, K, "D^T")
+
+
+def test_alpha_linearity_power_of_two_exact():
+    M, N, K = 256, 256, 192
+    A, B, _ = synth.gemm_bf16(M, N, K, seed=47)
+    Ad, Bd = A.cuda(), B.cuda()
+    D1 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    D4 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    swg.gemm(0, 0, M, N, K, 1.0, Ad, K, Bd, N, 0.0, D1, N, swg.BF16_F32OUT)
+    swg.gemm(0, 0, M, N, K, 4.0, Ad, K, Bd, N, 0.0, D4, N, swg.BF16_F32OUT)
+    torch.cuda.synchronize()
+    assert torch.equal(D4, 4.0 * D1)
+
+
+def test_beta_one_accumulates_twice():
+    """gemm with beta = 1 run twice over the same C adds A B twice."""
+    M, N, K = 128, 256, 128
+    A, B, _ = synth.gemm_bf16(M, N, K, seed=53, dist="ints")
+    Ad, Bd = A.cuda(), B.cuda()
+    C = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    swg.gemm(0, 0, M, N, K, 1.0, Ad, K, Bd, N, 1.0, C, N, swg.BF16_F32OUT)
+    swg.gemm(0, 0, M, N, K, 1.0, Ad, K, Bd, N, 1.0, C, N, swg.BF16_F32OUT)
+    torch.cuda.synchronize()
+    AB = oracle.gemm(0, 0, M, N, K, 1.0, A, K, B, N, 0.0)
+    assert np.array_equal(to_f64(C), 2 * AB)   # small integers: exact
+
+
+@pytest.mark.parametrize("size", [4096, 8192])
+@pytest.mark.parametrize("tA", [0, 1])
+@pytest.mark.parametrize("tB", [0, 1])
+def test_square_bf16_sampled(size, tA, tB):
+    """The benchmark's square bf16 cases, alpha = 1, beta = 0: every output
+    finite, sampled rows (first, last, tile edges, random) equal to the
+    oracle within tolerance."""
+    M = N = K = size
+    A, B, _ = synth.gemm_bf16(M, N, K, tA, tB, seed=1)
+    Ad, Bd = A.cuda(), B.cuda()
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    swg.gemm(tA, tB, M, N, K, 1.0, Ad, A.shape[1], Bd, B.shape[1], 0.0, D, N, swg.BF16)
+    assert swg.get_device_error() == 0
+    assert bool(torch.isfinite(D).all())
+    rng = np.random.default_rng(size + tA * 2 + tB)
+    rows = sorted({0, 127, 128, M - 1, *rng.integers(0, M, 4).tolist()})
+    yhat = oracle.gemm(tA, tB, M, N, K, 1.0, A, A.shape[1], B, B.shape[1], 0.0, rows=rows)
+    check_half(to_f64(D)[rows], yhat, f"{size}^3 tA={tA} tB={tB}")

@@ -1,0 +1,99 @@
+"""Fused SwiGLU parity: Y = SiLU(A W1) (.) (A W2) as one GEMM over the
+interleaved W_fused with the pair-multiply epilogue ("Sobreposição de Ativação
+em Nível de Tile para Inferência Eficiente de LLM", Metodologia, Kernel-2),
+against the oracle computed from SEPARATE W1 and W2.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import swiglu_mlp_gb300 as swg
+import synth
+from helpers import check_half, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _fused_weight(W1, W2, K, N):
+    """W_fused from the oracle's interleave (not from the CUDA path)."""
+    Wf = oracle.interleave(W1, W2, K, N)
+    return torch.from_numpy(Wf.view(np.int16)).view(torch.bfloat16)
+
+
+def run(M, K, N, seed, rows=None, w_std=0.02):
+    A, W1, W2 = synth.swiglu(M, K, N, seed=seed, w_std=w_std)
+    Wf = _fused_weight(W1, W2, K, N)
+    Y = torch.full((M, N), 9.0, dtype=torch.bfloat16, device="cuda")
+    swg.swiglu_mlp(A.cuda(), Wf.cuda(), Y, M, N, K)
+    assert swg.get_device_error() == 0
+    yhat = oracle.swiglu(A, W1, W2, M, N, K, rows=rows)
+    y = to_f64(Y)
+    if rows is not None:
+        y = y[np.asarray(rows)]
+    return y, yhat
+
+
+@pytest.mark.parametrize("M,K,N", [(128, 64, 128), (1, 8, 8), (100, 200, 48), (300, 136, 520),
+                                   (129, 72, 264), (256, 512, 1024)])
+def test_swiglu_small_shapes(M, K, N):
+    y, yhat = run(M, K, N, seed=M + K + N, w_std=0.1)
+    check_half(y, yhat, f"swiglu {M}x{K}x{N}")
+
+
+@pytest.mark.parametrize("M", [128, 512, 2048])
+def test_swiglu_small_model_shape(M):
+    """A [M x 896] ~ N(0,1), W1, W2 [896 x 4864] ~ N(0, 0.02)."""
+    rows = None if M == 128 else sorted({0, 127, 128, M - 1, M // 3})
+    y, yhat = run(M, 896, 4864, seed=3, rows=rows)
+    check_half(y, yhat, f"small-model M={M}")
+
+
+@pytest.mark.parametrize("M", [512, 2048, 8192])
+def test_swiglu_8b_shape_sampled(M):
+    """A [M x 4096] ~ N(0,1), W1, W2 [4096 x 14336] ~ N(0, 0.02); sampled rows."""
+    y, yhat = run(M, 4096, 14336, seed=3, rows=[0, 129, M - 1])
+    check_half(y, yhat, f"8B M={M}")
+
+
+def test_interleave_kernel_bitwise():
+    K, N = 96, 4864
+    _, W1, W2 = synth.swiglu(1, K, N, seed=77)
+    Wf = swg.interleave_weights(W1.cuda(), W2.cuda())
+    torch.cuda.synchronize()
+    want = oracle.interleave(W1, W2, K, N)
+    assert np.array_equal(Wf.cpu().view(torch.int16).numpy().view(np.uint16), want)
+
+
+def test_fused_equals_two_gemms_plus_elementwise():
+    """The fused kernel against the unfused data flow: two FP32-output GEMMs
+    (Gate, Up) from the same library, then SiLU(Gate) * Up in FP64 on the
+    host."""
+    M, K, N = 384, 896, 640
+    A, W1, W2 = synth.swiglu(M, K, N, seed=88, w_std=0.05)
+    Ad = A.cuda()
+    G = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    U = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    swg.gemm(0, 0, M, N, K, 1.0, Ad, K, W1.cuda(), N, 0.0, G, N, swg.BF16_F32OUT)
+    swg.gemm(0, 0, M, N, K, 1.0, Ad, K, W2.cuda(), N, 0.0, U, N, swg.BF16_F32OUT)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    swg.swiglu_mlp(Ad, _fused_weight(W1, W2, K, N).cuda(), Y, M, N, K)
+    torch.cuda.synchronize()
+    g, u = to_f64(G), to_f64(U)
+    unfused = g / (1.0 + np.exp(-g)) * u
+    check_half(to_f64(Y), unfused, "fused vs two GEMMs")
+
+
+def test_swiglu_k_zero_gives_zero():
+    M, N = 64, 64
+    Y = torch.full((M, N), 3.0, dtype=torch.bfloat16, device="cuda")
+    swg.swiglu_mlp(0, 0, Y, M, N, 0)
+    torch.cuda.synchronize()
+    assert torch.all(Y == 0)
+
+
+def test_swiglu_large_magnitudes_finite():
+    """Gate values far into both SiLU tails: outputs stay finite and match."""
+    M, K, N = 128, 64, 256
+    y, yhat = run(M, K, N, seed=91, w_std=8.0)
+    check_half(y, yhat, "large gate magnitudes")
