@@ -1,0 +1,517 @@
+"""Benchmark: GEMM / fused-SwiGLU TFLOPS on one GB300 against the dense bf16
+peak, and skinny split-K HBM GB/s.
+
+One STEP = the bf16 GEMM D = A B at M = N = K = 8192 for all four
+(transA, transB) combinations (alpha = 1, beta = 0), launched through the C ABI
+on inputs already resident in HBM.  ``value`` = 4 * 2 * 8192^3 * steps * ranks
+/ (max-over-ranks time) in TFLOP/s.  Each rank runs its own replica (the path
+has no exchange step), so scaling is weak.
+
+The same JSON line carries, measured in the same run:
+  roofline      the tcgen05 GEMM kernel's achieved TFLOP/s (CUDA events on the
+                launching stream) against the measured dense bf16 peak;
+  e2e           the same metric with A, B copied from pinned host memory and
+                the four D read back inside the timed region;
+  cpu_baseline  the FP64 oracle on the host cores over a bounded row sample;
+  components    fused SwiGLU (small-model and 8B shapes) and skinny split-K
+                timings with an L2 flush between repetitions;
+  clocks        SM clocks and throttle reasons sampled during the timed region.
+
+``--impl reference`` times the FP64 oracle instead (rank 0 only), as the
+reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+SIZE = 8192
+TRANS = [(0, 0), (0, 1), (1, 0), (1, 1)]
+FLOP_PER_GEMM = 2.0 * SIZE ** 3
+METRIC = "GEMM and fused-SwiGLU TFLOPS at 1 GB300 vs dense BF16 peak; skinny HBM GB/s"
+WORKLOAD = ("bf16 GEMM D = A B, M = N = K = 8192, all four transA/transB combinations "
+            "per step, alpha = 1, beta = 0")
+KERNEL_NAME = "tc_gemm_kernel<256, EPI_STORE>"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+def kernel_source_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "swiglu_mlp_gb300", "csrc")
+    for name in ("tc_gemm.cuh", "ptx.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(profile_name: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (matching digest); otherwise None."""
+    path = os.path.join(ROOT, "profiles", profile_name)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    dig = re.search(r"kernel_source_digest:\s*([0-9a-f]+)", text)
+    tb = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not dig or not tb or dig.group(1) != kernel_source_digest():
+        return None
+    return float(tb.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons (every 200 ms)."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+        sm = [num(r[1]) for r in rows]
+        sm_max = max(num(r[2]) for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower().startswith("active")})
+        load = [s for s in sm if not math.isnan(s)]
+        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": sm_max,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(num(r[3]) for r in rows)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_group(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def aggregate(elapsed_s: float, units: float, dist_mod, device=None):
+    """Whole-job view: max elapsed time over ranks, sum of units over ranks."""
+    if dist_mod is None:
+        return elapsed_s, units
+    import torch
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    dist_mod.all_reduce(u, op=dist_mod.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ------------------------------------------------------------------ oracle timing
+
+def time_oracle_sample(rows: int, cols: int, trans=(0, 0), A=None, B=None):
+    """FP64 oracle on the host: the first `rows` x `cols` outputs of the 8192^3
+    GEMM.  Returns (seconds, flops, threads)."""
+    import oracle
+    import synth
+    if A is None:
+        A, B, _ = synth.gemm_bf16(SIZE, SIZE, SIZE, trans[0], trans[1], seed=1)
+    tA, tB = trans
+    t0 = time.perf_counter()
+    oracle.gemm(tA, tB, SIZE, SIZE, SIZE, 1.0, A, A.shape[1], B, B.shape[1], 0.0,
+                rows=list(range(rows)), cols=list(range(cols)))
+    dt = time.perf_counter() - t0
+    return dt, 2.0 * rows * cols * SIZE, min(oracle.num_cores(), rows)
+
+
+def cpu_baseline(target_s: float = 12.0, cols: int = 2048):
+    """Oracle throughput on a bounded sample sized to about target_s seconds."""
+    import synth
+    A, B, _ = synth.gemm_bf16(SIZE, SIZE, SIZE, 0, 0, seed=1)
+    dt, _, _ = time_oracle_sample(64, cols, A=A, B=B)
+    rows = int(max(64, min(SIZE, 64 * target_s / max(dt, 1e-3))))
+    rows = (rows // 64) * 64
+    dt, flops, cores = time_oracle_sample(rows, cols, A=A, B=B)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{rows} rows x {cols} columns of the op(A)=A, op(B)=B 8192^3 GEMM "
+                      f"(FP64, {dt:.1f} s)"}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_ours(args):
+    import torch
+
+    import swiglu_mlp_gb300 as swg
+    import synth
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_mod = init_group(world, "nccl")
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    swg.load()
+
+    A, B, _ = synth.gemm_bf16(SIZE, SIZE, SIZE, 0, 0, seed=1 + rank)
+    Ad, Bd = A.to(dev), B.to(dev)
+    Ds = [torch.empty((SIZE, SIZE), dtype=torch.bfloat16, device=dev) for _ in TRANS]
+
+    def step(events=None):
+        for i, (tA, tB) in enumerate(TRANS):
+            if events is not None:
+                events[i][0].record(stream)
+            swg.gemm(tA, tB, SIZE, SIZE, SIZE, 1.0, Ad, SIZE, Bd, SIZE, 0.0, Ds[i], SIZE,
+                     swg.BF16, stream=stream)
+            if events is not None:
+                events[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if swg.get_device_error(stream) != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    sampler = ClockSampler(local)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in TRANS] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if dist_mod:
+        dist_mod.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    launches0 = swg.launch_count()
+    t_start.record(stream)
+    for s in range(args.steps):
+        step(ev[s])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = swg.launch_count() - launches0
+    clocks = sampler.stop()
+    if dist_mod:
+        dist_mod.barrier()
+    if swg.get_device_error(stream) != 0:
+        raise RuntimeError("device error word set during the timed region")
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    launch_ms = [e0.elapsed_time(e1) for row in ev for (e0, e1) in row]
+    flops_local = FLOP_PER_GEMM * len(TRANS) * args.steps
+    elapsed_max, flops_all = aggregate(elapsed, flops_local, dist_mod, dev)
+    value = flops_all / elapsed_max / 1e12
+
+    # ---- end to end: pinned host inputs in, results out, inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, A, B, Ad, Bd, Ds, step, dist_mod, dev)
+
+    components = None
+    if rank == 0 and not args.no_components:
+        components = run_components(args, dev, stream)
+
+    if rank != 0:
+        return None
+    peaks, peak_src = load_peaks()
+    avg_launch_s = statistics.mean(launch_ms) / 1e3
+    achieved = FLOP_PER_GEMM / avg_launch_s / 1e12
+    peak = float(peaks["bf16_tflops"])
+    traffic = profiled_traffic("tc_gemm_bf16_8192.md")
+    out = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(elapsed_max * 1e3 / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: A, B ~ N(0,1) rounded to bf16, seeded (seed 1 + rank)",
+        "config": {"workload": WORKLOAD, "M": SIZE, "N": SIZE, "K": SIZE,
+                   "trans": [list(t) for t in TRANS], "alpha": 1.0, "beta": 0.0,
+                   "l2": "inputs larger than L2 (A + B = 256 MiB > 129 MB); no flush",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "kernel": KERNEL_NAME,
+                     "peak_source": f"{peak_src} dense bf16 burst (MEASURED_PEAKS.json)"
+                     if peak_src == "measured" else "fallback 1.9 PFLOP/s bf16 burst",
+                     "frac_of_sustained": round(achieved / float(peaks["bf16_tflops_sustained"]),
+                                                4),
+                     "algorithmic_flops_per_launch": FLOP_PER_GEMM,
+                     "avg_launch_ms": round(avg_launch_s * 1e3, 4)},
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if components is not None:
+        out["components"] = components
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return out
+
+
+def run_e2e(args, A, B, Ad, Bd, Ds, step, dist_mod, dev):
+    """Same step through the public API with host buffers: A, B copied in from
+    pinned memory and the four D copied out, all inside the timed region."""
+    import torch
+    Ah = A.pin_memory()
+    Bh = B.pin_memory()
+    Dh = [torch.empty((SIZE, SIZE), dtype=torch.bfloat16).pin_memory() for _ in TRANS]
+
+    def e2e_step():
+        Ad.copy_(Ah, non_blocking=True)
+        Bd.copy_(Bh, non_blocking=True)
+        step()
+        for i in range(len(TRANS)):
+            Dh[i].copy_(Ds[i], non_blocking=True)
+
+    for _ in range(max(1, min(args.warmup, 3))):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    n = max(1, min(args.steps, 10))
+    if dist_mod:
+        dist_mod.barrier()
+    t0 = time.perf_counter()
+    for _ in range(n):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    elapsed = time.perf_counter() - t0
+    e_max, flops = aggregate(elapsed, FLOP_PER_GEMM * len(TRANS) * n, dist_mod, dev)
+    return {"value": round(flops / e_max / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": (Ah.numel() + Bh.numel()) * 2,
+            "d2h_bytes_per_step": sum(d.numel() for d in Dh) * 2, "steps": n}
+
+
+def l2_flush(buf):
+    buf.zero_()
+
+
+def time_reps(fn, reps, dev, stream, flush_buf):
+    import torch
+    times = []
+    for _ in range(reps):
+        l2_flush(flush_buf)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        times.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    ms = sorted(a.elapsed_time(b) for a, b in times)
+    return statistics.median(ms), ms[0]
+
+
+def run_components(args, dev, stream):
+    """SwiGLU and skinny split-K timings (median of reps, L2 flushed before each)."""
+    import torch
+
+    import swiglu_mlp_gb300 as swg
+    import synth
+
+    peaks, _ = load_peaks()
+    bw = float(peaks["hbm_gbs"])
+    P = float(peaks["bf16_tflops"])
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    reps = args.component_reps
+    res = {}
+    for name, M, K, N in [("swiglu_small_M128", 128, 896, 4864),
+                          ("swiglu_small_M512", 512, 896, 4864),
+                          ("swiglu_small_M2048", 2048, 896, 4864),
+                          ("swiglu_8b_M512", 512, 4096, 14336),
+                          ("swiglu_8b_M2048", 2048, 4096, 14336),
+                          ("swiglu_8b_M8192", 8192, 4096, 14336)]:
+        A, W1, W2 = synth.swiglu(M, K, N, seed=3)
+        Ad = A.to(dev)
+        Wf = swg.interleave_weights(W1.to(dev), W2.to(dev), stream=stream)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        fn = lambda: swg.swiglu_mlp(Ad, Wf, Y, M, N, K, stream=stream)  # noqa: E731
+        for _ in range(3):
+            fn()
+        med, best = time_reps(fn, reps, dev, stream, flush)
+        flops = 2.0 * M * 2 * N * K
+        byts = (M * K + K * 2 * N + M * N) * 2
+        roof_s = max(flops / (P * 1e12), byts / (bw * 1e9))
+        res[name] = {"median_us": round(med * 1e3, 2), "tflops": round(flops / med / 1e9, 1),
+                     "gbs": round(byts / med / 1e6, 1),
+                     "roofline_frac": round(roof_s / (med / 1e3), 4),
+                     "bound": "tensor" if flops / (P * 1e12) > byts / (bw * 1e9) else "hbm"}
+        del Ad, Wf, Y
+    for M in (16, 32, 64):
+        N, K = 4096, 16384
+        A, B, C = synth.skinny(M)
+        Ad, Bd, C0 = A.to(dev), B.to(dev), C.to(dev)
+        Cd = C0.clone()
+
+        def fn():
+            swg.gemm(0, 0, M, N, K, 1.0, Ad, K, Bd, N, 1.0, Cd, N, swg.BF16, stream=stream)
+
+        for _ in range(3):
+            fn()
+        times = []
+        for _ in range(reps):
+            Cd.copy_(C0)                 # restore C (beta = 1) outside the events
+            l2_flush(flush)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            times.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        ms = sorted(a.elapsed_time(b) for a, b in times)
+        med = statistics.median(ms)
+        flops = 2.0 * M * N * K
+        byts = (M * K + K * N + 2 * M * N) * 2
+        roof_s = max(flops / (P * 1e12), byts / (bw * 1e9))
+        res[f"skinny_splitk_M{M}"] = {"median_us": round(med * 1e3, 2),
+                                      "tflops": round(flops / med / 1e9, 1),
+                                      "gbs": round(byts / med / 1e6, 1),
+                                      "hbm_frac": round(byts / med / 1e6 / bw, 4),
+                                      "roofline_frac": round(roof_s / (med / 1e3), 4),
+                                      "bound": "hbm"}
+        del Ad, Bd, C0, Cd
+    if swg.get_device_error(stream) != 0:
+        raise RuntimeError("device error word set during the component timings")
+    return res
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    import synth
+    oracle.build()
+    A, B, _ = synth.gemm_bf16(SIZE, SIZE, SIZE, 0, 0, seed=1)
+    rows, cols = args.reference_rows, args.reference_cols
+
+    def step():
+        fl = 0.0
+        for tA, tB in TRANS:
+            _, f, _ = time_oracle_sample(rows, cols, (tA, tB), A, B)
+            fl += f
+        return fl
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    flops = 0.0
+    for _ in range(args.steps):
+        flops += step()
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    cores = min(oracle.num_cores(), rows)
+    sample = (f"{rows} rows x {cols} columns of each of the four 8192^3 GEMMs per step "
+              "(FP64 oracle, all host cores)")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic: A, B ~ N(0,1) rounded to bf16, seed 1",
+        "config": {"workload": WORKLOAD, "M": SIZE, "N": SIZE, "K": SIZE,
+                   "trans": [list(t) for t in TRANS], "alpha": 1.0, "beta": 0.0,
+                   "parallelism": "host threads"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-components", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--component-reps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--reference-rows", type=int, default=64)
+    ap.add_argument("--reference-cols", type=int, default=512)
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    out = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -63,9 +63,11 @@ def _load():
             lib = ctypes.CDLL(build())
             i64, f64, vp, i32 = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int
             lib.orc_gemm.argtypes = [i32, i32, i64, i64, i64, f64, vp, i64, i32,
-                                     vp, i64, i32, f64, vp, i64, i32, vp, i64, vp, i32]
+                                     vp, i64, i32, f64, vp, i64, i32, vp, i64, vp, i64,
+                                     vp, i32]
             lib.orc_gemm.restype = i32
-            lib.orc_swiglu.argtypes = [vp, i64, vp, vp, i64, i64, i64, i64, vp, i64, vp, i32]
+            lib.orc_swiglu.argtypes = [vp, i64, vp, vp, i64, i64, i64, i64, vp, i64, vp, i64,
+                                       vp, i32]
             lib.orc_swiglu.restype = i32
             lib.orc_interleave.argtypes = [vp, vp, vp, i64, i64]
             lib.orc_interleave.restype = None
@@ -107,20 +109,22 @@ def _ptr(a):
 
 
 def _rows(rows, M):
+    """Index subset (rows or columns) as int64, or (None, M) for all."""
     if rows is None:
         return None, M
     r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
     if r.size and (r.min() < 0 or r.max() >= M):
-        raise IndexError("row index out of range")
+        raise IndexError("index out of range")
     return r, int(r.size)
 
 
 def gemm(transA: int, transB: int, M: int, N: int, K: int, alpha: float,
          A, lda: int, B, ldb: int, beta: float, C=None, ldc: int = 0,
          in_type: str = "bf16", c_type: str = "bf16", rows=None,
-         threads: int = 0) -> np.ndarray:
+         threads: int = 0, cols=None) -> np.ndarray:
     """D = alpha * op(A) op(B) + beta * C_old in double; returns the rows
-    ``rows`` (all rows when None) as a float64 array of shape (len(rows), N).
+    ``rows`` (all when None) and columns ``cols`` (all when None) as a float64
+    array of shape (len(rows), len(cols)).
     A is stored M x K (transA = 0) or K x M (transA = 1) with row stride lda;
     B is stored K x N (transB = 0) or N x K (transB = 1) with row stride ldb;
     C is M x N with row stride ldc and is not read when beta == 0."""
@@ -129,29 +133,32 @@ def gemm(transA: int, transB: int, M: int, N: int, K: int, alpha: float,
     b = _as_buffer(B, in_type)
     c = _as_buffer(C, c_type) if beta != 0.0 else None
     r, n_rows = _rows(rows, M)
-    out = np.empty((n_rows, N), dtype=np.float64)
+    cs, n_cols = _rows(cols, N)
+    out = np.empty((n_rows, n_cols), dtype=np.float64)
     rc = lib.orc_gemm(int(transA), int(transB), M, N, K, float(alpha),
                       _ptr(a), lda, TYPES[in_type], _ptr(b), ldb, TYPES[in_type],
                       float(beta), _ptr(c), ldc, TYPES[c_type],
-                      _ptr(r), n_rows, out.ctypes.data, int(threads))
+                      _ptr(r), n_rows, _ptr(cs), n_cols, out.ctypes.data, int(threads))
     if rc != 0:
         raise ValueError("oracle gemm rejected its arguments")
     return out
 
 
 def swiglu(A, W1, W2, M: int, N: int, K: int, rows=None, threads: int = 0,
-           lda: int | None = None, ldw: int | None = None) -> np.ndarray:
+           lda: int | None = None, ldw: int | None = None, cols=None) -> np.ndarray:
     """Y = SiLU(A W1) (.) (A W2) in double, from bf16 A (M x K) and separate
-    bf16 W1, W2 (K x N); returns float64 rows ``rows`` (all when None)."""
+    bf16 W1, W2 (K x N); returns float64 rows ``rows`` x columns ``cols`` (all
+    when None)."""
     lib = _load()
     a = _as_buffer(A, "bf16")
     w1 = _as_buffer(W1, "bf16")
     w2 = _as_buffer(W2, "bf16")
     r, n_rows = _rows(rows, M)
-    out = np.empty((n_rows, N), dtype=np.float64)
+    cs, n_cols = _rows(cols, N)
+    out = np.empty((n_rows, n_cols), dtype=np.float64)
     rc = lib.orc_swiglu(_ptr(a), lda if lda is not None else K, _ptr(w1), _ptr(w2),
                         ldw if ldw is not None else N, M, N, K, _ptr(r), n_rows,
-                        out.ctypes.data, int(threads))
+                        _ptr(cs), n_cols, out.ctypes.data, int(threads))
     if rc != 0:
         raise ValueError("oracle swiglu rejected its arguments")
     return out

@@ -105,7 +105,8 @@ typedef struct {
     const double *opB;            /* op(B) widened, K x N, row-major */
     const void *C; int64_t ldc; int c_type;
     const int64_t *rows; int64_t n_rows;
-    double *D;                    /* n_rows x N */
+    const int64_t *cols;          /* output column j of D is column cols[j] (NULL: j) */
+    double *D;                    /* n_rows x N, N = number of computed columns */
     int64_t r_begin, r_end;
 } gemm_job;
 
@@ -137,9 +138,10 @@ static void *gemm_rows(void *arg)
                 acc[j] += a * brow[j];
         }
         for (int64_t j = 0; j < N; ++j) {
+            int64_t col = g->cols ? g->cols[j] : j;
             double y = g->alpha * acc[j];
             if (g->beta != 0.0)
-                y += g->beta * load_elem(g->C, i * g->ldc + j, g->c_type);
+                y += g->beta * load_elem(g->C, i * g->ldc + col, g->c_type);
             acc[j] = y;
         }
     }
@@ -158,32 +160,40 @@ static int pick_threads(int n_threads, int64_t n_rows)
     return n_threads;
 }
 
-/* Widen op(B) into a dense K x N double matrix: opB(p,j) = B[p*ldb + j]
- * (op = N, B stored K x N) or B[j*ldb + p] (op = T, B stored N x K). */
+/* Widen the selected columns of op(B) into a dense K x N double matrix:
+ * opB(p,c) = B[p*ldb + c] (op = N, B stored K x N) or B[c*ldb + p] (op = T,
+ * B stored N x K), with c = cols[j] (or j when cols is NULL). */
 static double *widen_opB(int transB, int64_t N, int64_t K, const void *B,
-                         int64_t ldb, int b_type)
+                         int64_t ldb, int b_type, const int64_t *cols)
 {
     double *opB = (double *)malloc(sizeof(double) * (size_t)(K * N > 0 ? K * N : 1));
     if (!opB) return NULL;
     for (int64_t p = 0; p < K; ++p)
-        for (int64_t j = 0; j < N; ++j)
-            opB[p * N + j] = load_elem(B, transB ? j * ldb + p : p * ldb + j, b_type);
+        for (int64_t j = 0; j < N; ++j) {
+            int64_t c = cols ? cols[j] : j;
+            opB[p * N + j] = load_elem(B, transB ? c * ldb + p : p * ldb + c, b_type);
+        }
     return opB;
 }
 
-/* Computes rows[0..n_rows) of D (all rows 0..M-1 when rows == NULL, and then
- * n_rows must equal M).  D is n_rows x N doubles, row-major.  Returns 0 on
- * success, -1 on bad arguments or allocation failure. */
+/* Computes D at rows[0..n_rows) x cols[0..n_cols) (all rows 0..M-1 when rows
+ * == NULL, and then n_rows must equal M; all columns when cols == NULL, and
+ * then n_cols must equal N).  D is n_rows x n_cols doubles, row-major.  Each
+ * element is the same sum whichever rows and columns are requested.  Returns
+ * 0 on success, -1 on bad arguments or allocation failure. */
 int orc_gemm(int transA, int transB, int64_t M, int64_t N, int64_t K,
              double alpha, const void *A, int64_t lda, int a_type,
              const void *B, int64_t ldb, int b_type, double beta,
              const void *C, int64_t ldc, int c_type,
-             const int64_t *rows, int64_t n_rows, double *D, int n_threads)
+             const int64_t *rows, int64_t n_rows, const int64_t *cols,
+             int64_t n_cols, double *D, int n_threads)
 {
-    if (M < 0 || N < 0 || K < 0 || n_rows < 0 || !D) return -1;
+    if (M < 0 || N < 0 || K < 0 || n_rows < 0 || n_cols < 0 || !D) return -1;
     if (!rows && n_rows != M) return -1;
+    if (!cols && n_cols != N) return -1;
+    N = n_cols;
     if (n_rows == 0 || N == 0) return 0;
-    double *opB = widen_opB(transB, N, K, B, ldb, b_type);
+    double *opB = widen_opB(transB, N, K, B, ldb, b_type, cols);
     if (!opB) return -1;
     int T = pick_threads(n_threads, n_rows);
     pthread_t th[256];
@@ -196,7 +206,7 @@ int orc_gemm(int transA, int transB, int64_t M, int64_t N, int64_t K,
         g->A = A; g->lda = lda; g->a_type = a_type;
         g->opB = opB;
         g->C = C; g->ldc = ldc; g->c_type = c_type;
-        g->rows = rows; g->n_rows = n_rows; g->D = D;
+        g->rows = rows; g->n_rows = n_rows; g->cols = cols; g->D = D;
         g->r_begin = n_rows * t / T;
         g->r_end = n_rows * (t + 1) / T;
         pthread_create(&th[t], NULL, gemm_rows, g);
@@ -214,22 +224,25 @@ int orc_gemm(int transA, int transB, int64_t M, int64_t N, int64_t K,
  * Both products come from orc_gemm with alpha = 1, beta = 0. */
 int orc_swiglu(const uint16_t *A, int64_t lda, const uint16_t *W1,
                const uint16_t *W2, int64_t ldw, int64_t M, int64_t N,
-               int64_t K, const int64_t *rows, int64_t n_rows, double *Y,
-               int n_threads)
+               int64_t K, const int64_t *rows, int64_t n_rows,
+               const int64_t *cols, int64_t n_cols, double *Y, int n_threads)
 {
     if (!rows && n_rows != M) return -1;
-    if (n_rows == 0 || N == 0) return 0;
-    double *G = (double *)malloc(sizeof(double) * (size_t)(n_rows * N));
-    double *U = (double *)malloc(sizeof(double) * (size_t)(n_rows * N));
+    if (!cols && n_cols != N) return -1;
+    if (n_rows == 0 || n_cols == 0) return 0;
+    double *G = (double *)malloc(sizeof(double) * (size_t)(n_rows * n_cols));
+    double *U = (double *)malloc(sizeof(double) * (size_t)(n_rows * n_cols));
     int rc = (G && U) ? 0 : -1;
     if (rc == 0)
         rc = orc_gemm(0, 0, M, N, K, 1.0, A, lda, ORC_BF16, W1, ldw, ORC_BF16,
-                      0.0, NULL, 0, ORC_BF16, rows, n_rows, G, n_threads);
+                      0.0, NULL, 0, ORC_BF16, rows, n_rows, cols, n_cols, G,
+                      n_threads);
     if (rc == 0)
         rc = orc_gemm(0, 0, M, N, K, 1.0, A, lda, ORC_BF16, W2, ldw, ORC_BF16,
-                      0.0, NULL, 0, ORC_BF16, rows, n_rows, U, n_threads);
+                      0.0, NULL, 0, ORC_BF16, rows, n_rows, cols, n_cols, U,
+                      n_threads);
     if (rc == 0)
-        for (int64_t e = 0; e < n_rows * N; ++e)
+        for (int64_t e = 0; e < n_rows * n_cols; ++e)
             Y[e] = orc_silu(G[e]) * U[e];
     free(G);
     free(U);

@@ -135,12 +135,21 @@ def test_bruteforce_exact(dtype, kind, tA, tB, shape):
                 assert Fraction(D[i, j]) == want, (i, j, alpha, beta)
 
 
-def test_rows_subset_matches_full():
+@pytest.mark.parametrize("tA,tB", [(0, 0), (1, 1)])
+def test_rows_and_cols_subsets_match_full(tA, tB):
     M, N, K = 9, 6, 11
-    A, B, _ = synth.gemm_bf16(M, N, K, seed=7)
-    full = oracle.gemm(0, 0, M, N, K, 1.0, A, K, B, N, 0.0)
-    part = oracle.gemm(0, 0, M, N, K, 1.0, A, K, B, N, 0.0, rows=[5, 2, 8])
+    A, B, C = synth.gemm_bf16(M, N, K, tA, tB, seed=7, c=True)
+    lda, ldb = A.shape[1], B.shape[1]
+    full = oracle.gemm(tA, tB, M, N, K, 1.5, A, lda, B, ldb, -1.0, C, N)
+    part = oracle.gemm(tA, tB, M, N, K, 1.5, A, lda, B, ldb, -1.0, C, N, rows=[5, 2, 8])
     assert np.array_equal(part, full[[5, 2, 8]])
+    sub = oracle.gemm(tA, tB, M, N, K, 1.5, A, lda, B, ldb, -1.0, C, N, rows=[5, 2, 8],
+                      cols=[4, 0, 5])
+    assert np.array_equal(sub, full[np.ix_([5, 2, 8], [4, 0, 5])])
+    A2, W1, W2 = synth.swiglu(M, K, N, seed=8)
+    yf = oracle.swiglu(A2, W1, W2, M, N, K)
+    assert np.array_equal(oracle.swiglu(A2, W1, W2, M, N, K, rows=[1, 3], cols=[5, 1]),
+                          yf[np.ix_([1, 3], [5, 1])])
 
 
 def test_transpose_identity():
