@@ -345,7 +345,11 @@ def run_e2e(args, A, B, Ad, Bd, Ds, step, dist_mod, dev):
 
 
 def l2_flush(buf):
-    buf.zero_()
+    """Writes a buffer larger than L2, then reads a second one, so L2 holds
+    only clean lines of an unrelated buffer: the timed kernel neither hits in
+    L2 nor pays for the write-back of the flush's dirty lines."""
+    buf[0].zero_()
+    buf[1].sum()
 
 
 def time_reps(fn, reps, dev, stream, flush_buf):
@@ -364,55 +368,76 @@ def time_reps(fn, reps, dev, stream, flush_buf):
     return statistics.median(ms), ms[0]
 
 
-def run_components(args, dev, stream):
-    """SwiGLU and skinny split-K timings (median of reps, L2 flushed before each)."""
+def component_cases():
+    """(name, kind, M, K, N) of the fused-SwiGLU and skinny split-K workloads."""
+    cases = [(f"swiglu_small_M{m}", "swiglu", m, 896, 4864) for m in (128, 512, 2048)]
+    cases += [(f"swiglu_8b_M{m}", "swiglu", m, 4096, 14336) for m in (512, 2048, 8192)]
+    cases += [(f"skinny_splitk_M{m}", "skinny", m, 16384, 4096) for m in (16, 32, 64)]
+    return cases
+
+
+def build_case(kind, M, K, N, dev, stream):
+    """Returns (fn, reset, flops, algorithmic_bytes) for one workload; `reset`
+    restores C between repetitions (beta = 1) and is run outside the events."""
     import torch
 
     import swiglu_mlp_gb300 as swg
     import synth
-
-    peaks, _ = load_peaks()
-    bw = float(peaks["hbm_gbs"])
-    P = float(peaks["bf16_tflops"])
-    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    reps = args.component_reps
-    res = {}
-    for name, M, K, N in [("swiglu_small_M128", 128, 896, 4864),
-                          ("swiglu_small_M512", 512, 896, 4864),
-                          ("swiglu_small_M2048", 2048, 896, 4864),
-                          ("swiglu_8b_M512", 512, 4096, 14336),
-                          ("swiglu_8b_M2048", 2048, 4096, 14336),
-                          ("swiglu_8b_M8192", 8192, 4096, 14336)]:
+    if kind == "swiglu":
         A, W1, W2 = synth.swiglu(M, K, N, seed=3)
         Ad = A.to(dev)
         Wf = swg.interleave_weights(W1.to(dev), W2.to(dev), stream=stream)
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        fn = lambda: swg.swiglu_mlp(Ad, Wf, Y, M, N, K, stream=stream)  # noqa: E731
-        for _ in range(3):
-            fn()
-        med, best = time_reps(fn, reps, dev, stream, flush)
-        flops = 2.0 * M * 2 * N * K
-        byts = (M * K + K * 2 * N + M * N) * 2
-        roof_s = max(flops / (P * 1e12), byts / (bw * 1e9))
-        res[name] = {"median_us": round(med * 1e3, 2), "tflops": round(flops / med / 1e9, 1),
-                     "gbs": round(byts / med / 1e6, 1),
-                     "roofline_frac": round(roof_s / (med / 1e3), 4),
-                     "bound": "tensor" if flops / (P * 1e12) > byts / (bw * 1e9) else "hbm"}
-        del Ad, Wf, Y
-    for M in (16, 32, 64):
-        N, K = 4096, 16384
-        A, B, C = synth.skinny(M)
+
+        def fn():
+            swg.swiglu_mlp(Ad, Wf, Y, M, N, K, stream=stream)
+        return fn, None, 2.0 * M * 2 * N * K, (M * K + K * 2 * N + M * N) * 2
+    if kind == "skinny":
+        A, B, C = synth.skinny(M, N, K)
         Ad, Bd, C0 = A.to(dev), B.to(dev), C.to(dev)
         Cd = C0.clone()
 
         def fn():
             swg.gemm(0, 0, M, N, K, 1.0, Ad, K, Bd, N, 1.0, Cd, N, swg.BF16, stream=stream)
 
+        def reset():
+            Cd.copy_(C0)
+        return fn, reset, 2.0 * M * N * K, (M * K + K * N + 2 * M * N) * 2
+    if kind.startswith("gemm"):
+        tA, tB = {"gemm_nn": (0, 0), "gemm_nt": (0, 1), "gemm_tn": (1, 0),
+                  "gemm_tt": (1, 1)}[kind]
+        A, B, _ = synth.gemm_bf16(M, N, K, tA, tB, seed=1)
+        Ad, Bd = A.to(dev), B.to(dev)
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+        def fn():
+            swg.gemm(tA, tB, M, N, K, 1.0, Ad, A.shape[1], Bd, B.shape[1], 0.0, D, N, swg.BF16,
+                     stream=stream)
+        return fn, None, 2.0 * M * N * K, (M * K + K * N + M * N) * 2
+    raise ValueError(kind)
+
+
+def run_components(args, dev, stream):
+    """SwiGLU and skinny split-K timings: median of reps, each after an L2
+    flush and (skinny) a restore of C, both outside the CUDA events."""
+    import torch
+
+    import swiglu_mlp_gb300 as swg
+
+    peaks, _ = load_peaks()
+    bw = float(peaks["hbm_gbs"])
+    P = float(peaks["bf16_tflops"])
+    flush = (torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev),
+             torch.zeros(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev))
+    res = {}
+    for name, kind, M, K, N in component_cases():
+        fn, reset, flops, byts = build_case(kind, M, K, N, dev, stream)
         for _ in range(3):
             fn()
         times = []
-        for _ in range(reps):
-            Cd.copy_(C0)                 # restore C (beta = 1) outside the events
+        for _ in range(args.component_reps):
+            if reset:
+                reset()
             l2_flush(flush)
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
@@ -423,19 +448,43 @@ def run_components(args, dev, stream):
         torch.cuda.synchronize(dev)
         ms = sorted(a.elapsed_time(b) for a, b in times)
         med = statistics.median(ms)
-        flops = 2.0 * M * N * K
-        byts = (M * K + K * N + 2 * M * N) * 2
-        roof_s = max(flops / (P * 1e12), byts / (bw * 1e9))
-        res[f"skinny_splitk_M{M}"] = {"median_us": round(med * 1e3, 2),
-                                      "tflops": round(flops / med / 1e9, 1),
-                                      "gbs": round(byts / med / 1e6, 1),
-                                      "hbm_frac": round(byts / med / 1e6 / bw, 4),
-                                      "roofline_frac": round(roof_s / (med / 1e3), 4),
-                                      "bound": "hbm"}
-        del Ad, Bd, C0, Cd
+        t_tensor, t_hbm = flops / (P * 1e12), byts / (bw * 1e9)
+        entry = {"median_us": round(med * 1e3, 2), "min_us": round(ms[0] * 1e3, 2),
+                 "tflops": round(flops / med / 1e9, 1), "gbs": round(byts / med / 1e6, 1),
+                 "roofline_frac": round(max(t_tensor, t_hbm) / (med / 1e3), 4),
+                 "bound": "tensor" if t_tensor > t_hbm else "hbm"}
+        if kind == "skinny":
+            entry["hbm_frac"] = round(byts / med / 1e6 / bw, 4)
+        res[name] = entry
     if swg.get_device_error(stream) != 0:
         raise RuntimeError("device error word set during the component timings")
     return res
+
+
+def run_profile_case(args):
+    """A few launches of one workload and nothing else, for an ncu capture:
+    2 warm-up launches, then `--profile-launches` more."""
+    import torch
+
+    import swiglu_mlp_gb300 as swg
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    table = {c[0]: c[1:] for c in component_cases()}
+    for t in ("nn", "nt", "tn", "tt"):
+        table[f"gemm8192_{t}"] = (f"gemm_{t}", SIZE, SIZE, SIZE)
+    kind, M, K, N = table[args.profile_case]
+    fn, reset, _, _ = build_case(kind, M, K, N, dev, stream)
+    for _ in range(2 + args.profile_launches):
+        if reset:
+            reset()
+        fn()
+    torch.cuda.synchronize(dev)
+    rc = swg.get_device_error(stream)
+    print(json.dumps({"profile_case": args.profile_case, "launches": 2 + args.profile_launches,
+                      "device_error": rc}))
+    if rc != 0:
+        raise SystemExit(1)
 
 
 # ------------------------------------------------------------------ reference arm
@@ -505,7 +554,13 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-rows", type=int, default=64)
     ap.add_argument("--reference-cols", type=int, default=512)
+    ap.add_argument("--profile-case", default=None,
+                    help="run only a few launches of one workload (for ncu captures)")
+    ap.add_argument("--profile-launches", type=int, default=2)
     args = ap.parse_args(argv)
+    if args.profile_case:
+        run_profile_case(args)
+        return
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     out = run_reference(args) if args.impl == "reference" else run_ours(args)

@@ -86,8 +86,10 @@ typedef enum {
  *                   fill the GPU ("为什么 GEMM 是 CUDA 的必修课", 关键技术 item 5);
  *                   the partial sums are reduced in a fixed order, so repeated
  *                   calls give bit-identical results.  The FP32 partials live
- *                   in a library-owned workspace, allocated on first use per
- *                   (device, stream) and freed by swg_shutdown().
+ *                   in a library-owned workspace, allocated (cudaMalloc) on
+ *                   first use per (device, stream), grown when a larger split
+ *                   needs it, and freed by swg_shutdown().  Two kernels are
+ *                   launched: the GEMM and a dependent reduction.
  */
 SWG_API int gemm(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
          const void *A, int64_t lda, const void *B, int64_t ldb, float beta,
@@ -97,8 +99,8 @@ SWG_API int gemm(int transA, int transB, int64_t M, int64_t N, int64_t K, float 
  * gemm_ex — gemm with an explicit split-K factor.
  *   split_k == 0  automatic choice (what gemm does);
  *   split_k == 1  no split;
- *   split_k >= 2  split the K loop into at most split_k contiguous ranges
- *                 (fewer when K has fewer 64-wide blocks).
+ *   split_k >= 2  split the K loop into at most min(split_k, 16) contiguous
+ *                 ranges (fewer when K has fewer 64-wide blocks).
  * Every other argument and rule is that of gemm.
  */
 SWG_API int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,
@@ -145,8 +147,7 @@ SWG_API const char *swg_status_string(int status);
  * Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns SWG_OK when no kernel reported a problem since the last call,
  * SWG_ERR_DEVICE_TIMEOUT when a bounded wait ran out, SWG_ERR_CUDA when the
- * synchronisation itself failed.  After a timeout the library's split-K
- * tickets for this stream are cleared, so later calls start clean.
+ * synchronisation itself failed.
  */
 SWG_API int swg_get_device_error(void *stream);
 

@@ -56,9 +56,8 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // ----------------------------------------------------------------- per device
 
 struct Workspace {
-    void *base = nullptr;   // [tickets | partials]
+    void *base = nullptr;   // split-K FP32 partials
     size_t bytes = 0;
-    size_t ticket_bytes = 0;
 };
 
 struct DeviceState {
@@ -88,38 +87,26 @@ int device_state(DeviceState *&out)
     return SWG_OK;
 }
 
-// Grow-only split-K workspace for (device, stream).  Tickets are zeroed on
-// allocation and every reducing CTA resets its own ticket.
-int workspace(DeviceState *d, cudaStream_t s, size_t ticket_bytes, size_t part_bytes,
-              Workspace *&out)
+// Grow-only split-K workspace for (device, stream).  Only the stream that
+// owns it uses it, so stream order keeps calls from overlapping.
+int workspace(DeviceState *d, cudaStream_t s, size_t bytes, Workspace *&out)
 {
     if (std::getenv("SWG_TEST_FAIL_ALLOC")) return SWG_ERR_NO_MEMORY;
     std::lock_guard<std::mutex> lk(g_mu);
     Workspace &w = d->ws[s];
-    ticket_bytes = (ticket_bytes + 255) & ~size_t(255);
-    const size_t need = ticket_bytes + part_bytes;
-    if (w.base == nullptr || w.ticket_bytes < ticket_bytes || w.bytes < need) {
-        const size_t tb = std::max(ticket_bytes, w.ticket_bytes);
-        const size_t total = tb + std::max(part_bytes, w.bytes - w.ticket_bytes);
+    if (w.base == nullptr || w.bytes < bytes) {
         if (w.base) {
             if (cudaStreamSynchronize(s) != cudaSuccess) return SWG_ERR_CUDA;
             cudaFree(w.base);
-            w.base = nullptr;
+            w = Workspace{};
         }
         void *p = nullptr;
-        if (cudaMalloc(&p, total) != cudaSuccess) {
+        if (cudaMalloc(&p, bytes) != cudaSuccess) {
             cudaGetLastError();
-            w = Workspace{};
             return SWG_ERR_NO_MEMORY;
         }
-        if (cudaMemsetAsync(p, 0, tb, s) != cudaSuccess) {
-            cudaFree(p);
-            w = Workspace{};
-            return SWG_ERR_CUDA;
-        }
         w.base = p;
-        w.bytes = total;
-        w.ticket_bytes = tb;
+        w.bytes = bytes;
     }
     out = &w;
     return SWG_OK;
@@ -319,6 +306,7 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
     } else if (split_k > 1) {
         splits = (int)std::min<int64_t>(split_k, kb);
     }
+    splits = std::min(splits, swg::MAX_SPLITS);
     int kbps = (int)kb;
     if (splits > 1) {
         kbps = (int)cdiv(kb, splits);
@@ -365,13 +353,16 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
     if (splits > 1) {
         const int64_t ld_ws = cdiv(N, 4) * 4;
         Workspace *w = nullptr;
-        if (int rc = workspace(d, s, sizeof(int) * (size_t)p.tiles,
-                               sizeof(float) * (size_t)splits * (size_t)M * (size_t)ld_ws, w))
+        if (int rc = workspace(d, s, sizeof(float) * (size_t)splits * (size_t)M * (size_t)ld_ws,
+                               w))
             return rc;
-        p.tickets = static_cast<int *>(w->base);
-        p.ws = reinterpret_cast<float *>(static_cast<char *>(w->base) + w->ticket_bytes);
+        p.ws = static_cast<float *>(w->base);
         p.ld_ws = ld_ws;
         e = swg::launch_tc_splitk(bn, ta, tb, p, grid, s);
+        if (e == cudaSuccess) {
+            g_launches++;
+            e = swg::launch_splitk_reduce(p, d->sms, s);
+        }
     } else {
         e = swg::launch_tc_store(bn, ta, tb, p, grid, s);
     }
@@ -471,13 +462,6 @@ int swg_get_device_error(void *stream)
     if (v != 0) {
         const int zero = 0;
         if (cudaMemcpyToSymbol(g_err_word, &zero, sizeof(int)) != cudaSuccess) return SWG_ERR_CUDA;
-        int dev = 0;
-        cudaGetDevice(&dev);
-        std::lock_guard<std::mutex> lk(g_mu);
-        auto it = g_dev.find(dev);
-        if (it != g_dev.end())
-            for (auto &kv : it->second.ws)
-                if (kv.second.base) cudaMemset(kv.second.base, 0, kv.second.ticket_bytes);
         return v;
     }
     return SWG_OK;

@@ -22,4 +22,8 @@ cudaError_t launch_tc_swiglu(int bn, const CUtensorMap &ta, const CUtensorMap &t
 cudaError_t launch_tc_splitk(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
                              const TileParams &p, int grid, cudaStream_t s);
 
+// In-order reduction of the split-K partials into D (alpha, beta, cast),
+// launched as a programmatic dependent of the split-K GEMM on the same stream.
+cudaError_t launch_splitk_reduce(const TileParams &p, int sms, cudaStream_t s);
+
 }  // namespace swg

@@ -16,9 +16,11 @@
 //                    applies the fused epilogue:
 //                      EPI_STORE  D = alpha*acc + beta*C, cast, 16-byte stores;
 //                      EPI_SWIGLU Y = SiLU(acc[2j]) * acc[2j+1] per column pair;
-//                      EPI_SPLITK FP32 partial to the workspace, then the last
-//                                 arriving CTA of the tile sums all partials in
-//                                 split order and stores alpha*sum + beta*C.
+//                      EPI_SPLITK FP32 partial of one K range to the
+//                                 workspace; splitk_reduce_kernel (launched
+//                                 right behind, programmatic dependent launch)
+//                                 sums the partials in split order and stores
+//                                 alpha*sum + beta*C.
 // The double TMEM accumulator lets the epilogue of tile t overlap the main
 // loop of tile t+1.
 //
@@ -53,6 +55,7 @@ constexpr int NUM_THREADS = 192;
 constexpr int NUM_EPI_THREADS = 128;
 constexpr int EPI_WARP0 = 2;
 constexpr int ERR_TIMEOUT = 6;       // == SWG_ERR_DEVICE_TIMEOUT
+constexpr int MAX_SPLITS = 16;       // split-K ranges per tile (host enforces)
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 
 struct TileParams {
@@ -72,7 +75,6 @@ struct TileParams {
     int out_kind;                // OutKind
     float *ws;                   // split-K partials [splits][M][ld_ws]
     long long ld_ws;
-    int *tickets;                // split-K arrival counters, one per tile
     int *err;                    // device error word
 };
 
@@ -135,9 +137,12 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
            ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// SiLU(x) = x * sigmoid(x) = x / (1 + e^-x) in FP32 without a division
+// slow path: __expf and __fdividef are the CUDA fast intrinsics.  Limits:
+// x -> -inf gives 1 + e^-x = inf and x * (1/inf) = -0; x -> +inf gives x.
 __device__ __forceinline__ float silu_f32(float x)
 {
-    return x / (1.0f + __expf(-x));
+    return __fdividef(x, 1.0f + __expf(-x));
 }
 
 __device__ __forceinline__ uint32_t pack2(float a, float b, int out_kind)
@@ -241,6 +246,57 @@ __device__ __forceinline__ void store_row_chunk(const TileParams &p, long long o
     }
 }
 
+// One 32-column chunk of one accumulator row (row m of the output, first
+// column n of the tile's column space) through the epilogue EPI.
+template <int EPI>
+__device__ __forceinline__ void epi_chunk(const TileParams &p, const uint32_t (&r)[32], int m, int n,
+                                          int split)
+{
+    if (n >= p.N) return;
+    const int cnt = (p.N - n) < 32 ? (p.N - n) : 32;
+    if (EPI == EPI_STORE) {
+        float a[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) a[j] = __uint_as_float(r[j]);
+        store_row_chunk(p, (long long)m * p.ldd + n, a, cnt);
+    } else if (EPI == EPI_SWIGLU) {
+        // Column pair (2j, 2j+1) of the 2N-space is (Gate_j, Up_j); output
+        // column n/2 + j.
+        const long long off = (long long)m * p.ldd + n / 2;
+        float y[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            y[j] = silu_f32(__uint_as_float(r[2 * j])) * __uint_as_float(r[2 * j + 1]);
+        __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.D) + off;
+        if (cnt == 32) {
+            uint32_t w[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) w[j] = pack2(y[2 * j], y[2 * j + 1], OUT_BF16);
+            uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+            d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (2 * j < cnt) dst[j] = __float2bfloat16_rn(y[j]);
+        }
+    } else {
+        // Split-K: raw FP32 partial of this K range; reduced by a second kernel.
+        float *dst = p.ws + ((long long)split * p.M + m) * p.ld_ws + n;
+        if (cnt == 32) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                reinterpret_cast<float4 *>(dst)[j] =
+                    make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (j < cnt) dst[j] = __uint_as_float(r[j]);
+        }
+    }
+}
+
 template <int BN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -262,10 +318,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t *mma_done = bars + 2 * S + 4;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + C::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
-    volatile int *last_flag = reinterpret_cast<volatile int *>(tmem_holder + 2);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+
+    // Split-K: let the reduction kernel queued behind this one be scheduled
+    // now; it waits (griddepcontrol.wait) until this grid has completed.
+    if (EPI == EPI_SPLITK) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -278,7 +337,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         mbar_init(smem_u32(mma_done), 1);
         *abort_flag = 0;
-        *last_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
@@ -403,7 +461,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                 // TMEM lane quarter of this warp
         const int row = q * 32 + lane;
-        const int et = threadIdx.x - EPI_WARP0 * 32;
         int t = 0;
         for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++t) {
             int mb, nb, split, tile;
@@ -412,124 +469,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t acc_phase = (t >> 1) & 1;
             bool ok = wait_bounded(smem_u32(&acc_full[acc]), acc_phase, abort_flag, p.err);
             ok = __all_sync(0xffffffffu, ok);
-            if (EPI == EPI_SPLITK) ok = named_bar_and(1, NUM_EPI_THREADS, ok);
             if (!ok) break;
             tc_fence_after();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
             const int m = mb * BM + row;
             const bool row_ok = m < p.M;
+            // Two register buffers: the load of chunk c+1 is in flight while
+            // chunk c is converted and stored (tcgen05.wait::ld waits for all
+            // earlier loads, so each wait retires exactly the older chunk).
+            uint32_t ra[32], rb[32];
+            tmem_ld_32cols(t_row, ra);
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld_32cols(t_row + c * 32, r);
-                tmem_ld_wait();
-                const int n = nb * BN + c * 32;
-                if (!row_ok || n >= p.N) continue;
-                const int cnt = (p.N - n) < 32 ? (p.N - n) : 32;
-                if (EPI == EPI_STORE) {
-                    float a[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) a[j] = __uint_as_float(r[j]);
-                    store_row_chunk(p, (long long)m * p.ldd + n, a, cnt);
-                } else if (EPI == EPI_SWIGLU) {
-                    // Column pair (2j, 2j+1) of the 2N-space = (Gate_j, Up_j).
-                    const long long off = (long long)m * p.ldd + n / 2;
-                    uint32_t w[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float y0 = silu_f32(__uint_as_float(r[4 * j])) *
-                                         __uint_as_float(r[4 * j + 1]);
-                        const float y1 = silu_f32(__uint_as_float(r[4 * j + 2])) *
-                                         __uint_as_float(r[4 * j + 3]);
-                        w[j] = pack2(y0, y1, OUT_BF16);
-                    }
-                    if (cnt == 32) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(
-                            reinterpret_cast<__nv_bfloat16 *>(p.D) + off);
-                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                    } else {
-                        __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.D) + off;
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            if (2 * j < cnt) {
-                                const float y = silu_f32(__uint_as_float(r[2 * j])) *
-                                                __uint_as_float(r[2 * j + 1]);
-                                dst[j] = __float2bfloat16_rn(y);
-                            }
-                        }
-                    }
-                } else {
-                    float *dst = p.ws + ((long long)split * p.M + m) * p.ld_ws + n;
-                    if (cnt == 32) {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            reinterpret_cast<float4 *>(dst)[j] =
-                                make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                            __uint_as_float(r[4 * j + 2]),
-                                            __uint_as_float(r[4 * j + 3]));
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (j < cnt) dst[j] = __uint_as_float(r[j]);
-                    }
-                }
+            for (int c = 0; c < BN / 32; c += 2) {
+                tmem_ld_wait(ra);
+                tmem_ld_32cols(t_row + (c + 1) * 32, rb);
+                if (row_ok) epi_chunk<EPI>(p, ra, m, nb * BN + c * 32, split);
+                tmem_ld_wait(rb);
+                if (c + 2 < BN / 32) tmem_ld_32cols(t_row + (c + 2) * 32, ra);
+                if (row_ok) epi_chunk<EPI>(p, rb, m, nb * BN + (c + 1) * 32, split);
             }
             // Accumulator drained: hand it back to the MMA warp.
             tc_fence_before();
             mbar_arrive(smem_u32(&acc_empty[acc]));
-
-            if (EPI == EPI_SPLITK) {
-                // Publish this split's partial; the last of p.splits arrivals
-                // reduces all of them in split order 0..splits-1.
-                __threadfence();
-                named_bar_sync(1, NUM_EPI_THREADS);
-                if (et == 0) {
-                    const int old = atomicAdd(&p.tickets[tile], 1);
-                    const int last = old == p.splits - 1;
-                    if (last) p.tickets[tile] = 0;   // ready for the next call
-                    *last_flag = last;
-                }
-                named_bar_sync(1, NUM_EPI_THREADS);
-                if (*last_flag) {
-                    __threadfence();
-                    const int m0 = mb * BM, n0 = nb * BN;
-                    const int rows = (p.M - m0) < BM ? (p.M - m0) : BM;
-                    const int cols = (p.N - n0) < BN ? (p.N - n0) : BN;
-                    const int quads = (cols + 3) / 4;
-                    for (int idx = et; idx < rows * quads; idx += NUM_EPI_THREADS) {
-                        const int rr = idx / quads;
-                        const int cc = (idx - rr * quads) * 4;
-                        const int mm = m0 + rr, nn = n0 + cc;
-                        const int cnt = (cols - cc) < 4 ? (cols - cc) : 4;
-                        float s4[4] = {0.f, 0.f, 0.f, 0.f};
-                        for (int s = 0; s < p.splits; ++s) {
-                            const float *src = p.ws + ((long long)s * p.M + mm) * p.ld_ws + nn;
-                            if (cnt == 4) {
-                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
-                                s4[0] += v.x;
-                                s4[1] += v.y;
-                                s4[2] += v.z;
-                                s4[3] += v.w;
-                            } else {
-#pragma unroll
-                                for (int j = 0; j < 4; ++j)
-                                    if (j < cnt) s4[j] += __ldcg(src + j);
-                            }
-                        }
-                        const long long off = (long long)mm * p.ldd + nn;
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            if (j < cnt) {
-                                float v = p.alpha * s4[j];
-                                if (p.beta != 0.0f)
-                                    v += p.beta * load_out(p.D, off + j, p.out_kind);
-                                store_out(p.D, off + j, v, p.out_kind);
-                            }
-                        }
-                    }
-                }
-            }
         }
     }
 
