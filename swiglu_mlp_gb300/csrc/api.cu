@@ -65,6 +65,7 @@ struct DeviceState {
     int sms = 0;
     int *err = nullptr;                          // address of g_err_word
     std::map<cudaStream_t, Workspace> ws;
+    std::map<int, int> max_pairs;                // (kind, bn) -> resident CTA pairs
 };
 
 std::map<int, DeviceState> g_dev;
@@ -185,6 +186,79 @@ int pick_bn(int64_t M, int64_t N, int sms, const int *cands, int ncand)
         }
     }
     return best;
+}
+
+// Resident CTA pairs of a pair kernel (kind 0 = GEMM store, 1 = SwiGLU).
+int max_pairs(DeviceState *d, int kind, int bn)
+{
+    const int key = kind * 1024 + bn;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = d->max_pairs.find(key);
+        if (it != d->max_pairs.end()) return it->second;
+    }
+    const int n = kind == 0 ? swg::max_active_pairs_store(bn, d->sms)
+                            : swg::max_active_pairs_swiglu(bn, d->sms);
+    std::lock_guard<std::mutex> lk(g_mu);
+    d->max_pairs[key] = n;
+    return n;
+}
+
+// Tile mode override for tests and tuning: SWG_TILE_MODE=1cta forces
+// single-CTA 128-row tiles, =2cta forces CTA-pair 256-row tiles, =2cta128
+// and =2cta256 also fix the pair tile's width.
+int forced_tile_mode(int *pair_bn)
+{
+    const char *v = std::getenv("SWG_TILE_MODE");
+    *pair_bn = 0;
+    if (!v) return 0;
+    if (v[0] == '1') return 1;
+    if (v[0] == '2') {
+        *pair_bn = std::atoi(v + 4);   // "2cta" -> 0, "2cta128" -> 128
+        return 2;
+    }
+    return 0;
+}
+
+struct TileChoice {
+    bool pair = false;
+    int bn = 256;
+    int units = 0;      // CTAs (single) or CTA pairs (pair) to launch
+};
+
+// Chooses single-CTA or CTA-pair tiles and the tile width for an output of
+// M x N (N in the tile-column space), by last-wave fill; pairs halve the B
+// operand each SM loads, so they win ties and are used whenever M > 128.
+TileChoice choose_tiles(DeviceState *d, int kind, int64_t M, int64_t N, const int *single_bns,
+                        int n_single)
+{
+    TileChoice c;
+    int only_bn = 0;
+    const int mode = forced_tile_mode(&only_bn);
+    bool try_pair = (M > swg::BM && mode != 1) || mode == 2;
+    if (try_pair) {
+        static const int pair_bns[] = {256, 128};
+        double best = -1.0;
+        for (int bn : pair_bns) {
+            if (only_bn && bn != only_bn) continue;
+            const int slots = max_pairs(d, kind, bn);
+            if (slots <= 0) continue;
+            const int64_t tiles = cdiv(M, 2 * swg::BM) * cdiv(N, bn);
+            const int64_t waves = cdiv(tiles, slots);
+            const double eff = double(tiles) / double(waves * slots);
+            const double score = eff * (bn == 256 ? 1.0 : 0.9);
+            if (score > best + 1e-9) {
+                best = score;
+                c.pair = true;
+                c.bn = bn;
+                c.units = (int)std::min<int64_t>(tiles, slots);
+            }
+        }
+        if (c.pair) return c;
+    }
+    c.bn = pick_bn(M, N, d->sms, single_bns, n_single);
+    c.units = (int)std::min<int64_t>(cdiv(M, swg::BM) * cdiv(N, c.bn), d->sms);
+    return c;
 }
 
 // ----------------------------------------------------------------- small kernels
@@ -312,10 +386,13 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
         kbps = (int)cdiv(kb, splits);
         splits = (int)cdiv(kb, kbps);
     }
+    TileChoice tc;
     if (splits <= 1) {
         static const int cands[] = {256, 128};
-        bn = pick_bn(M, N, d->sms, cands, 2);
+        tc = choose_tiles(d, 0, M, N, cands, 2);
+        bn = tc.bn;
     }
+    const bool pair = tc.pair;
 
     const bool a_mn = transA == SWG_OP_T;
     const bool b_mn = transB == SWG_OP_N;
@@ -323,14 +400,14 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
     bool ok = a_mn ? make_tmap(&ta, A, ti.in_bf16, M, K, lda, 64)
                    : make_tmap(&ta, A, ti.in_bf16, K, M, lda, swg::BM);
     ok = ok && (b_mn ? make_tmap(&tb, B, ti.in_bf16, N, K, ldb, 64)
-                     : make_tmap(&tb, B, ti.in_bf16, K, N, ldb, bn));
+                     : make_tmap(&tb, B, ti.in_bf16, K, N, ldb, pair ? bn / 2 : bn));
     if (!ok) return SWG_ERR_CUDA;
 
     TileParams p{};
     p.M = (int)M;
     p.N = (int)N;
     p.K = (int)K;
-    p.m_blocks = (int)mblk;
+    p.m_blocks = (int)(pair ? cdiv(M, 2 * swg::BM) : mblk);
     p.n_blocks = (int)cdiv(N, bn);
     p.k_blocks = (int)kb;
     p.tiles = p.m_blocks * p.n_blocks;
@@ -338,7 +415,7 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
     p.kb_per_split = kbps;
     p.units = p.tiles * splits;
     p.group_m = 16;
-    p.idesc = make_idesc(ti.in_bf16, a_mn, b_mn, swg::BM, bn);
+    p.idesc = make_idesc(ti.in_bf16, a_mn, b_mn, pair ? 2 * swg::BM : swg::BM, bn);
     p.a_mn_major = a_mn;
     p.b_mn_major = b_mn;
     p.alpha = alpha;
@@ -348,9 +425,9 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
     p.out_kind = ti.out_kind;
     p.err = d->err;
 
-    const int grid = (int)std::min<int64_t>(p.units, d->sms);
     cudaError_t e;
     if (splits > 1) {
+        const int grid = (int)std::min<int64_t>(p.units, d->sms);
         const int64_t ld_ws = cdiv(N, 4) * 4;
         Workspace *w = nullptr;
         if (int rc = workspace(d, s, sizeof(float) * (size_t)splits * (size_t)M * (size_t)ld_ws,
@@ -364,7 +441,7 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
             e = swg::launch_splitk_reduce(p, d->sms, s);
         }
     } else {
-        e = swg::launch_tc_store(bn, ta, tb, p, grid, s);
+        e = swg::launch_tc_store(bn, pair, ta, tb, p, tc.units, s);
     }
     if (e != cudaSuccess) return SWG_ERR_CUDA;
     g_launches++;
@@ -403,7 +480,9 @@ int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M, int64_t N
 
     const int64_t N2 = 2 * N;
     static const int cands[] = {256, 128, 64};
-    const int bn = pick_bn(M, N2, d->sms, cands, 3);
+    const TileChoice tc = choose_tiles(d, 1, M, N2, cands, 3);
+    const int bn = tc.bn;
+    const bool pair = tc.pair;
     CUtensorMap ta, tb;
     if (!make_tmap(&ta, A, true, K, M, K, swg::BM) || !make_tmap(&tb, W_fused, true, N2, K, N2, 64))
         return SWG_ERR_CUDA;
@@ -412,7 +491,7 @@ int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M, int64_t N
     p.M = (int)M;
     p.N = (int)N2;
     p.K = (int)K;
-    p.m_blocks = (int)cdiv(M, swg::BM);
+    p.m_blocks = (int)cdiv(M, pair ? 2 * swg::BM : swg::BM);
     p.n_blocks = (int)cdiv(N2, bn);
     p.k_blocks = (int)cdiv(K, swg::BK);
     p.tiles = p.m_blocks * p.n_blocks;
@@ -420,7 +499,7 @@ int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M, int64_t N
     p.kb_per_split = p.k_blocks;
     p.units = p.tiles;
     p.group_m = 16;
-    p.idesc = make_idesc(true, false, true, swg::BM, bn);
+    p.idesc = make_idesc(true, false, true, pair ? 2 * swg::BM : swg::BM, bn);
     p.a_mn_major = 0;
     p.b_mn_major = 1;
     p.alpha = 1.0f;
@@ -429,8 +508,8 @@ int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M, int64_t N
     p.ldd = N;
     p.out_kind = swg::OUT_BF16;
     p.err = d->err;
-    const int grid = (int)std::min<int64_t>(p.units, d->sms);
-    if (swg::launch_tc_swiglu(bn, ta, tb, p, grid, s) != cudaSuccess) return SWG_ERR_CUDA;
+    if (swg::launch_tc_swiglu(bn, pair, ta, tb, p, tc.units, s) != cudaSuccess)
+        return SWG_ERR_CUDA;
     g_launches++;
     return SWG_OK;
 }

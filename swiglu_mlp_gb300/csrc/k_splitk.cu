@@ -106,8 +106,8 @@ cudaError_t launch_tc_splitk(int bn, const CUtensorMap &ta, const CUtensorMap &t
                              const TileParams &p, int grid, cudaStream_t s)
 {
     switch (bn) {
-    case 128: return launch_tc_impl<128, EPI_SPLITK>(ta, tb, p, grid, s);
-    case 256: return launch_tc_impl<256, EPI_SPLITK>(ta, tb, p, grid, s);
+    case 128: return launch_tc_impl<128, EPI_SPLITK, false>(ta, tb, p, grid, s);
+    case 256: return launch_tc_impl<256, EPI_SPLITK, false>(ta, tb, p, grid, s);
     default: return cudaErrorInvalidValue;
     }
 }

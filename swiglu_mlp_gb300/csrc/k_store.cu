@@ -3,14 +3,30 @@
 #include "launch_impl.cuh"
 
 namespace swg {
-cudaError_t launch_tc_store(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
-                            const TileParams &p, int grid, cudaStream_t s)
+cudaError_t launch_tc_store(int bn, bool pair, const CUtensorMap &ta, const CUtensorMap &tb,
+                            const TileParams &p, int units, cudaStream_t s)
+{
+    if (pair) {
+        switch (bn) {
+        case 128: return launch_tc_impl<128, EPI_STORE, true>(ta, tb, p, units, s);
+        case 256: return launch_tc_impl<256, EPI_STORE, true>(ta, tb, p, units, s);
+        default: return cudaErrorInvalidValue;
+        }
+    }
+    switch (bn) {
+    case 64: return launch_tc_impl<64, EPI_STORE, false>(ta, tb, p, units, s);
+    case 128: return launch_tc_impl<128, EPI_STORE, false>(ta, tb, p, units, s);
+    case 256: return launch_tc_impl<256, EPI_STORE, false>(ta, tb, p, units, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+int max_active_pairs_store(int bn, int sms)
 {
     switch (bn) {
-    case 64: return launch_tc_impl<64, EPI_STORE>(ta, tb, p, grid, s);
-    case 128: return launch_tc_impl<128, EPI_STORE>(ta, tb, p, grid, s);
-    case 256: return launch_tc_impl<256, EPI_STORE>(ta, tb, p, grid, s);
-    default: return cudaErrorInvalidValue;
+    case 128: return max_active_pairs_impl<128, EPI_STORE>(sms);
+    case 256: return max_active_pairs_impl<256, EPI_STORE>(sms);
+    default: return 0;
     }
 }
 }  // namespace swg

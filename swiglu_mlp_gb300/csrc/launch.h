@@ -9,18 +9,20 @@
 
 namespace swg {
 
-// Shared-memory bytes the tcgen05 kernel needs for a given BN.
-int tc_smem_bytes(int bn);
-
-// Launches the persistent tcgen05 kernel with the given epilogue.  `bn` is one
-// of the tile widths the TU instantiates; anything else returns
-// cudaErrorInvalidValue without launching.
-cudaError_t launch_tc_store(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
-                            const TileParams &p, int grid, cudaStream_t s);
-cudaError_t launch_tc_swiglu(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
-                             const TileParams &p, int grid, cudaStream_t s);
+// Launch the persistent tcgen05 kernel with the given epilogue.  `bn` is one
+// of the tile widths the TU instantiates (anything else returns
+// cudaErrorInvalidValue without launching); `pair` selects the CTA-pair
+// (cta_group::2, 256-row tile) variant, for which `units` counts pairs.
+cudaError_t launch_tc_store(int bn, bool pair, const CUtensorMap &ta, const CUtensorMap &tb,
+                            const TileParams &p, int units, cudaStream_t s);
+cudaError_t launch_tc_swiglu(int bn, bool pair, const CUtensorMap &ta, const CUtensorMap &tb,
+                             const TileParams &p, int units, cudaStream_t s);
 cudaError_t launch_tc_splitk(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
-                             const TileParams &p, int grid, cudaStream_t s);
+                             const TileParams &p, int units, cudaStream_t s);
+
+// Resident CTA pairs for the pair variants (0 if unknown or not instantiated).
+int max_active_pairs_store(int bn, int sms);
+int max_active_pairs_swiglu(int bn, int sms);
 
 // In-order reduction of the split-K partials into D (alpha, beta, cast),
 // launched as a programmatic dependent of the split-K GEMM on the same stream.

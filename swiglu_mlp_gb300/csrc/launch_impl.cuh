@@ -7,25 +7,72 @@
 
 namespace swg {
 
-// Opt the kernel into its dynamic shared memory once per device.
-template <int BN, int EPI>
+// Opts the kernel into its dynamic shared memory once per device and
+// launches it.  `units` is the number of CTAs (1-CTA mode) or of CTA pairs
+// (PAIR: launched as clusters of two).
+template <int BN, int EPI, bool PAIR>
 cudaError_t launch_tc_impl(const CUtensorMap &ta, const CUtensorMap &tb, const TileParams &p,
-                           int grid, cudaStream_t s)
+                           int units, cudaStream_t s)
 {
+    using C = Cfg<BN, PAIR>;
     static std::atomic<unsigned long long> configured{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
-    auto kernel = tc_gemm_kernel<BN, EPI>;
+    auto kernel = tc_gemm_kernel<BN, EPI, PAIR>;
     if (!(configured.load() & bit)) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Cfg<BN>::SMEM_BYTES);
+                                 C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
-    kernel<<<grid, NUM_THREADS, Cfg<BN>::SMEM_BYTES, s>>>(ta, tb, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (PAIR) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3(2 * units);
+    } else {
+        cfg.gridDim = dim3(units);
+    }
+    return cudaLaunchKernelEx(&cfg, kernel, ta, tb, p);
+}
+
+// How many CTA pairs of this kernel can be resident at once (clusters of two
+// need two free SMs in one GPC); 0 on error.
+template <int BN, int EPI>
+int max_active_pairs_impl(int sms)
+{
+    using C = Cfg<BN, true>;
+    auto kernel = tc_gemm_kernel<BN, EPI, true>;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (sms / 2));
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 }  // namespace swg

@@ -1,7 +1,7 @@
 // tc_gemm.cuh — persistent, warp-specialised tcgen05 GEMM for sm_103a.
 //
 // One CTA per SM walks a static list of output tiles (BM x BN, BM = 128).
-// Roles inside a CTA (192 threads):
+// Roles inside a CTA (320 threads):
 //   warp 0, lane 0 : TMA producer.  For every 64-wide K block it waits for a
 //                    free shared-memory stage, arms the stage's "full" barrier
 //                    with the byte count and issues the tile loads of op(A)
@@ -11,9 +11,10 @@
 //                    tcgen05.mma (M=128, N=BN, K=16, FP32 accumulate) into one
 //                    of two TMEM accumulators and commits each stage back to
 //                    its "empty" barrier, each finished tile to "acc_full".
-//   warps 2..5     : epilogue.  Each thread owns one accumulator row (TMEM
-//                    lane), reads it 32 columns at a time with tcgen05.ld and
-//                    applies the fused epilogue:
+//   warps 2..9     : epilogue.  Each thread owns one accumulator row (TMEM
+//                    lane) and half of the tile's columns (two warps per lane
+//                    quarter), reads them 32 columns at a time with
+//                    tcgen05.ld and applies the fused epilogue:
 //                      EPI_STORE  D = alpha*acc + beta*C, cast, 16-byte stores;
 //                      EPI_SWIGLU Y = SiLU(acc[2j]) * acc[2j+1] per column pair;
 //                      EPI_SPLITK FP32 partial of one K range to the
@@ -51,12 +52,14 @@ enum OutKind { OUT_BF16 = 0, OUT_F16 = 1, OUT_F32 = 2 };
 constexpr int BM = 128;
 constexpr int BK = 64;               // 64 x 16-bit = one 128-byte swizzle row
 constexpr int UMMA_K = 16;           // K of one kind::f16 MMA
-constexpr int NUM_THREADS = 192;
-constexpr int NUM_EPI_THREADS = 128;
+constexpr int NUM_EPI_WARPS = 8;      // two per TMEM lane quarter
+constexpr int NUM_EPI_THREADS = NUM_EPI_WARPS * 32;
+constexpr int NUM_THREADS = 64 + NUM_EPI_THREADS;
 constexpr int EPI_WARP0 = 2;
 constexpr int ERR_TIMEOUT = 6;       // == SWG_ERR_DEVICE_TIMEOUT
 constexpr int MAX_SPLITS = 16;       // split-K ranges per tile (host enforces)
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // pipeline waits
+constexpr uint64_t DRAIN_LIMIT_NS = 1000000ull;      // teardown drains
 
 struct TileParams {
     int M, N, K;                 // N is the 2N-space width for SwiGLU
@@ -78,10 +81,15 @@ struct TileParams {
     int *err;                    // device error word
 };
 
-template <int BN>
+// Tile configuration.  BN is the MMA's N (the tile width).  With PAIR, two
+// CTAs of a cluster share one 256-row MMA: each holds its 128 rows of A and
+// BN/2 columns of B per stage and receives its 128 accumulator rows.
+template <int BN, bool PAIR>
 struct Cfg {
+    static constexpr int TILE_M = PAIR ? 2 * BM : BM;
+    static constexpr int B_COLS = PAIR ? BN / 2 : BN;     // B columns held per CTA
     static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int B_BYTES = B_COLS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES_RAW = (192 * 1024) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
@@ -90,6 +98,7 @@ struct Cfg {
                                    : (2 * BN) <= 128 ? 128 : (2 * BN) <= 256 ? 256 : 512;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 64;
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64, 128, 192 or 256");
+    static_assert(!PAIR || BN % 128 == 0, "pair tiles split B in 64-column boxes per CTA");
 };
 
 // Tile coordinates of work unit u (grouped raster: walk GROUP m-blocks down a
@@ -110,8 +119,13 @@ __device__ __forceinline__ void unit_coords(const TileParams &p, int u, int &mb,
     nb = local / gm;
 }
 
+// Waits for the phase of `bar` with the given parity.  Gives up (returning
+// false) when another role has raised the abort flag, or after `limit_ns`;
+// a time-out raises the abort flag and records ERR_TIMEOUT.  The drain waits
+// at teardown pass honour_abort = false and a short limit.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                             int *err, bool honour_abort = true)
+                                             int *err, bool honour_abort = true,
+                                             uint64_t limit_ns = WAIT_LIMIT_NS)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
@@ -119,7 +133,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 31) == 0) {
             if (honour_abort && *abort_flag) return false;
-            if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
                 atomicCAS(err, 0, ERR_TIMEOUT);
                 return false;
@@ -297,12 +311,12 @@ __device__ __forceinline__ void epi_chunk(const TileParams &p, const uint32_t (&
     }
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const TileParams p)
 {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, PAIR>;
     constexpr int S = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte swizzled stages need 1024-byte alignment.
@@ -321,6 +335,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // Pair mode: rank 0 of the cluster issues the MMAs; work is indexed by
+    // cluster, and this CTA owns rows [128*rank, 128*rank + 128) of the tile.
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int first_unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int unit_step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
     // Split-K: let the reduction kernel queued behind this one be scheduled
     // now; it waits (griddepcontrol.wait) until this grid has completed.
@@ -333,7 +353,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&acc_full[b]), 1);
-            mbar_init(smem_u32(&acc_empty[b]), NUM_EPI_THREADS);
+            // one arrival per epilogue warp, from both CTAs in pair mode
+            mbar_init(smem_u32(&acc_empty[b]), NUM_EPI_WARPS * (PAIR ? 2 : 1));
         }
         mbar_init(smem_u32(mma_done), 1);
         *abort_flag = 0;
@@ -342,11 +363,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_desc(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(smem_u32(tmem_holder), C::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    // Pair mode: the peer's loads signal the leader's barriers, so both CTAs'
+    // barriers must be initialised before either starts.
+    if (PAIR)
+        cluster_sync_all();
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
@@ -357,37 +388,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             uint32_t armed = 0, armed_parity = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+            for (int u = first_unit; u < p.units && ok; u += unit_step) {
                 int mb, nb, split, tile;
                 unit_coords(p, u, mb, nb, split, tile);
                 const int kb0 = split * p.kb_per_split;
                 int kb1 = kb0 + p.kb_per_split;
                 kb1 = kb1 < p.k_blocks ? kb1 : p.k_blocks;
-                const int m0 = mb * BM, n0 = nb * BN;
+                const int m0 = mb * C::TILE_M + (int)rank * BM;
+                const int n0 = nb * BN + (int)rank * C::B_COLS;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bounded(smem_u32(&empty[stage]), phase ^ 1, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = smem_u32(&full[stage]);
-                    mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                    const uint32_t fb_local = smem_u32(&full[stage]);
+                    uint32_t fb = fb_local;
+                    if (PAIR) {
+                        // both CTAs' bytes complete on the leader's barrier
+                        fb = mapa_shared(fb_local, 0);
+                        if (leader) mbar_arrive_expect_tx(fb_local, 2 * C::STAGE_BYTES);
+                    } else {
+                        mbar_arrive_expect_tx(fb_local, C::STAGE_BYTES);
+                    }
                     armed |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     const uint32_t a_dst = smem_u32(sA + stage * C::A_BYTES);
                     const uint32_t b_dst = smem_u32(sB + stage * C::B_BYTES);
                     const int k0 = kb * BK;
+                    auto load = [&](uint32_t dst, const CUtensorMap *tm, int x, int y) {
+                        if (PAIR)
+                            tma_load_2d_pair(dst, tm, fb, x, y);
+                        else
+                            tma_load_2d(dst, tm, fb, x, y);
+                    };
                     if (!p.a_mn_major) {
-                        tma_load_2d(a_dst, &tmA, fb, k0, m0);               // box {64 K, 128 M}
+                        load(a_dst, &tmA, k0, m0);                          // box {64 K, 128 M}
                     } else {
-                        tma_load_2d(a_dst, &tmA, fb, m0, k0);               // box {64 M, 64 K}
-                        tma_load_2d(a_dst + 8192, &tmA, fb, m0 + 64, k0);
+                        load(a_dst, &tmA, m0, k0);                          // box {64 M, 64 K}
+                        load(a_dst + 8192, &tmA, m0 + 64, k0);
                     }
                     if (!p.b_mn_major) {
-                        tma_load_2d(b_dst, &tmB, fb, k0, n0);               // box {64 K, BN N}
+                        load(b_dst, &tmB, k0, n0);                          // box {64 K, B_COLS N}
                     } else {
 #pragma unroll
-                        for (int c = 0; c < BN / 64; ++c)                   // box {64 N, 64 K}
-                            tma_load_2d(b_dst + c * 8192, &tmB, fb, n0 + c * 64, k0);
+                        for (int c = 0; c < C::B_COLS / 64; ++c)            // box {64 N, 64 K}
+                            load(b_dst + c * 8192, &tmB, n0 + c * 64, k0);
                     }
                     if (++stage == S) {
                         stage = 0;
@@ -396,15 +441,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             // Never leave with loads in flight into this CTA's shared memory.
-            for (int s = 0; s < S; ++s)
-                if (armed & (1u << s))
-                    wait_bounded(smem_u32(&full[s]), (armed_parity >> s) & 1, abort_flag, p.err,
-                                 false);
+            if (!PAIR || leader) {
+                for (int s = 0; s < S; ++s)
+                    if (armed & (1u << s))
+                        wait_bounded(smem_u32(&full[s]), (armed_parity >> s) & 1, abort_flag,
+                                     p.err, false, DRAIN_LIMIT_NS);
+            } else if (!ok) {
+                // The peer's loads complete on the leader's barriers, which
+                // it cannot poll; after an abort give them time to land.
+                const uint64_t t0 = global_timer_ns();
+                while (global_timer_ns() - t0 < 200000ull) {
+                }
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             // K-major operand: next K=16 slice is 32 bytes further in the
             // swizzled row; MN-major: two 8-row K groups (2 x 1024 bytes) further.
             const uint32_t a_kstep = p.a_mn_major ? 2048u : 32u;
@@ -415,7 +468,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             bool ok = true;
             int t = 0;
-            for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++t) {
+            for (int u = first_unit; u < p.units && ok; u += unit_step, ++t) {
                 int mb, nb, split, tile;
                 unit_coords(p, u, mb, nb, split, tile);
                 const int kb0 = split * p.kb_per_split;
@@ -441,28 +494,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                         const uint64_t ad = smem_desc(a_base + kk * a_kstep, a_lbo, 1024);
                         const uint64_t bd = smem_desc(b_base + kk * b_kstep, b_lbo, 1024);
-                        tc_mma_f16(d_tmem, ad, bd, p.idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                        const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
+                        if (PAIR)
+                            tc_mma_f16_pair(d_tmem, ad, bd, p.idesc, accum);
+                        else
+                            tc_mma_f16(d_tmem, ad, bd, p.idesc, accum);
                     }
-                    tc_commit(smem_u32(&empty[stage]));
+                    if (PAIR)
+                        tc_commit_pair(smem_u32(&empty[stage]));
+                    else
+                        tc_commit(smem_u32(&empty[stage]));
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
                 if (!ok) break;
-                tc_commit(smem_u32(&acc_full[acc]));
+                if (PAIR)
+                    tc_commit_pair(smem_u32(&acc_full[acc]));
+                else
+                    tc_commit(smem_u32(&acc_full[acc]));
             }
             // Never free TMEM under a running MMA.
-            tc_commit(smem_u32(mma_done));
-            wait_bounded(smem_u32(mma_done), 0, abort_flag, p.err, false);
+            if (PAIR)
+                tc_commit_pair_local(smem_u32(mma_done));
+            else
+                tc_commit(smem_u32(mma_done));
+            wait_bounded(smem_u32(mma_done), 0, abort_flag, p.err, false, DRAIN_LIMIT_NS);
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
+        // Warp w may only read TMEM lanes 32*(w%4) .. 32*(w%4)+31; warps 2..5
+        // take the first half of the tile's 32-column chunks, warps 6..9 the
+        // second half.
         const int q = warp & 3;                 // TMEM lane quarter of this warp
         const int row = q * 32 + lane;
+        constexpr int NC = BN / 32;             // 32-column chunks per tile (>= 2)
+        const int c_begin = ((warp - EPI_WARP0) / 4) * (NC / 2);
+        const int c_end = c_begin + NC / 2;
         int t = 0;
-        for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++t) {
+        for (int u = first_unit; u < p.units; u += unit_step, ++t) {
             int mb, nb, split, tile;
             unit_coords(p, u, mb, nb, split, tile);
             const int acc = t & 1;
@@ -472,33 +544,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-            const int m = mb * BM + row;
+            const int m = mb * C::TILE_M + (int)rank * BM + row;
             const bool row_ok = m < p.M;
             // Two register buffers: the load of chunk c+1 is in flight while
             // chunk c is converted and stored (tcgen05.wait::ld waits for all
             // earlier loads, so each wait retires exactly the older chunk).
             uint32_t ra[32], rb[32];
-            tmem_ld_32cols(t_row, ra);
+            tmem_ld_32cols(t_row + c_begin * 32, ra);
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; c += 2) {
+            for (int c = c_begin; c < c_end; c += 2) {
                 tmem_ld_wait(ra);
-                tmem_ld_32cols(t_row + (c + 1) * 32, rb);
+                if (c + 1 < c_end) tmem_ld_32cols(t_row + (c + 1) * 32, rb);
                 if (row_ok) epi_chunk<EPI>(p, ra, m, nb * BN + c * 32, split);
-                tmem_ld_wait(rb);
-                if (c + 2 < BN / 32) tmem_ld_32cols(t_row + (c + 2) * 32, ra);
-                if (row_ok) epi_chunk<EPI>(p, rb, m, nb * BN + (c + 1) * 32, split);
+                if (c + 1 < c_end) {
+                    tmem_ld_wait(rb);
+                    if (c + 2 < c_end) tmem_ld_32cols(t_row + (c + 2) * 32, ra);
+                    if (row_ok) epi_chunk<EPI>(p, rb, m, nb * BN + (c + 1) * 32, split);
+                }
             }
-            // Accumulator drained: hand it back to the MMA warp.
+            // Accumulator drained: hand it back to the MMA warp (the leader's
+            // barrier in pair mode), one arrival per warp.
             tc_fence_before();
-            mbar_arrive(smem_u32(&acc_empty[acc]));
+            __syncwarp();
+            if (lane == 0) {
+                if (PAIR)
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[acc]), 0));
+                else
+                    mbar_arrive(smem_u32(&acc_empty[acc]));
+            }
         }
     }
 
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
-    __syncthreads();
+    // Pair mode: neither CTA may free its tensor memory or exit while the
+    // leader's MMAs or the peer's arrivals can still reach it.
+    if (PAIR)
+        cluster_sync_all();
+    else
+        __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if (warp == 1) {
+        if (PAIR)
+            tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
 }
 
 }  // namespace swg

@@ -1,0 +1,69 @@
+"""Both tile shapes of the tcgen05 kernels against the oracle.
+
+The library picks, per call, single-CTA 128-row tiles or CTA-pair 256-row
+tiles (two CTAs of a cluster sharing one cta_group::2 MMA, each holding half
+of B).  SWG_TILE_MODE forces one or the other so both are checked on the same
+ragged shapes, all four op combinations, and the fused SwiGLU epilogue.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import swiglu_mlp_gb300 as swg
+import synth
+from helpers import check_half, padded, round_up, to_f64
+
+pytestmark = pytest.mark.gpu
+
+MODES = ["1cta", "2cta128", "2cta256"]
+
+
+@pytest.fixture
+def tile_mode(request, monkeypatch):
+    monkeypatch.setenv("SWG_TILE_MODE", request.param)
+    return request.param
+
+
+@pytest.mark.parametrize("tile_mode", MODES, indirect=True)
+@pytest.mark.parametrize("tA,tB", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("shape", [(256, 256, 128), (300, 520, 200), (129, 392, 72),
+                                   (1000, 640, 1024), (64, 256, 64)])
+def test_gemm_tile_modes(tile_mode, tA, tB, shape):
+    M, N, K = shape
+    g = synth.generator(M * 7 + N * 3 + K + 11 * tA + 13 * tB)
+    A = synth.normal(synth.stored_shape(tA, M, K), g)
+    B = synth.normal(synth.stored_shape(tB, K, N), g)
+    C = synth.normal((M, N), g)
+    lda, ldb, ldc = round_up(A.shape[1], 8), round_up(B.shape[1], 8), round_up(N, 8)
+    Ap, Bp, Cp = padded(A, lda, 2.0), padded(B, ldb, 2.0), padded(C, ldc, 4.0)
+    Cd = Cp.cuda()
+    swg.gemm(tA, tB, M, N, K, 0.5, Ap.cuda(), lda, Bp.cuda(), ldb, 1.0, Cd, ldc, swg.BF16)
+    assert swg.get_device_error() == 0
+    out = Cd.cpu()
+    assert torch.equal(out[:, N:], Cp[:, N:])
+    yhat = oracle.gemm(tA, tB, M, N, K, 0.5, Ap, lda, Bp, ldb, 1.0, Cp, ldc)
+    check_half(to_f64(out[:, :N]), yhat, f"{tile_mode} {shape} tA={tA} tB={tB}")
+
+
+@pytest.mark.parametrize("tile_mode", MODES, indirect=True)
+@pytest.mark.parametrize("M,K,N", [(256, 256, 128), (300, 136, 520), (640, 896, 1216)])
+def test_swiglu_tile_modes(tile_mode, M, K, N):
+    A, W1, W2 = synth.swiglu(M, K, N, seed=M + K, w_std=0.08)
+    Wf = torch.from_numpy(oracle.interleave(W1, W2, K, N).view(np.int16)).view(torch.bfloat16)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    swg.swiglu_mlp(A.cuda(), Wf.cuda(), Y, M, N, K)
+    assert swg.get_device_error() == 0
+    check_half(to_f64(Y), oracle.swiglu(A, W1, W2, M, N, K), f"{tile_mode} swiglu {M}x{K}x{N}")
+
+
+@pytest.mark.parametrize("tile_mode", ["1cta", "2cta256"], indirect=True)
+def test_square_4096_tile_modes(tile_mode):
+    M = N = K = 4096
+    A, B, _ = synth.gemm_bf16(M, N, K, 0, 0, seed=1)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    swg.gemm(0, 0, M, N, K, 1.0, A.cuda(), K, B.cuda(), N, 0.0, D, N, swg.BF16)
+    assert swg.get_device_error() == 0
+    rows = [0, 255, 256, 2049, M - 1]
+    yhat = oracle.gemm(0, 0, M, N, K, 1.0, A, K, B, N, 0.0, rows=rows)
+    check_half(to_f64(D)[rows], yhat, f"{tile_mode} 4096^3")
