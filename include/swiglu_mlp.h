@@ -140,6 +140,41 @@ SWG_API int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M,
 SWG_API int swiglu_interleave(const void *W1, const void *W2, void *W_fused,
                       int64_t K, int64_t N, void *stream);
 
+/*
+ * gemm_splitk_noalloc — the split-K form of gemm that allocates no device
+ * memory.  The pages have no counterpart to this call; it exists for callers
+ * that cannot call cudaMalloc once they are running, for example a host
+ * framework that already holds nearly all device memory in its own pool, or a
+ * serving loop that forbids cudaMalloc/cudaFree because they can synchronise
+ * the whole device.
+ *
+ * It computes exactly what gemm_ex computes (same arguments, same rules, same
+ * fixed-order reduction, split_k with the same meaning, but always through
+ * the split-K kernels) and launches the same two kernels.  The FP32 partial
+ * sums go to a fixed array of SWG_NOALLOC_SCRATCH_BYTES that is part of the
+ * library's device image: every GPU that loads the library holds it until the
+ * process exits.  The caller still passes A, B and C.
+ *
+ *   Limit        the partials need splits * M * round_up(N, 4) * 4 bytes; a
+ *                call that would need more than SWG_NOALLOC_SCRATCH_BYTES
+ *                returns SWG_ERR_UNSUPPORTED and launches nothing (pick a
+ *                smaller split_k, or use gemm / gemm_ex).
+ *   Allocation   none: no cudaMalloc, cudaFree or allocating library call.
+ *   First call   on each device looks up the array's device address
+ *                (cudaGetSymbolAddress) with that device current; make that
+ *                first call before any stream capture.
+ *   Sharing      all calls, on every stream, use the one array and it keeps
+ *                the last call's contents (each call writes every partial it
+ *                reads, so nothing needs clearing).  Calls that overlap on the
+ *                GPU race with each other: order them, e.g. on one stream.
+ */
+#define SWG_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+SWG_API int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N,
+                                int64_t K, float alpha, const void *A,
+                                int64_t lda, const void *B, int64_t ldb,
+                                float beta, void *C, int64_t ldc, int dtype,
+                                int split_k, void *stream);
+
 /* Human-readable name of a swg_status value (static string, never NULL). */
 SWG_API const char *swg_status_string(int status);
 

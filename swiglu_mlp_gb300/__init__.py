@@ -18,7 +18,7 @@ import threading
 
 __all__ = [
     "SwgError", "OP_N", "OP_T", "F16_F32OUT", "BF16", "F16", "BF16_F32OUT",
-    "gemm", "gemm_ex", "swiglu_mlp", "swiglu_interleave", "status_string",
+    "gemm", "gemm_ex", "gemm_splitk_noalloc", "swiglu_mlp", "swiglu_interleave", "status_string",
     "get_device_error", "launch_count", "shutdown", "gemm_into",
     "swiglu_mlp_into", "interleave_weights", "library_path", "load",
 ]
@@ -62,6 +62,9 @@ def load():
         lib.gemm_ex.argtypes = [i32, i32, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, i32,
                                 i32, vp]
         lib.gemm_ex.restype = i32
+        lib.gemm_splitk_noalloc.argtypes = [i32, i32, i64, i64, i64, f32, vp, i64, vp, i64,
+                                            f32, vp, i64, i32, i32, vp]
+        lib.gemm_splitk_noalloc.restype = i32
         lib.swiglu_mlp.argtypes = [vp, vp, vp, i64, i64, i64, vp]
         lib.swiglu_mlp.restype = i32
         lib.swiglu_interleave.argtypes = [vp, vp, vp, i64, i64, vp]
@@ -115,6 +118,18 @@ def gemm_ex(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtype,
     return _check(load().gemm_ex(int(transA), int(transB), int(M), int(N), int(K), float(alpha),
                                  _ptr(A), int(lda), _ptr(B), int(ldb), float(beta), _ptr(C),
                                  int(ldc), int(dtype), int(split_k), _stream(stream)), "gemm_ex")
+
+
+def gemm_splitk_noalloc(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtype,
+                        split_k=0, stream=None):
+    """Split-K GEMM that allocates no device memory: its partial sums live in
+    a fixed array inside the library (see the C header for the size limit and
+    the sharing rules)."""
+    return _check(load().gemm_splitk_noalloc(int(transA), int(transB), int(M), int(N), int(K),
+                                             float(alpha), _ptr(A), int(lda), _ptr(B), int(ldb),
+                                             float(beta), _ptr(C), int(ldc), int(dtype),
+                                             int(split_k), _stream(stream)),
+                  "gemm_splitk_noalloc")
 
 
 def swiglu_mlp(A, W_fused, Y, M, N, K, stream=None):

@@ -564,3 +564,149 @@ void swg_shutdown(void)
 }
 
 }  // extern "C"
+
+// =================================================================== no-allocation split-K
+//
+// gemm_splitk_noalloc runs the same split-K kernels as gemm_ex, but its FP32
+// partial sums live in a fixed array that is part of the library's device
+// image instead of in a workspace obtained with cudaMalloc.  It is for callers
+// that must not allocate device memory once they are running: for example a
+// host framework that has already reserved nearly all device memory in its
+// own pool (so a cudaMalloc would fail or fragment it), or a serving loop
+// that forbids cudaMalloc/cudaFree because they can synchronise the device.
+
+namespace {
+
+constexpr size_t kNoallocScratchFloats = SWG_NOALLOC_SCRATCH_BYTES / sizeof(float);
+
+// The partials.  Every GPU that loads this library holds these bytes until
+// the process exits.  All calls share them; a call overwrites every element it
+// later reads, so nothing here needs to start at zero.
+static __device__ __align__(256) float g_noalloc_scratch[kNoallocScratchFloats];
+
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+bool g_noalloc_ready[kNoallocMaxDevices];
+float *g_noalloc_ptr[kNoallocMaxDevices];   // device address of g_noalloc_scratch
+int *g_noalloc_err[kNoallocMaxDevices];     // device address of g_err_word
+int g_noalloc_sms[kNoallocMaxDevices];
+
+// Once per device, with that device current: the device addresses of the
+// scratch array and of the error word.  In host code the symbols themselves
+// are host-side stand-ins, so kernels must be given these addresses instead.
+int noalloc_setup(int &dev)
+{
+    if (cudaGetDevice(&dev) != cudaSuccess) return SWG_ERR_CUDA;
+    if (dev < 0 || dev >= kNoallocMaxDevices) return SWG_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_ready[dev]) return SWG_OK;
+    void *scratch = nullptr, *err = nullptr;
+    if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess) return SWG_ERR_CUDA;
+    if (cudaGetSymbolAddress(&err, g_err_word) != cudaSuccess) return SWG_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return SWG_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<float *>(scratch);
+    g_noalloc_err[dev] = static_cast<int *>(err);
+    g_noalloc_sms[dev] = sms;
+    g_noalloc_ready[dev] = true;
+    return SWG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
+                        const void *A, int64_t lda, const void *B, int64_t ldb, float beta,
+                        void *C, int64_t ldc, int dtype, int split_k, void *stream)
+{
+    TypeInfo ti;
+    if (!type_info(dtype, ti)) return SWG_ERR_UNSUPPORTED;
+    if ((transA != SWG_OP_N && transA != SWG_OP_T) || (transB != SWG_OP_N && transB != SWG_OP_T))
+        return SWG_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0 || split_k < 0) return SWG_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return SWG_OK;
+    const int64_t a_cols = transA ? M : K, b_cols = transB ? K : N;
+    if (C == nullptr || ldc < N) return SWG_ERR_INVALID_ARG;
+    if (K > 0 && (A == nullptr || B == nullptr || lda < a_cols || ldb < b_cols))
+        return SWG_ERR_INVALID_ARG;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim || ldc > kMaxDim || lda > kMaxDim ||
+        ldb > kMaxDim)
+        return SWG_ERR_UNSUPPORTED;
+    if (!aligned16(C) || (ldc * ti.out_bytes) % 16 != 0) return SWG_ERR_MISALIGNED;
+    if (K > 0 && (!aligned16(A) || !aligned16(B) || (lda * 2) % 16 != 0 || (ldb * 2) % 16 != 0))
+        return SWG_ERR_MISALIGNED;
+
+    // Split factor, as gemm_ex chooses it, but never below one range.
+    const int64_t kb = cdiv(K, swg::BK);
+    const int64_t tiles = cdiv(M, swg::BM) * cdiv(N, 256);
+    int splits = 1;
+    int dev = 0;
+    if (int rc = noalloc_setup(dev)) return rc;
+    const int sms = g_noalloc_sms[dev];
+    if (split_k == 0) {
+        if (tiles * 2 <= sms && kb >= 8) splits = (int)std::min<int64_t>(sms / tiles, kb / 4);
+    } else {
+        splits = (int)std::min<int64_t>(split_k, kb);
+    }
+    splits = std::max(1, std::min(splits, swg::MAX_SPLITS));
+    int kbps = (int)std::max<int64_t>(kb, 1);
+    if (kb > 0) {
+        kbps = (int)cdiv(kb, splits);
+        splits = (int)cdiv(kb, kbps);
+    }
+    const int64_t ld_ws = cdiv(N, 4) * 4;
+    if ((uint64_t)splits * (uint64_t)M * (uint64_t)ld_ws > kNoallocScratchFloats)
+        return SWG_ERR_UNSUPPORTED;   // partials would not fit in the fixed array
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        scale_kernel<<<grid_for(M * N, sms), 256, 0, s>>>(C, ldc, (int)M, (int)N, beta,
+                                                           ti.out_kind);
+        g_launches++;
+        return cudaGetLastError() == cudaSuccess ? SWG_OK : SWG_ERR_CUDA;
+    }
+
+    const int bn = 256;
+    const bool a_mn = transA == SWG_OP_T;
+    const bool b_mn = transB == SWG_OP_N;
+    CUtensorMap ta, tb;
+    bool ok = a_mn ? make_tmap(&ta, A, ti.in_bf16, M, K, lda, 64)
+                   : make_tmap(&ta, A, ti.in_bf16, K, M, lda, swg::BM);
+    ok = ok && (b_mn ? make_tmap(&tb, B, ti.in_bf16, N, K, ldb, 64)
+                     : make_tmap(&tb, B, ti.in_bf16, K, N, ldb, bn));
+    if (!ok) return SWG_ERR_CUDA;
+
+    TileParams p{};
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.m_blocks = (int)cdiv(M, swg::BM);
+    p.n_blocks = (int)cdiv(N, bn);
+    p.k_blocks = (int)kb;
+    p.tiles = p.m_blocks * p.n_blocks;
+    p.splits = splits;
+    p.kb_per_split = kbps;
+    p.units = p.tiles * splits;
+    p.group_m = 16;
+    p.idesc = make_idesc(ti.in_bf16, a_mn, b_mn, swg::BM, bn);
+    p.a_mn_major = a_mn;
+    p.b_mn_major = b_mn;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.D = C;
+    p.ldd = ldc;
+    p.out_kind = ti.out_kind;
+    p.ws = g_noalloc_ptr[dev];
+    p.ld_ws = ld_ws;
+    p.err = g_noalloc_err[dev];
+    const int grid = (int)std::min<int64_t>(p.units, sms);
+    if (swg::launch_tc_splitk(bn, ta, tb, p, grid, s) != cudaSuccess) return SWG_ERR_CUDA;
+    g_launches++;
+    if (swg::launch_splitk_reduce(p, sms, s) != cudaSuccess) return SWG_ERR_CUDA;
+    g_launches++;
+    return SWG_OK;
+}
+
+}  // extern "C"
