@@ -17,7 +17,7 @@
 #include <mutex>
 #include <vector>
 
-#include "../../include/swiglu_mlp.h"
+#include "swiglu_mlp.h"
 #include "launch.h"
 
 namespace {
@@ -261,6 +261,81 @@ TileChoice choose_tiles(DeviceState *d, int kind, int64_t M, int64_t N, const in
     return c;
 }
 
+// Split-K GEMM with swapped operands for M <= 64: the kernel computes
+// D^T = op(B)^T op(A)^T with op(B)^T (N x K) as its 128-row operand and
+// op(A)^T as its BN-column operand, writes transposed FP32 partials
+// ws[split][m][n], and the usual in-order reduction forms D.
+int splitk_swapped(DeviceState *d, const TypeInfo &ti, int transA, int transB, int64_t M,
+                   int64_t N, int64_t K, float alpha, const void *A, int64_t lda, const void *B,
+                   int64_t ldb, float beta, void *C, int64_t ldc, int split_k, cudaStream_t s)
+{
+    const int64_t kb = cdiv(K, swg::BK);
+    // op(A)^T is the kernel's B operand: K-major when A is stored M x K
+    // (op N), MN-major (one 64-wide atom) when stored K x M (op T).
+    const bool bT_mn = transA == SWG_OP_T;
+    const int bn = bT_mn ? 64 : (M <= 16 ? 16 : M <= 32 ? 32 : 64);
+    const int64_t tiles = cdiv(N, swg::BM) * cdiv(M, bn);
+    int splits;
+    if (split_k == 0)
+        splits = (int)std::min<int64_t>(std::max<int64_t>(d->sms / tiles, 1), std::max<int64_t>(kb / 4, 1));
+    else
+        splits = (int)std::min<int64_t>(split_k, kb);
+    splits = std::max(1, std::min(splits, swg::MAX_SPLITS));
+    const int kbps = (int)cdiv(kb, splits);
+    splits = (int)cdiv(kb, kbps);
+
+    // op(B)^T is the kernel's A operand: MN-major when B is stored K x N (op N).
+    const bool aT_mn = transB == SWG_OP_N;
+    CUtensorMap ta, tb;
+    bool ok = aT_mn ? make_tmap(&ta, B, ti.in_bf16, N, K, ldb, 64)
+                    : make_tmap(&ta, B, ti.in_bf16, K, N, ldb, swg::BM);
+    ok = ok && (bT_mn ? make_tmap(&tb, A, ti.in_bf16, M, K, lda, 64)
+                      : make_tmap(&tb, A, ti.in_bf16, K, M, lda, bn));
+    if (!ok) return SWG_ERR_CUDA;
+
+    const int64_t ld_ws = cdiv(N, 4) * 4;
+    Workspace *w = nullptr;
+    if (int rc = workspace(d, s, sizeof(float) * (size_t)splits * (size_t)M * (size_t)ld_ws, w))
+        return rc;
+
+    TileParams p{};           // in the kernel's (transposed) frame
+    p.M = (int)N;
+    p.N = (int)M;
+    p.K = (int)K;
+    p.m_blocks = (int)cdiv(N, swg::BM);
+    p.n_blocks = (int)cdiv(M, bn);
+    p.k_blocks = (int)kb;
+    p.tiles = p.m_blocks * p.n_blocks;
+    p.splits = splits;
+    p.kb_per_split = kbps;
+    p.units = p.tiles * splits;
+    p.group_m = 16;
+    p.idesc = make_idesc(ti.in_bf16, aT_mn, bT_mn, swg::BM, bn);
+    p.a_mn_major = aT_mn;
+    p.b_mn_major = bT_mn;
+    p.ws = static_cast<float *>(w->base);
+    p.ld_ws = ld_ws;
+    p.err = d->err;
+    const int grid = (int)std::min<int64_t>(p.units, d->sms);
+    if (swg::launch_tc_splitk_t(bn, ta, tb, p, grid, s) != cudaSuccess) return SWG_ERR_CUDA;
+    g_launches++;
+
+    TileParams r{};           // the reduction works in the output's frame
+    r.M = (int)M;
+    r.N = (int)N;
+    r.splits = splits;
+    r.alpha = alpha;
+    r.beta = beta;
+    r.D = C;
+    r.ldd = ldc;
+    r.out_kind = ti.out_kind;
+    r.ws = p.ws;
+    r.ld_ws = ld_ws;
+    if (swg::launch_splitk_reduce(r, d->sms, s) != cudaSuccess) return SWG_ERR_CUDA;
+    g_launches++;
+    return SWG_OK;
+}
+
 // ----------------------------------------------------------------- small kernels
 
 __global__ void scale_kernel(void *D, long long ldd, int M, int N, float beta, int out_kind)
@@ -381,6 +456,12 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
         splits = (int)std::min<int64_t>(split_k, kb);
     }
     splits = std::min(splits, swg::MAX_SPLITS);
+    // Few rows and a split K: compute the transposed product instead, so the
+    // large operand fills the MMA's 128 rows and the <= 64 rows of op(A)
+    // become its N (smaller stages, deeper pipeline, fewer partials).
+    if (splits > 1 && M <= 64)
+        return splitk_swapped(d, ti, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C,
+                              ldc, split_k, static_cast<cudaStream_t>(stream));
     int kbps = (int)kb;
     if (splits > 1) {
         kbps = (int)cdiv(kb, splits);

@@ -20,6 +20,11 @@ cudaError_t launch_tc_swiglu(int bn, bool pair, const CUtensorMap &ta, const CUt
 cudaError_t launch_tc_splitk(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
                              const TileParams &p, int units, cudaStream_t s);
 
+// Split-K with swapped operands (the kernel computes the transposed product;
+// `bn` 16, 32 or 64 is the width of the original rows it covers).
+cudaError_t launch_tc_splitk_t(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
+                               const TileParams &p, int units, cudaStream_t s);
+
 // Resident CTA pairs for the pair variants (0 if unknown or not instantiated).
 int max_active_pairs_store(int bn, int sms);
 int max_active_pairs_swiglu(int bn, int sms);

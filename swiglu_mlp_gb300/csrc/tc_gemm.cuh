@@ -46,7 +46,11 @@
 
 namespace swg {
 
-enum EpiKind { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SPLITK = 2 };
+// EPI_SPLITK_T: split-K with swapped operands.  The kernel computes the
+// transposed product (its rows are the output's columns), so each thread owns
+// one output column and its registers hold output rows; the partial is written
+// transposed back to ws[split][row][column].
+enum EpiKind { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SPLITK = 2, EPI_SPLITK_T = 3 };
 enum OutKind { OUT_BF16 = 0, OUT_F16 = 1, OUT_F32 = 2 };
 
 constexpr int BM = 128;
@@ -91,13 +95,15 @@ struct Cfg {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = B_COLS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    // 192 KB of stages (measured: a seventh 32 KB pair stage did not help
+    // and shrank L1), at most 12.
     static constexpr int STAGES_RAW = (192 * 1024) / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+    static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
     static constexpr int NUM_BARS = 2 * STAGES + 5;
     static constexpr int TMEM_COLS = (2 * BN) <= 32 ? 32 : (2 * BN) <= 64 ? 64
                                    : (2 * BN) <= 128 ? 128 : (2 * BN) <= 256 ? 256 : 512;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 64;
-    static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64, 128, 192 or 256");
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "BN must be a multiple of 16, <= 256");
     static_assert(!PAIR || BN % 128 == 0, "pair tiles split B in 64-column boxes per CTA");
 };
 
@@ -344,7 +350,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     // Split-K: let the reduction kernel queued behind this one be scheduled
     // now; it waits (griddepcontrol.wait) until this grid has completed.
-    if (EPI == EPI_SPLITK) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (EPI == EPI_SPLITK || EPI == EPI_SPLITK_T)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -523,6 +530,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             wait_bounded(smem_u32(mma_done), 0, abort_flag, p.err, false, DRAIN_LIMIT_NS);
         }
         __syncwarp();
+    } else if (EPI == EPI_SPLITK_T) {
+        // ------------------------------------------------- epilogue (swapped)
+        // TMEM lane = output column n (kernel row), TMEM column j = output row
+        // m (kernel column).  BN <= 32: warps 2..5 read all BN columns; BN = 64:
+        // warps 2..5 take columns 0..31 and warps 6..9 columns 32..63.
+        constexpr int W = BN >= 32 ? 32 : 16;
+        const int q = warp & 3;
+        const int h = (warp - EPI_WARP0) / 4;
+        const bool active = (BN == 64) || h == 0;
+        const int j0 = BN == 64 ? h * 32 : 0;
+        int t = 0;
+        for (int u = first_unit; u < p.units; u += unit_step, ++t) {
+            int mb, nb, split, tile;
+            unit_coords(p, u, mb, nb, split, tile);
+            const int acc = t & 1;
+            const uint32_t acc_phase = (t >> 1) & 1;
+            bool ok = wait_bounded(smem_u32(&acc_full[acc]), acc_phase, abort_flag, p.err);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            if (active) {
+                uint32_t r[W];
+                tmem_ld_cols(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + j0, r);
+                tmem_ld_wait(r);
+                const int n = mb * BM + q * 32 + lane;          // output column
+                if (n < p.M) {
+#pragma unroll
+                    for (int j = 0; j < W; ++j) {
+                        const int m = nb * BN + j0 + j;         // output row
+                        if (m < p.N)
+                            p.ws[((long long)split * p.N + m) * p.ld_ws + n] = __uint_as_float(r[j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&acc_empty[acc]));
+        }
     } else {
         // ------------------------------------------------------------ epilogue
         // Warp w may only read TMEM lanes 32*(w%4) .. 32*(w%4)+31; warps 2..5

@@ -92,3 +92,29 @@ def test_split_and_unsplit_agree():
     torch.cuda.synchronize()
     d = (D1 - D2).abs().max().item()
     assert d <= 1e-4 * np.sqrt(K) * D1.abs().max().item()
+
+
+@pytest.mark.parametrize("M", [1, 7, 16, 17, 33, 64])
+@pytest.mark.parametrize("tA,tB", [(0, 0), (1, 1)])
+@pytest.mark.parametrize("split_k", [0, 4])
+def test_few_rows_swapped_operands(M, tA, tB, split_k):
+    """M <= 64 with a split K runs the transposed product (the large operand
+    on the MMA's 128 rows); ragged N and K, beta != 0."""
+    N, K = 520, 2056
+    g = synth.generator(200 + M + 2 * tA + tB + split_k)
+    A = synth.normal(synth.stored_shape(tA, M, K), g)
+    B = synth.normal(synth.stored_shape(tB, K, N), g)
+    C = synth.normal((M, N), g)
+    lda = ((A.shape[1] + 7) // 8) * 8
+    from helpers import padded
+    Ap = padded(A, lda, 7.0)
+    Cd = torch.zeros((M, 528), dtype=torch.bfloat16)
+    Cd[:, :N] = C
+    Cd = Cd.cuda()
+    swg.gemm_ex(tA, tB, M, N, K, 1.25, Ap.cuda(), lda, B.cuda(), B.shape[1], -0.5, Cd, 528,
+                swg.BF16, split_k)
+    assert swg.get_device_error() == 0
+    out = Cd.cpu()
+    assert torch.all(out[:, N:] == 0)
+    yhat = oracle.gemm(tA, tB, M, N, K, 1.25, Ap, lda, B, B.shape[1], -0.5, C, N)
+    check_half(to_f64(out[:, :N]), yhat, f"swapped M={M} tA={tA} tB={tB} split={split_k}")
