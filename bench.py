@@ -63,7 +63,7 @@ def kernel_source_digest() -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "swiglu_mlp_gb300", "csrc")
-    for name in ("tc_gemm.cuh", "ptx.cuh"):
+    for name in ("tc_gemm.cuh", "ptx.cuh", "api.cu"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -185,13 +185,16 @@ def time_oracle_sample(rows: int, cols: int, trans=(0, 0), A=None, B=None):
     return dt, 2.0 * rows * cols * SIZE, min(oracle.num_cores(), rows)
 
 
-def cpu_baseline(target_s: float = 12.0, cols: int = 2048):
-    """Oracle throughput on a bounded sample sized to about target_s seconds."""
+def cpu_baseline(target_s: float = 12.0):
+    """Oracle throughput on a bounded sample: every row and a number of columns
+    sized to about target_s seconds (the oracle's cost, including widening the
+    sampled columns of B, is linear in the column count)."""
     import synth
     A, B, _ = synth.gemm_bf16(SIZE, SIZE, SIZE, 0, 0, seed=1)
-    dt, _, _ = time_oracle_sample(64, cols, A=A, B=B)
-    rows = int(max(64, min(SIZE, 64 * target_s / max(dt, 1e-3))))
-    rows = (rows // 64) * 64
+    rows = SIZE
+    dt, _, _ = time_oracle_sample(rows, 32, A=A, B=B)
+    cols = int(max(32, min(SIZE, 32 * target_s / max(dt, 1e-3))))
+    cols = (cols // 32) * 32
     dt, flops, cores = time_oracle_sample(rows, cols, A=A, B=B)
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{rows} rows x {cols} columns of the op(A)=A, op(B)=B 8192^3 GEMM "

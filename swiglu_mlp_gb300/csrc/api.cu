@@ -495,7 +495,9 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
     p.splits = splits;
     p.kb_per_split = kbps;
     p.units = p.tiles * splits;
-    p.group_m = 16;
+    // Raster groups: about as many A panels as B panels per wave of tiles
+    // (256-row pair tiles: 8 m-blocks; 128-row tiles: 16).
+    p.group_m = pair ? 8 : 16;
     p.idesc = make_idesc(ti.in_bf16, a_mn, b_mn, pair ? 2 * swg::BM : swg::BM, bn);
     p.a_mn_major = a_mn;
     p.b_mn_major = b_mn;
@@ -579,7 +581,7 @@ int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M, int64_t N
     p.splits = 1;
     p.kb_per_split = p.k_blocks;
     p.units = p.tiles;
-    p.group_m = 16;
+    p.group_m = pair ? 8 : 16;
     p.idesc = make_idesc(true, false, true, pair ? 2 * swg::BM : swg::BM, bn);
     p.a_mn_major = 0;
     p.b_mn_major = 1;

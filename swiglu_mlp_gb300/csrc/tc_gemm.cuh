@@ -380,13 +380,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     tc_fence_before();
     // Pair mode: the peer's loads signal the leader's barriers, so both CTAs'
-    // barriers must be initialised before either starts.
-    if (PAIR)
+    // barriers must be initialised before either starts.  Single CTA: the
+    // producer initialised the barriers itself and needs no tensor memory, so
+    // it starts loading at once and only releases the other warps, which
+    // wait for the barrier set-up and the TMEM address.
+    if (PAIR) {
         cluster_sync_all();
-    else
-        __syncthreads();
+    } else if (warp == 0) {
+        __syncwarp();
+        named_bar_arrive(2, NUM_THREADS);
+    } else {
+        named_bar_sync(2, NUM_THREADS);
+    }
     tc_fence_after();
-    const uint32_t tmem_base = *tmem_holder;
+    const uint32_t tmem_base = (PAIR || warp != 0) ? *tmem_holder : 0u;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
