@@ -416,6 +416,8 @@ def component_cases():
     cases = [(f"swiglu_small_M{m}", "swiglu", m, 896, 4864) for m in (128, 512, 2048)]
     cases += [(f"swiglu_8b_M{m}", "swiglu", m, 4096, 14336) for m in (512, 2048, 8192)]
     cases += [(f"skinny_splitk_M{m}", "skinny", m, 16384, 4096) for m in (16, 32, 64)]
+    cases += [(f"decode_gemv_M{m}", "gemv", m, 4096, 4096) for m in (1, 8)]
+    cases += [("mlp_small_M2048", "mlp", 2048, 896, 4864), ("mlp_8b_M2048", "mlp", 2048, 4096, 14336)]
     return cases
 
 
@@ -446,6 +448,31 @@ def build_case(kind, M, K, N, dev, stream):
         def reset():
             Cd.copy_(C0)
         return fn, reset, 2.0 * M * N * K, (M * K + K * N + 2 * M * N) * 2
+    if kind == "mlp":
+        # Out = (SiLU(A W1) (.) (A W2)) W_down + Out (residual, beta = 1)
+        A, W1, W2 = synth.swiglu(M, K, N, seed=3)
+        Wd = synth.normal((N, K), synth.generator(6), std=0.02).to(dev)
+        Ad = A.to(dev)
+        Wf = swg.interleave_weights(W1.to(dev), W2.to(dev), stream=stream)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        R = synth.normal((M, K), synth.generator(7)).to(dev)
+        Out = R.clone()
+
+        def fn():
+            swg.swiglu_mlp_forward(Ad, Wf, Wd, Y, Out, M, N, K, 1.0, stream=stream)
+
+        def reset():
+            Out.copy_(R)
+        return fn, reset, 6.0 * M * N * K, (M * K + K * 2 * N + N * K + 2 * M * K) * 2
+    if kind == "gemv":
+        g = synth.generator(5)
+        A = synth.normal((M, K), g).to(dev)
+        B = synth.normal((K, N), g).to(dev)
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+        def fn():
+            swg.gemm(0, 0, M, N, K, 1.0, A, K, B, N, 0.0, D, N, swg.BF16, stream=stream)
+        return fn, None, 2.0 * M * N * K, (M * K + K * N + M * N) * 2
     if kind.startswith("gemm"):
         tA, tB = {"gemm_nn": (0, 0), "gemm_nt": (0, 1), "gemm_tn": (1, 0),
                   "gemm_tt": (1, 1)}[kind]
@@ -496,7 +523,7 @@ def run_components(args, dev, stream):
                  "tflops": round(flops / med / 1e9, 1), "gbs": round(byts / med / 1e6, 1),
                  "roofline_frac": round(max(t_tensor, t_hbm) / (med / 1e3), 4),
                  "bound": "tensor" if t_tensor > t_hbm else "hbm"}
-        if kind == "skinny":
+        if kind in ("skinny", "gemv"):
             entry["hbm_frac"] = round(byts / med / 1e6 / bw, 4)
         res[name] = entry
     if swg.get_device_error(stream) != 0:
@@ -516,7 +543,11 @@ def run_profile_case(args):
     table = {c[0]: c[1:] for c in component_cases()}
     for t in ("nn", "nt", "tn", "tt"):
         table[f"gemm8192_{t}"] = (f"gemm_{t}", SIZE, SIZE, SIZE)
-    kind, M, K, N = table[args.profile_case]
+    name = args.profile_case
+    if name.startswith("gemm_") and "x" in name:       # gemm_MxNxK (op N, op N)
+        M, N, K = (int(v) for v in name[5:].split("x"))
+        table[name] = ("gemm_nn", M, K, N)
+    kind, M, K, N = table[name]
     fn, reset, _, _ = build_case(kind, M, K, N, dev, stream)
     for _ in range(2 + args.profile_launches):
         if reset:

@@ -131,6 +131,31 @@ SWG_API int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M,
                int64_t N, int64_t K, void *stream);
 
 /*
+ * swiglu_mlp_forward — the whole gated MLP of a transformer block:
+ *     Out = (SiLU(A * W1) (.) (A * W2)) * W_down + beta * Out
+ * "GEMM o Coração Matemático", §13.3 (the feed-forward block as two GEMMs
+ * around an activation) with the gated activation of "Sobreposição de
+ * Ativação em Nível de Tile para Inferência Eficiente de LLM", Definição do
+ * Problema.  beta = 1 adds a residual already held in Out.
+ *
+ *   A        bfloat16, M x K, row stride K (K = model width).
+ *   W_fused  bfloat16, K x 2N, row stride 2N (interleaved Gate/Up, as for
+ *            swiglu_mlp).
+ *   W_down   bfloat16, N x K, row stride K.
+ *   Y        bfloat16, M x N, row stride N: receives the gated activation
+ *            (caller-owned; Gate and Up themselves never reach memory).
+ *   Out      bfloat16, M x K, row stride K: read when beta != 0, written.
+ *   Two kernels run on `stream`: swiglu_mlp's fused kernel, then gemm.
+ *   Alignment: pointers 16-byte aligned, K % 8 == 0, N % 8 == 0, else
+ *   SWG_ERR_MISALIGNED.  M == 0 or K == 0: nothing to do.  All arguments are
+ *   checked before the first launch.
+ */
+SWG_API int swiglu_mlp_forward(const void *A, const void *W_fused,
+                               const void *W_down, void *Y, void *Out,
+                               int64_t M, int64_t N, int64_t K, float beta,
+                               void *stream);
+
+/*
  * swiglu_interleave — builds W_fused (K x 2N, row stride 2N) from W1 and W2
  * (each K x N, row stride N), bfloat16: column 2n <- W1 column n (Gate),
  * column 2n+1 <- W2 column n (Up).  Same page and section as swiglu_mlp.

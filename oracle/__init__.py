@@ -17,6 +17,8 @@ computes, with the passage it follows:
   Inferência Eficiente de LLM", Definição do Problema; Metodologia, Kernel-2).
 * :func:`interleave` — W_fused with even columns from W1 (Gate) and odd columns
   from W2 (Up) (same page, Metodologia, Kernel-2).
+* :func:`mlp` — the full gated MLP, (SiLU(A W1) (.) (A W2)) W_down + beta * Out
+  ("GEMM o Coração Matemático", §13.3, with the gated activation above).
 * :func:`silu`, :func:`f16_to_f64`, :func:`bf16_to_f64` — the scalar pieces.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` against values and
@@ -69,6 +71,8 @@ def _load():
             lib.orc_swiglu.argtypes = [vp, i64, vp, vp, i64, i64, i64, i64, vp, i64, vp, i64,
                                        vp, i32]
             lib.orc_swiglu.restype = i32
+            lib.orc_mlp.argtypes = [vp, vp, vp, vp, vp, f64, i64, i64, i64, vp, i64, vp, i32]
+            lib.orc_mlp.restype = i32
             lib.orc_interleave.argtypes = [vp, vp, vp, i64, i64]
             lib.orc_interleave.restype = None
             lib.orc_silu.argtypes = [f64]
@@ -161,6 +165,23 @@ def swiglu(A, W1, W2, M: int, N: int, K: int, rows=None, threads: int = 0,
                         _ptr(cs), n_cols, out.ctypes.data, int(threads))
     if rc != 0:
         raise ValueError("oracle swiglu rejected its arguments")
+    return out
+
+
+def mlp(A, W1, W2, Wd, M: int, N: int, K: int, beta: float = 0.0, Out_old=None, rows=None,
+        threads: int = 0) -> np.ndarray:
+    """Out = (SiLU(A W1) (.) (A W2)) W_down + beta * Out_old in double: A is
+    M x K, W1 and W2 K x N, W_down N x K, Out_old M x K, all bf16 (Out_old read
+    only when beta != 0).  The gated activation is not rounded."""
+    lib = _load()
+    a, w1, w2, wd = (_as_buffer(x, "bf16") for x in (A, W1, W2, Wd))
+    o = _as_buffer(Out_old, "bf16") if beta != 0.0 else None
+    r, n_rows = _rows(rows, M)
+    out = np.empty((n_rows, K), dtype=np.float64)
+    rc = lib.orc_mlp(_ptr(a), _ptr(w1), _ptr(w2), _ptr(wd), _ptr(o), float(beta), M, N, K,
+                     _ptr(r), n_rows, out.ctypes.data, int(threads))
+    if rc != 0:
+        raise ValueError("oracle mlp rejected its arguments")
     return out
 
 

@@ -266,3 +266,41 @@ int orc_num_cores(void)
     long c = sysconf(_SC_NPROCESSORS_ONLN);
     return c > 0 ? (int)c : 1;
 }
+
+/* ---- full gated MLP -------------------------------------------------- */
+
+/* Out = Y * W_down + beta * Out_old with Y = SiLU(A W1) (.) (A W2) kept in
+ * double (not rounded).  The FFN of "GEMM o Coração Matemático", §13.3 (two
+ * GEMMs around an activation), with the gated activation of "Sobreposição de
+ * Ativação em Nível de Tile ...", Definição do Problema.  A: M x K bf16,
+ * W1/W2: K x N bf16, W_down: N x K bf16, Out_old: M x K bf16 (read only when
+ * beta != 0).  Out: n_rows x K doubles for rows[] (all when rows == NULL). */
+int orc_mlp(const uint16_t *A, const uint16_t *W1, const uint16_t *W2,
+            const uint16_t *Wd, const uint16_t *Out_old, double beta, int64_t M,
+            int64_t N, int64_t K, const int64_t *rows, int64_t n_rows,
+            double *Out, int n_threads)
+{
+    if (!rows && n_rows != M) return -1;
+    if (n_rows == 0 || K == 0) return 0;
+    double *Y = (double *)malloc(sizeof(double) * (size_t)(n_rows * (N > 0 ? N : 1)));
+    if (!Y) return -1;
+    int rc = orc_swiglu(A, K, W1, W2, N, M, N, K, rows, n_rows, NULL, N, Y, n_threads);
+    if (rc == 0) {
+        for (int64_t r = 0; r < n_rows; ++r) {
+            const int64_t i = rows ? rows[r] : r;
+            double *o = Out + r * K;
+            for (int64_t k = 0; k < K; ++k)
+                o[k] = 0.0;
+            for (int64_t n = 0; n < N; ++n) {        /* ascending n for each o[k] */
+                const double y = Y[r * N + n];
+                for (int64_t k = 0; k < K; ++k)
+                    o[k] += y * orc_bf16_to_f64(Wd[n * K + k]);
+            }
+            if (beta != 0.0)
+                for (int64_t k = 0; k < K; ++k)
+                    o[k] += beta * orc_bf16_to_f64(Out_old[i * K + k]);
+        }
+    }
+    free(Y);
+    return rc;
+}

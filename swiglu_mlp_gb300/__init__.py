@@ -18,7 +18,7 @@ import threading
 
 __all__ = [
     "SwgError", "OP_N", "OP_T", "F16_F32OUT", "BF16", "F16", "BF16_F32OUT",
-    "gemm", "gemm_ex", "gemm_splitk_noalloc", "swiglu_mlp", "swiglu_interleave", "status_string",
+    "gemm", "gemm_ex", "gemm_splitk_noalloc", "swiglu_mlp", "swiglu_mlp_forward", "swiglu_interleave", "status_string",
     "get_device_error", "launch_count", "shutdown", "gemm_into",
     "swiglu_mlp_into", "interleave_weights", "library_path", "load",
 ]
@@ -67,6 +67,8 @@ def load():
         lib.gemm_splitk_noalloc.restype = i32
         lib.swiglu_mlp.argtypes = [vp, vp, vp, i64, i64, i64, vp]
         lib.swiglu_mlp.restype = i32
+        lib.swiglu_mlp_forward.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, f32, vp]
+        lib.swiglu_mlp_forward.restype = i32
         lib.swiglu_interleave.argtypes = [vp, vp, vp, i64, i64, vp]
         lib.swiglu_interleave.restype = i32
         lib.swg_status_string.argtypes = [i32]
@@ -136,6 +138,13 @@ def swiglu_mlp(A, W_fused, Y, M, N, K, stream=None):
     """Y = SiLU(A W1) (.) (A W2) over the interleaved W_fused (see the C header)."""
     return _check(load().swiglu_mlp(_ptr(A), _ptr(W_fused), _ptr(Y), int(M), int(N), int(K),
                                     _stream(stream)), "swiglu_mlp")
+
+
+def swiglu_mlp_forward(A, W_fused, W_down, Y, Out, M, N, K, beta=0.0, stream=None):
+    """Out = (SiLU(A W1) (.) (A W2)) W_down + beta * Out (see the C header)."""
+    return _check(load().swiglu_mlp_forward(_ptr(A), _ptr(W_fused), _ptr(W_down), _ptr(Y),
+                                            _ptr(Out), int(M), int(N), int(K), float(beta),
+                                            _stream(stream)), "swiglu_mlp_forward")
 
 
 def swiglu_interleave(W1, W2, W_fused, K, N, stream=None):

@@ -188,7 +188,8 @@ int pick_bn(int64_t M, int64_t N, int sms, const int *cands, int ncand)
     return best;
 }
 
-// Resident CTA pairs of a pair kernel (kind 0 = GEMM store, 1 = SwiGLU).
+// Resident CTA pairs of a pair kernel (kind 0 = GEMM store, 1 = SwiGLU,
+// 2 = split-K partials).
 int max_pairs(DeviceState *d, int kind, int bn)
 {
     const int key = kind * 1024 + bn;
@@ -197,8 +198,9 @@ int max_pairs(DeviceState *d, int kind, int bn)
         auto it = d->max_pairs.find(key);
         if (it != d->max_pairs.end()) return it->second;
     }
-    const int n = kind == 0 ? swg::max_active_pairs_store(bn, d->sms)
-                            : swg::max_active_pairs_swiglu(bn, d->sms);
+    const int n = kind == 0   ? swg::max_active_pairs_store(bn, d->sms)
+                  : kind == 1 ? swg::max_active_pairs_swiglu(bn, d->sms)
+                              : swg::max_active_pairs_splitk(bn, d->sms);
     std::lock_guard<std::mutex> lk(g_mu);
     d->max_pairs[key] = n;
     return n;
@@ -237,9 +239,15 @@ TileChoice choose_tiles(DeviceState *d, int kind, int64_t M, int64_t N, const in
     const int mode = forced_tile_mode(&only_bn);
     bool try_pair = (M > swg::BM && mode != 1) || mode == 2;
     if (try_pair) {
-        static const int pair_bns[] = {256, 128};
+        // 128-wide pair tiles measured well below 256-wide ones (they load
+        // 24 KB per 256 MMA cycles), so only a forced mode selects them.
+        static const int pair_bns_auto[] = {256};
+        static const int pair_bns_forced[] = {256, 128};
+        const int *pair_bns = only_bn ? pair_bns_forced : pair_bns_auto;
+        const int n_pair_bns = only_bn ? 2 : 1;
         double best = -1.0;
-        for (int bn : pair_bns) {
+        for (int i = 0; i < n_pair_bns; ++i) {
+            const int bn = pair_bns[i];
             if (only_bn && bn != only_bn) continue;
             const int slots = max_pairs(d, kind, bn);
             if (slots <= 0) continue;
@@ -444,12 +452,19 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
 
     const int64_t kb = cdiv(K, swg::BK);
     const int64_t mblk = cdiv(M, swg::BM);
+    // Tile shape first (single-CTA or CTA pair, and width), then the split:
+    // K is split when the tiles would fill at most half of the slots that
+    // shape can keep resident ("为什么 GEMM 是 CUDA 的必修课", 关键技术 item 5).
+    static const int cands[] = {256, 128};
+    TileChoice tc = choose_tiles(d, 0, M, N, cands, 2);
+    const bool pair = tc.pair;
+    const int bn = tc.bn;
+    const int64_t tiles = (pair ? cdiv(M, 2 * swg::BM) : mblk) * cdiv(N, bn);
+    const int slots = pair ? max_pairs(d, 2, bn) : d->sms;
     int splits = 1;
-    int bn = 256;
     if (split_k == 0) {
-        const int64_t tiles256 = mblk * cdiv(N, 256);
-        if (tiles256 * 2 <= d->sms && kb >= 8) {
-            splits = (int)std::min<int64_t>(d->sms / tiles256, kb / 4);
+        if (slots > 0 && tiles * 2 <= slots && kb >= 8) {
+            splits = (int)std::min<int64_t>(slots / tiles, kb / 4);
             if (splits < 2) splits = 1;
         }
     } else if (split_k > 1) {
@@ -467,13 +482,6 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
         kbps = (int)cdiv(kb, splits);
         splits = (int)cdiv(kb, kbps);
     }
-    TileChoice tc;
-    if (splits <= 1) {
-        static const int cands[] = {256, 128};
-        tc = choose_tiles(d, 0, M, N, cands, 2);
-        bn = tc.bn;
-    }
-    const bool pair = tc.pair;
 
     const bool a_mn = transA == SWG_OP_T;
     const bool b_mn = transB == SWG_OP_N;
@@ -510,7 +518,7 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
 
     cudaError_t e;
     if (splits > 1) {
-        const int grid = (int)std::min<int64_t>(p.units, d->sms);
+        const int units = (int)std::min<int64_t>(p.units, slots);
         const int64_t ld_ws = cdiv(N, 4) * 4;
         Workspace *w = nullptr;
         if (int rc = workspace(d, s, sizeof(float) * (size_t)splits * (size_t)M * (size_t)ld_ws,
@@ -518,7 +526,7 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
             return rc;
         p.ws = static_cast<float *>(w->base);
         p.ld_ws = ld_ws;
-        e = swg::launch_tc_splitk(bn, ta, tb, p, grid, s);
+        e = swg::launch_tc_splitk(bn, pair, ta, tb, p, units, s);
         if (e == cudaSuccess) {
             g_launches++;
             e = swg::launch_splitk_reduce(p, d->sms, s);
@@ -595,6 +603,26 @@ int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M, int64_t N
         return SWG_ERR_CUDA;
     g_launches++;
     return SWG_OK;
+}
+
+int swiglu_mlp_forward(const void *A, const void *W_fused, const void *W_down, void *Y, void *Out,
+                       int64_t M, int64_t N, int64_t K, float beta, void *stream)
+{
+    // Everything both launches need is checked first, so a rejected call
+    // writes nothing.
+    if (M < 0 || N < 0 || K < 0) return SWG_ERR_INVALID_ARG;
+    if (M == 0 || K == 0) return SWG_OK;          // Out is M x K
+    if (Out == nullptr || A == nullptr || W_fused == nullptr) return SWG_ERR_INVALID_ARG;
+    if (N > 0 && (Y == nullptr || W_down == nullptr)) return SWG_ERR_INVALID_ARG;
+    if (M > kMaxDim || 2 * N > kMaxDim || K > kMaxDim) return SWG_ERR_UNSUPPORTED;
+    if (!aligned16(Out) || !aligned16(A) || !aligned16(W_fused) || K % 8 != 0)
+        return SWG_ERR_MISALIGNED;
+    if (N > 0 && (!aligned16(Y) || !aligned16(W_down) || N % 8 != 0)) return SWG_ERR_MISALIGNED;
+    // Y = SiLU(A W1) (.) (A W2) through the fused kernel, then the down
+    // projection Out = Y W_down + beta * Out through gemm.
+    if (int rc = swiglu_mlp(A, W_fused, Y, M, N, K, stream)) return rc;
+    return gemm(SWG_OP_N, SWG_OP_N, M, K, N, 1.0f, Y, N, W_down, K, beta, Out, K, SWG_BF16,
+                stream);
 }
 
 int swiglu_interleave(const void *W1, const void *W2, void *W_fused, int64_t K, int64_t N,
@@ -785,7 +813,7 @@ int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N, int64_t K,
     p.ld_ws = ld_ws;
     p.err = g_noalloc_err[dev];
     const int grid = (int)std::min<int64_t>(p.units, sms);
-    if (swg::launch_tc_splitk(bn, ta, tb, p, grid, s) != cudaSuccess) return SWG_ERR_CUDA;
+    if (swg::launch_tc_splitk(bn, false, ta, tb, p, grid, s) != cudaSuccess) return SWG_ERR_CUDA;
     g_launches++;
     if (swg::launch_splitk_reduce(p, sms, s) != cudaSuccess) return SWG_ERR_CUDA;
     g_launches++;

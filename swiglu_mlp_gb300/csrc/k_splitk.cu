@@ -102,13 +102,29 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-cudaError_t launch_tc_splitk(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
-                             const TileParams &p, int grid, cudaStream_t s)
+cudaError_t launch_tc_splitk(int bn, bool pair, const CUtensorMap &ta, const CUtensorMap &tb,
+                             const TileParams &p, int units, cudaStream_t s)
+{
+    if (pair) {
+        switch (bn) {
+        case 128: return launch_tc_impl<128, EPI_SPLITK, true>(ta, tb, p, units, s);
+        case 256: return launch_tc_impl<256, EPI_SPLITK, true>(ta, tb, p, units, s);
+        default: return cudaErrorInvalidValue;
+        }
+    }
+    switch (bn) {
+    case 128: return launch_tc_impl<128, EPI_SPLITK, false>(ta, tb, p, units, s);
+    case 256: return launch_tc_impl<256, EPI_SPLITK, false>(ta, tb, p, units, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+int max_active_pairs_splitk(int bn, int sms)
 {
     switch (bn) {
-    case 128: return launch_tc_impl<128, EPI_SPLITK, false>(ta, tb, p, grid, s);
-    case 256: return launch_tc_impl<256, EPI_SPLITK, false>(ta, tb, p, grid, s);
-    default: return cudaErrorInvalidValue;
+    case 128: return max_active_pairs_impl<128, EPI_SPLITK>(sms);
+    case 256: return max_active_pairs_impl<256, EPI_SPLITK>(sms);
+    default: return 0;
     }
 }
 

@@ -17,7 +17,7 @@ cudaError_t launch_tc_store(int bn, bool pair, const CUtensorMap &ta, const CUte
                             const TileParams &p, int units, cudaStream_t s);
 cudaError_t launch_tc_swiglu(int bn, bool pair, const CUtensorMap &ta, const CUtensorMap &tb,
                              const TileParams &p, int units, cudaStream_t s);
-cudaError_t launch_tc_splitk(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
+cudaError_t launch_tc_splitk(int bn, bool pair, const CUtensorMap &ta, const CUtensorMap &tb,
                              const TileParams &p, int units, cudaStream_t s);
 
 // Split-K with swapped operands (the kernel computes the transposed product;
@@ -28,6 +28,7 @@ cudaError_t launch_tc_splitk_t(int bn, const CUtensorMap &ta, const CUtensorMap 
 // Resident CTA pairs for the pair variants (0 if unknown or not instantiated).
 int max_active_pairs_store(int bn, int sms);
 int max_active_pairs_swiglu(int bn, int sms);
+int max_active_pairs_splitk(int bn, int sms);
 
 // In-order reduction of the split-K partials into D (alpha, beta, cast),
 // launched as a programmatic dependent of the split-K GEMM on the same stream.

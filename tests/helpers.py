@@ -66,3 +66,21 @@ def report(y: np.ndarray, yhat: np.ndarray) -> dict:
     rel = err / np.maximum(np.abs(yhat), 1e-30)
     return {"max_abs": float(err.max()), "max_rel": float(rel.max()),
             "frac_rel_gt_1pct": float((rel > 1e-2).mean())}
+
+
+def check_two_stage(y, yhat, prop_bound, what=""):
+    """Output of a composition whose intermediate is stored in bf16 (the full
+    MLP: Y in bf16 between its two GEMMs).  The single-GEMM bound is widened by
+    the propagated rounding of the intermediate, prop_bound = 2^-8 * |Y| |W|
+    computed from the oracle's exact intermediate (2^-8 covers the bf16 store,
+    2^-9, plus the FP32 arithmetic before it)."""
+    assert y.shape == yhat.shape
+    assert np.isfinite(y).all(), f"{what}: non-finite outputs"
+    err = np.abs(y - yhat)
+    bound = ATOL + RTOL * np.abs(yhat) + prop_bound
+    bad = err > bound
+    if bad.any():
+        idx = np.argwhere(bad)[:5].tolist()
+        raise AssertionError(f"{what}: {int(bad.sum())} elements out of tolerance, e.g. {idx}; "
+                             f"{report(y, yhat)}")
+    return report(y, yhat)

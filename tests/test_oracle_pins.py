@@ -303,3 +303,35 @@ def test_swiglu_equals_two_gemms_plus_elementwise():
     Wf = oracle.interleave(W1, W2, K, N)
     assert np.array_equal(Wf[:, 0::2], W1.view(torch.int16).numpy().view(np.uint16))
     assert np.array_equal(Wf[:, 1::2], W2.view(torch.int16).numpy().view(np.uint16))
+
+
+def test_mlp_identity_down_projection_and_residual():
+    """With W_down = I (N = K) the MLP returns the gated activation itself, and
+    beta = 1 adds the residual; both exact in double."""
+    M, K = 6, 16
+    A, W1, W2 = synth.swiglu(M, K, K, seed=31, w_std=0.2)
+    eye = torch.eye(K, dtype=torch.bfloat16)
+    Y = oracle.swiglu(A, W1, W2, M, K, K)
+    assert np.array_equal(oracle.mlp(A, W1, W2, eye, M, K, K), Y)
+    R = synth.small_ints((M, K), synth.generator(32), -3, 3)
+    got = oracle.mlp(A, W1, W2, eye, M, K, K, beta=1.0, Out_old=R)
+    assert np.array_equal(got, Y + R.to(torch.float64).numpy())
+
+
+def test_mlp_down_projection_bruteforce():
+    """The down projection of the (pinned) gated activation, checked element
+    by element with Python floats summed in the same order; scaling W_down by
+    2 doubles the output exactly."""
+    M, N, K = 4, 10, 6
+    A, W1, W2 = synth.swiglu(M, K, N, seed=33, w_std=0.3)
+    Wd = synth.small_ints((N, K), synth.generator(34), -2, 2)
+    Y = oracle.swiglu(A, W1, W2, M, N, K)
+    Wdf = Wd.to(torch.float64).tolist()
+    out = oracle.mlp(A, W1, W2, Wd, M, N, K)
+    for i in range(M):
+        for k in range(K):
+            s = 0.0
+            for n in range(N):
+                s += Y[i, n] * Wdf[n][k]
+            assert out[i, k] == s
+    assert np.array_equal(oracle.mlp(A, W1, W2, (2 * Wd).to(torch.bfloat16), M, N, K), 2 * out)

@@ -118,3 +118,22 @@ def test_few_rows_swapped_operands(M, tA, tB, split_k):
     assert torch.all(out[:, N:] == 0)
     yhat = oracle.gemm(tA, tB, M, N, K, 1.25, Ap, lda, B, B.shape[1], -0.5, C, N)
     check_half(to_f64(out[:, :N]), yhat, f"swapped M={M} tA={tA} tB={tB} split={split_k}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8])
+@pytest.mark.parametrize("tA,tB", [(0, 0), (0, 1), (1, 0), (1, 1)])
+def test_decode_gemv_shapes(M, tA, tB):
+    """Decode-time GEMV: M = 1..8 rows against a 4096 x 4096 weight (about one
+    FLOP per byte, "GEMM o Coração Matemático" §14), every output checked."""
+    N = K = 4096
+    g = synth.generator(300 + M + 2 * tA + tB)
+    A = synth.normal(synth.stored_shape(tA, M, K), g)
+    B = synth.normal(synth.stored_shape(tB, K, N), g)
+    lda = ((A.shape[1] + 7) // 8) * 8
+    from helpers import padded
+    Ap = padded(A, lda, 5.0)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    swg.gemm(tA, tB, M, N, K, 1.0, Ap.cuda(), lda, B.cuda(), B.shape[1], 0.0, D, N, swg.BF16)
+    assert swg.get_device_error() == 0
+    yhat = oracle.gemm(tA, tB, M, N, K, 1.0, Ap, lda, B, B.shape[1], 0.0)
+    check_half(to_f64(D), yhat, f"gemv M={M} tA={tA} tB={tB}")

@@ -67,3 +67,24 @@ def test_square_4096_tile_modes(tile_mode):
     rows = [0, 255, 256, 2049, M - 1]
     yhat = oracle.gemm(0, 0, M, N, K, 1.0, A, K, B, N, 0.0, rows=rows)
     check_half(to_f64(D)[rows], yhat, f"{tile_mode} 4096^3")
+
+
+@pytest.mark.parametrize("tile_mode", ["1cta", "2cta128", "2cta256"], indirect=True)
+@pytest.mark.parametrize("split_k", [2, 3])
+@pytest.mark.parametrize("tA,tB", [(0, 0), (1, 1), (0, 1)])
+def test_split_k_both_tile_shapes(tile_mode, split_k, tA, tB):
+    """Split-K partials from single-CTA and CTA-pair tiles (M > 64, so the
+    operands are not swapped), reduced in split order."""
+    M, N, K = 300, 520, 1000
+    g = synth.generator(400 + split_k + 3 * tA + tB)
+    A = synth.normal(synth.stored_shape(tA, M, K), g)
+    B = synth.normal(synth.stored_shape(tB, K, N), g)
+    C = synth.normal((M, N), g)
+    lda, ldb = round_up(A.shape[1], 8), round_up(B.shape[1], 8)
+    Ap, Bp = padded(A, lda, 2.0), padded(B, ldb, 2.0)
+    Cd = C.cuda()
+    swg.gemm_ex(tA, tB, M, N, K, 0.75, Ap.cuda(), lda, Bp.cuda(), ldb, 0.5, Cd, N, swg.BF16,
+                split_k)
+    assert swg.get_device_error() == 0
+    yhat = oracle.gemm(tA, tB, M, N, K, 0.75, Ap, lda, Bp, ldb, 0.5, C, N)
+    check_half(to_f64(Cd), yhat, f"{tile_mode} split={split_k} tA={tA} tB={tB}")
