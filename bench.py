@@ -418,6 +418,8 @@ def component_cases():
     cases += [(f"skinny_splitk_M{m}", "skinny", m, 16384, 4096) for m in (16, 32, 64)]
     cases += [(f"decode_gemv_M{m}", "gemv", m, 4096, 4096) for m in (1, 8)]
     cases += [("mlp_small_M2048", "mlp", 2048, 896, 4864), ("mlp_8b_M2048", "mlp", 2048, 4096, 14336)]
+    cases += [("swiglu_dual_small_M2048", "dual", 2048, 896, 4864),
+              ("swiglu_dual_8b_M2048", "dual", 2048, 4096, 14336)]
     return cases
 
 
@@ -448,6 +450,14 @@ def build_case(kind, M, K, N, dev, stream):
         def reset():
             Cd.copy_(C0)
         return fn, reset, 2.0 * M * N * K, (M * K + K * N + 2 * M * N) * 2
+    if kind == "dual":
+        A, W1, W2 = synth.swiglu(M, K, N, seed=3)
+        Ad, W1d, W2d = A.to(dev), W1.to(dev), W2.to(dev)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+        def fn():
+            swg.swiglu_mlp_dual(Ad, W1d, W2d, Y, M, N, K, stream=stream)
+        return fn, None, 2.0 * M * 2 * N * K, (M * K + 2 * K * N + M * N) * 2
     if kind == "mlp":
         # Out = (SiLU(A W1) (.) (A W2)) W_down + Out (residual, beta = 1)
         A, W1, W2 = synth.swiglu(M, K, N, seed=3)

@@ -131,6 +131,26 @@ SWG_API int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M,
                int64_t N, int64_t K, void *stream);
 
 /*
+ * swiglu_mlp_dual — the same Y = SiLU(A * W1) (.) (A * W2), computed directly
+ * from SEPARATE W1 and W2 with no interleaved copy of the weights.
+ *
+ * Defined by "Sobreposição de Ativação em Nível de Tile para Inferência
+ * Eficiente de LLM", Metodologia, Kernel-1 (Gate and Up from their own weight
+ * matrices, SiLU on the Gate accumulator, the product formed in the
+ * epilogue).  One kernel: each output tile's accumulator holds the Gate
+ * columns in its first half and the matching Up columns in its second half,
+ * and the epilogue stores SiLU(gate) * up; neither reaches memory.
+ *
+ *   A       bfloat16, M x K, row stride K.
+ *   W1, W2  bfloat16, each K x N, row stride N.
+ *   Y       bfloat16, M x N, row stride N (written).
+ *   Alignment, sizes and the K == 0 case as for swiglu_mlp.
+ */
+SWG_API int swiglu_mlp_dual(const void *A, const void *W1, const void *W2,
+                            void *Y, int64_t M, int64_t N, int64_t K,
+                            void *stream);
+
+/*
  * swiglu_mlp_forward — the whole gated MLP of a transformer block:
  *     Out = (SiLU(A * W1) (.) (A * W2)) * W_down + beta * Out
  * "GEMM o Coração Matemático", §13.3 (the feed-forward block as two GEMMs

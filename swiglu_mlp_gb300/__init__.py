@@ -18,7 +18,7 @@ import threading
 
 __all__ = [
     "SwgError", "OP_N", "OP_T", "F16_F32OUT", "BF16", "F16", "BF16_F32OUT",
-    "gemm", "gemm_ex", "gemm_splitk_noalloc", "swiglu_mlp", "swiglu_mlp_forward", "swiglu_interleave", "status_string",
+    "gemm", "gemm_ex", "gemm_splitk_noalloc", "swiglu_mlp", "swiglu_mlp_dual", "swiglu_mlp_forward", "swiglu_interleave", "status_string",
     "get_device_error", "launch_count", "shutdown", "gemm_into",
     "swiglu_mlp_into", "interleave_weights", "library_path", "load",
 ]
@@ -67,6 +67,8 @@ def load():
         lib.gemm_splitk_noalloc.restype = i32
         lib.swiglu_mlp.argtypes = [vp, vp, vp, i64, i64, i64, vp]
         lib.swiglu_mlp.restype = i32
+        lib.swiglu_mlp_dual.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
+        lib.swiglu_mlp_dual.restype = i32
         lib.swiglu_mlp_forward.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, f32, vp]
         lib.swiglu_mlp_forward.restype = i32
         lib.swiglu_interleave.argtypes = [vp, vp, vp, i64, i64, vp]
@@ -138,6 +140,12 @@ def swiglu_mlp(A, W_fused, Y, M, N, K, stream=None):
     """Y = SiLU(A W1) (.) (A W2) over the interleaved W_fused (see the C header)."""
     return _check(load().swiglu_mlp(_ptr(A), _ptr(W_fused), _ptr(Y), int(M), int(N), int(K),
                                     _stream(stream)), "swiglu_mlp")
+
+
+def swiglu_mlp_dual(A, W1, W2, Y, M, N, K, stream=None):
+    """Y = SiLU(A W1) (.) (A W2) from separate K x N weights (see the C header)."""
+    return _check(load().swiglu_mlp_dual(_ptr(A), _ptr(W1), _ptr(W2), _ptr(Y), int(M), int(N),
+                                         int(K), _stream(stream)), "swiglu_mlp_dual")
 
 
 def swiglu_mlp_forward(A, W_fused, W_down, Y, Out, M, N, K, beta=0.0, stream=None):

@@ -189,7 +189,7 @@ int pick_bn(int64_t M, int64_t N, int sms, const int *cands, int ncand)
 }
 
 // Resident CTA pairs of a pair kernel (kind 0 = GEMM store, 1 = SwiGLU,
-// 2 = split-K partials).
+// 2 = split-K partials, 3 = SwiGLU from separate weights).
 int max_pairs(DeviceState *d, int kind, int bn)
 {
     const int key = kind * 1024 + bn;
@@ -200,7 +200,8 @@ int max_pairs(DeviceState *d, int kind, int bn)
     }
     const int n = kind == 0   ? swg::max_active_pairs_store(bn, d->sms)
                   : kind == 1 ? swg::max_active_pairs_swiglu(bn, d->sms)
-                              : swg::max_active_pairs_splitk(bn, d->sms);
+                  : kind == 2 ? swg::max_active_pairs_splitk(bn, d->sms)
+                              : swg::max_active_pairs_dual(bn, d->sms);
     std::lock_guard<std::mutex> lk(g_mu);
     d->max_pairs[key] = n;
     return n;
@@ -600,6 +601,65 @@ int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M, int64_t N
     p.out_kind = swg::OUT_BF16;
     p.err = d->err;
     if (swg::launch_tc_swiglu(bn, pair, ta, tb, p, tc.units, s) != cudaSuccess)
+        return SWG_ERR_CUDA;
+    g_launches++;
+    return SWG_OK;
+}
+
+int swiglu_mlp_dual(const void *A, const void *W1, const void *W2, void *Y, int64_t M, int64_t N,
+                    int64_t K, void *stream)
+{
+    if (M < 0 || N < 0 || K < 0) return SWG_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return SWG_OK;
+    if (Y == nullptr || (K > 0 && (A == nullptr || W1 == nullptr || W2 == nullptr)))
+        return SWG_ERR_INVALID_ARG;
+    if (M > kMaxDim || 2 * N > kMaxDim || K > kMaxDim) return SWG_ERR_UNSUPPORTED;
+    if (!aligned16(Y) || N % 8 != 0) return SWG_ERR_MISALIGNED;
+    if (K > 0 && (!aligned16(A) || !aligned16(W1) || !aligned16(W2) || K % 8 != 0))
+        return SWG_ERR_MISALIGNED;
+
+    DeviceState *d = nullptr;
+    if (int rc = device_state(d)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) {   // Gate = Up = 0, so Y = 0.
+        scale_kernel<<<grid_for(M * N, d->sms), 256, 0, s>>>(Y, N, (int)M, (int)N, 0.0f,
+                                                              swg::OUT_BF16);
+        g_launches++;
+        return cudaGetLastError() == cudaSuccess ? SWG_OK : SWG_ERR_CUDA;
+    }
+
+    // Tiles are chosen in the 2N-wide Gate|Up column space, as for swiglu_mlp.
+    static const int cands[] = {256, 128};
+    const TileChoice tc = choose_tiles(d, 3, M, 2 * N, cands, 2);
+    const int bn = tc.bn;
+    const bool pair = tc.pair;
+    CUtensorMap ta, tw1, tw2;
+    if (!make_tmap(&ta, A, true, K, M, K, swg::BM) || !make_tmap(&tw1, W1, true, N, K, N, 64) ||
+        !make_tmap(&tw2, W2, true, N, K, N, 64))
+        return SWG_ERR_CUDA;
+
+    TileParams p{};
+    p.M = (int)M;
+    p.N = (int)N;              // output columns; a tile covers bn/2 of them
+    p.K = (int)K;
+    p.m_blocks = (int)cdiv(M, pair ? 2 * swg::BM : swg::BM);
+    p.n_blocks = (int)cdiv(N, bn / 2);
+    p.k_blocks = (int)cdiv(K, swg::BK);
+    p.tiles = p.m_blocks * p.n_blocks;
+    p.splits = 1;
+    p.kb_per_split = p.k_blocks;
+    p.units = p.tiles;
+    p.group_m = pair ? 8 : 16;
+    p.idesc = make_idesc(true, false, true, pair ? 2 * swg::BM : swg::BM, bn);
+    p.a_mn_major = 0;
+    p.b_mn_major = 1;
+    p.alpha = 1.0f;
+    p.beta = 0.0f;
+    p.D = Y;
+    p.ldd = N;
+    p.out_kind = swg::OUT_BF16;
+    p.err = d->err;
+    if (swg::launch_tc_swiglu_dual(bn, pair, ta, tw1, tw2, p, tc.units, s) != cudaSuccess)
         return SWG_ERR_CUDA;
     g_launches++;
     return SWG_OK;

@@ -25,6 +25,13 @@ cudaError_t launch_tc_splitk(int bn, bool pair, const CUtensorMap &ta, const CUt
 cudaError_t launch_tc_splitk_t(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
                                const TileParams &p, int units, cudaStream_t s);
 
+// SwiGLU from separate W1 (tw1) and W2 (tw2), each K x N; BN = 128 or 256
+// (single CTA) or 256 (pair).
+cudaError_t launch_tc_swiglu_dual(int bn, bool pair, const CUtensorMap &ta, const CUtensorMap &tw1,
+                                  const CUtensorMap &tw2, const TileParams &p, int units,
+                                  cudaStream_t s);
+int max_active_pairs_dual(int bn, int sms);
+
 // Resident CTA pairs for the pair variants (0 if unknown or not instantiated).
 int max_active_pairs_store(int bn, int sms);
 int max_active_pairs_swiglu(int bn, int sms);

@@ -11,8 +11,8 @@ namespace swg {
 // launches it.  `units` is the number of CTAs (1-CTA mode) or of CTA pairs
 // (PAIR: launched as clusters of two).
 template <int BN, int EPI, bool PAIR>
-cudaError_t launch_tc_impl(const CUtensorMap &ta, const CUtensorMap &tb, const TileParams &p,
-                           int units, cudaStream_t s)
+cudaError_t launch_tc_impl(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tb2,
+                           const TileParams &p, int units, cudaStream_t s)
 {
     using C = Cfg<BN, PAIR>;
     static std::atomic<unsigned long long> configured{0};
@@ -43,7 +43,15 @@ cudaError_t launch_tc_impl(const CUtensorMap &ta, const CUtensorMap &tb, const T
     } else {
         cfg.gridDim = dim3(units);
     }
-    return cudaLaunchKernelEx(&cfg, kernel, ta, tb, p);
+    return cudaLaunchKernelEx(&cfg, kernel, ta, tb, tb2, p);
+}
+
+// Kernels with one B operand: the second B map is unused (passed again).
+template <int BN, int EPI, bool PAIR>
+cudaError_t launch_tc_impl(const CUtensorMap &ta, const CUtensorMap &tb, const TileParams &p,
+                           int units, cudaStream_t s)
+{
+    return launch_tc_impl<BN, EPI, PAIR>(ta, tb, tb, p, units, s);
 }
 
 // How many CTA pairs of this kernel can be resident at once (clusters of two

@@ -50,7 +50,17 @@ namespace swg {
 // transposed product (its rows are the output's columns), so each thread owns
 // one output column and its registers hold output rows; the partial is written
 // transposed back to ws[split][row][column].
-enum EpiKind { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SPLITK = 2, EPI_SPLITK_T = 3 };
+// EPI_SWIGLU_DUAL: SwiGLU from separate W1 and W2.  The B tile's first BN/2
+// columns come from W1 (Gate) and the last BN/2 from W2 (Up) -- in a CTA pair
+// the even CTA loads its half of B from W1 and the odd CTA from W2 -- so the
+// accumulator row holds Gate in columns [0, BN/2) and Up in [BN/2, BN).
+enum EpiKind {
+    EPI_STORE = 0,
+    EPI_SWIGLU = 1,
+    EPI_SPLITK = 2,
+    EPI_SPLITK_T = 3,
+    EPI_SWIGLU_DUAL = 4
+};
 enum OutKind { OUT_BF16 = 0, OUT_F16 = 1, OUT_F32 = 2 };
 
 constexpr int BM = 128;
@@ -320,7 +330,7 @@ __device__ __forceinline__ void epi_chunk(const TileParams &p, const uint32_t (&
 template <int BN, int EPI, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const TileParams p)
+                   const __grid_constant__ CUtensorMap tmB2, const TileParams p)
 {
     using C = Cfg<BN, PAIR>;
     constexpr int S = C::STAGES;
@@ -368,6 +378,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (EPI == EPI_SWIGLU_DUAL) tma_prefetch_desc(&tmB2);
     }
     if (warp == 1) {
         if (PAIR) {
@@ -441,7 +452,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         load(a_dst, &tmA, m0, k0);                          // box {64 M, 64 K}
                         load(a_dst + 8192, &tmA, m0 + 64, k0);
                     }
-                    if (!p.b_mn_major) {
+                    if (EPI == EPI_SWIGLU_DUAL) {
+                        // W1 / W2 are K x N (N-major), boxes {64 N, 64 K}.  Pair:
+                        // this CTA's B_COLS columns come from W1 (rank 0) or
+                        // W2 (rank 1); single CTA: BN/2 from each.
+                        const int nd = nb * (BN / 2);
+#pragma unroll
+                        for (int c = 0; c < C::B_COLS / 64; ++c) {
+                            const bool up = PAIR ? (rank != 0) : (c >= BN / 128);
+                            const int cc = PAIR ? c : (c % (BN / 128));
+                            load(b_dst + c * 8192, up ? &tmB2 : &tmB, nd + cc * 64, k0);
+                        }
+                    } else if (!p.b_mn_major) {
                         load(b_dst, &tmB, k0, n0);                          // box {64 K, B_COLS N}
                     } else {
 #pragma unroll
@@ -537,6 +559,68 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             wait_bounded(smem_u32(mma_done), 0, abort_flag, p.err, false, DRAIN_LIMIT_NS);
         }
         __syncwarp();
+    } else if (EPI == EPI_SWIGLU_DUAL) {
+        // ------------------------------------------ epilogue (separate W1, W2)
+        // Output column j of the tile = SiLU(acc[j]) * acc[BN/2 + j]; warps
+        // 2..5 take output columns [0, BN/4), warps 6..9 [BN/4, BN/2).
+        constexpr int HALF = BN / 2;
+        constexpr int PER_WARP = HALF / 2;     // instantiated for BN = 128, 256 only
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const int h = (warp - EPI_WARP0) / 4;
+        int t = 0;
+        for (int u = first_unit; u < p.units; u += unit_step, ++t) {
+            int mb, nb, split, tile;
+            unit_coords(p, u, mb, nb, split, tile);
+            const int acc = t & 1;
+            const uint32_t acc_phase = (t >> 1) & 1;
+            bool ok = wait_bounded(smem_u32(&acc_full[acc]), acc_phase, abort_flag, p.err);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+            const int m = mb * C::TILE_M + (int)rank * BM + row;
+#pragma unroll 1
+            for (int c = 0; c < PER_WARP / 32; ++c) {
+                const int j0 = h * PER_WARP + c * 32;
+                uint32_t g[32], v[32];
+                tmem_ld_32cols(t_row + j0, g);
+                tmem_ld_32cols(t_row + HALF + j0, v);
+                tmem_ld_wait(g);
+                tmem_ld_wait(v);
+                const int n = nb * HALF + j0;                   // output column
+                if (m < p.M && n < p.N) {
+                    const int cnt = (p.N - n) < 32 ? (p.N - n) : 32;
+                    float y[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        y[j] = silu_f32(__uint_as_float(g[j])) * __uint_as_float(v[j]);
+                    __nv_bfloat16 *dst =
+                        reinterpret_cast<__nv_bfloat16 *>(p.D) + (long long)m * p.ldd + n;
+                    if (cnt == 32) {
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+                        for (int w = 0; w < 4; ++w)
+                            d4[w] = make_uint4(pack2(y[8 * w], y[8 * w + 1], OUT_BF16),
+                                               pack2(y[8 * w + 2], y[8 * w + 3], OUT_BF16),
+                                               pack2(y[8 * w + 4], y[8 * w + 5], OUT_BF16),
+                                               pack2(y[8 * w + 6], y[8 * w + 7], OUT_BF16));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < cnt) dst[j] = __float2bfloat16_rn(y[j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (PAIR)
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[acc]), 0));
+                else
+                    mbar_arrive(smem_u32(&acc_empty[acc]));
+            }
+        }
     } else if (EPI == EPI_SPLITK_T) {
         // ------------------------------------------------- epilogue (swapped)
         // TMEM lane = output column n (kernel row), TMEM column j = output row

@@ -97,3 +97,30 @@ def test_swiglu_large_magnitudes_finite():
     M, K, N = 128, 64, 256
     y, yhat = run(M, K, N, seed=91, w_std=8.0)
     check_half(y, yhat, "large gate magnitudes")
+
+
+@pytest.mark.parametrize("tile_mode", ["1cta", "2cta256", None])
+@pytest.mark.parametrize("M,K,N", [(128, 64, 128), (300, 136, 520), (1, 8, 8), (640, 896, 4864)])
+def test_swiglu_separate_weights(monkeypatch, tile_mode, M, K, N):
+    """swiglu_mlp_dual: Gate from W1 and Up from W2 in one accumulator, no
+    interleaved copy; against the oracle from the same separate weights."""
+    if tile_mode:
+        monkeypatch.setenv("SWG_TILE_MODE", tile_mode)
+    A, W1, W2 = synth.swiglu(M, K, N, seed=M + 2 * N + K, w_std=0.08)
+    Y = torch.full((M, N), 9.0, dtype=torch.bfloat16, device="cuda")
+    swg.swiglu_mlp_dual(A.cuda(), W1.cuda(), W2.cuda(), Y, M, N, K)
+    assert swg.get_device_error() == 0
+    rows = None if M <= 300 else [0, 127, 128, 255, 256, M - 1]
+    yhat = oracle.swiglu(A, W1, W2, M, N, K, rows=rows)
+    y = to_f64(Y) if rows is None else to_f64(Y)[rows]
+    check_half(y, yhat, f"dual {tile_mode} {M}x{K}x{N}")
+
+
+def test_swiglu_separate_weights_8b_sampled():
+    M, K, N = 2048, 4096, 14336
+    A, W1, W2 = synth.swiglu(M, K, N, seed=3)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    swg.swiglu_mlp_dual(A.cuda(), W1.cuda(), W2.cuda(), Y, M, N, K)
+    assert swg.get_device_error() == 0
+    rows = [0, 255, 256, M - 1]
+    check_half(to_f64(Y)[rows], oracle.swiglu(A, W1, W2, M, N, K, rows=rows), "dual 8B")
