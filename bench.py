@@ -420,6 +420,9 @@ def component_cases():
     cases += [("mlp_small_M2048", "mlp", 2048, 896, 4864), ("mlp_8b_M2048", "mlp", 2048, 4096, 14336)]
     cases += [("swiglu_dual_small_M2048", "dual", 2048, 896, 4864),
               ("swiglu_dual_8b_M2048", "dual", 2048, 4096, 14336)]
+    cases += [("fp8_gemm_8192", "fp8gemm", 8192, 8192, 8192),
+              ("fp8_swiglu_8b_M2048", "fp8swiglu", 2048, 4096, 14336),
+              ("fp8_swiglu_8b_M8192", "fp8swiglu", 8192, 4096, 14336)]
     return cases
 
 
@@ -450,6 +453,27 @@ def build_case(kind, M, K, N, dev, stream):
         def reset():
             Cd.copy_(C0)
         return fn, reset, 2.0 * M * N * K, (M * K + K * N + 2 * M * N) * 2
+    if kind == "fp8gemm":
+        g = synth.generator(1)
+        A = torch.randn(M, K, generator=g).to(torch.float8_e4m3fn).to(dev)
+        Bt = torch.randn(N, K, generator=g).to(torch.float8_e4m3fn).to(dev)
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+        def fn():
+            swg.gemm(0, 1, M, N, K, 1.0 / 64, A, K, Bt, K, 0.0, D, N, swg.E4M3_BF16OUT,
+                     stream=stream)
+        return fn, None, 2.0 * M * N * K, (M * K + K * N) + M * N * 2
+    if kind == "fp8swiglu":
+        A, W1, W2, sw = synth.swiglu_e4m3(M, K, N, seed=3)
+        Wt = torch.empty((2 * N, K), dtype=torch.float8_e4m3fn)
+        Wt[0::2] = W1.t()
+        Wt[1::2] = W2.t()
+        Ad, Wtd = A.to(dev), Wt.to(dev)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+        def fn():
+            swg.swiglu_mlp_fp8(Ad, Wtd, Y, M, N, K, sw, stream=stream)
+        return fn, None, 2.0 * M * 2 * N * K, (M * K + K * 2 * N) + M * N * 2
     if kind == "dual":
         A, W1, W2 = synth.swiglu(M, K, N, seed=3)
         Ad, W1d, W2d = A.to(dev), W1.to(dev), W2.to(dev)
@@ -528,7 +552,9 @@ def run_components(args, dev, stream):
         torch.cuda.synchronize(dev)
         ms = sorted(a.elapsed_time(b) for a, b in times)
         med = statistics.median(ms)
-        t_tensor, t_hbm = flops / (P * 1e12), byts / (bw * 1e9)
+        # 8-bit cases: the measured bf16 peak x the nominal fp8 / bf16 ratio (2)
+        peak = P * (2.0 if kind.startswith("fp8") else 1.0)
+        t_tensor, t_hbm = flops / (peak * 1e12), byts / (bw * 1e9)
         entry = {"median_us": round(med * 1e3, 2), "min_us": round(ms[0] * 1e3, 2),
                  "tflops": round(flops / med / 1e9, 1), "gbs": round(byts / med / 1e6, 1),
                  "roofline_frac": round(max(t_tensor, t_hbm) / (med / 1e3), 4),

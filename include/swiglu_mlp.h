@@ -51,12 +51,21 @@ typedef enum {
 
 typedef enum { SWG_OP_N = 0, SWG_OP_T = 1 } swg_op;
 
-/* Storage types.  A and B share one input type; C and D share one output type. */
+/* Storage types.  A and B share one input type; C and D share one output type.
+ * The e4m3 types (8-bit floating point: 1 sign, 4 exponent bits with bias 7,
+ * 3 fraction bits; largest finite value 448) quantise A and B ("GEMM o
+ * Coração Matemático", §12.4); per-tensor dequantisation scales are applied by
+ * folding them into alpha (alpha * scale_A * scale_B).  They require
+ * op(A) = A and op(B) = B^T, i.e. A stored M x K and B stored N x K (both
+ * K-contiguous), lda and ldb multiples of 16, and no split-K; other
+ * combinations return SWG_ERR_UNSUPPORTED. */
 typedef enum {
     SWG_F16_F32OUT = 0,   /* A, B binary16;  C, D binary32 */
     SWG_BF16 = 1,         /* A, B, C, D bfloat16            */
     SWG_F16 = 2,          /* A, B, C, D binary16            */
-    SWG_BF16_F32OUT = 3   /* A, B bfloat16;  C, D binary32  */
+    SWG_BF16_F32OUT = 3,  /* A, B bfloat16;  C, D binary32  */
+    SWG_E4M3_BF16OUT = 4, /* A, B e4m3;      C, D bfloat16  */
+    SWG_E4M3_F32OUT = 5   /* A, B e4m3;      C, D binary32  */
 } swg_dtype;
 
 /*
@@ -129,6 +138,24 @@ SWG_API int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,
  */
 SWG_API int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M,
                int64_t N, int64_t K, void *stream);
+
+/*
+ * swiglu_mlp_fp8 — Y = SiLU(s * A W1) (.) (s * A W2) with e4m3 A and weights,
+ * s = scale_A * scale_W (per-tensor dequantisation scales), FP32
+ * accumulation, bfloat16 Y.  Same operation and sources as swiglu_mlp; the
+ * 8-bit form follows "GEMM o Coração Matemático", §12.4 (quantised operands).
+ *
+ *   A          e4m3, M x K, row stride K.
+ *   W_fused_t  e4m3, 2N x K, row stride K: the TRANSPOSED interleaved weight,
+ *              row 2n = W1 column n (Gate), row 2n+1 = W2 column n (Up)
+ *              (8-bit operands are read K-contiguous).
+ *   Y          bfloat16, M x N, row stride N (written).
+ *   scale      s above; applied to Gate and Up before the SiLU.
+ *   Alignment  pointers 16-byte aligned, K % 16 == 0, N % 8 == 0.
+ */
+SWG_API int swiglu_mlp_fp8(const void *A, const void *W_fused_t, void *Y,
+                           int64_t M, int64_t N, int64_t K, float scale,
+                           void *stream);
 
 /*
  * swiglu_mlp_dual — the same Y = SiLU(A * W1) (.) (A * W2), computed directly

@@ -19,7 +19,11 @@ computes, with the passage it follows:
   from W2 (Up) (same page, Metodologia, Kernel-2).
 * :func:`mlp` — the full gated MLP, (SiLU(A W1) (.) (A W2)) W_down + beta * Out
   ("GEMM o Coração Matemático", §13.3, with the gated activation above).
-* :func:`silu`, :func:`f16_to_f64`, :func:`bf16_to_f64` — the scalar pieces.
+* :func:`swiglu_typed`, :func:`interleave_t8` — the same SwiGLU on 8-bit
+  (e4m3) operands with a per-tensor scale, and the transposed interleave the
+  8-bit kernel reads ("GEMM o Coração Matemático", §12.4).
+* :func:`silu`, :func:`f16_to_f64`, :func:`bf16_to_f64`, :func:`e4m3_to_f64`
+  — the scalar pieces.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` against values and
 properties fixed outside the oracle (the page's worked example, exact integer
@@ -41,7 +45,7 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-TYPES = {"f16": 0, "bf16": 1, "f32": 2}
+TYPES = {"f16": 0, "bf16": 1, "f32": 2, "e4m3": 3}
 
 
 def build(force: bool = False) -> str:
@@ -73,6 +77,13 @@ def _load():
             lib.orc_swiglu.restype = i32
             lib.orc_mlp.argtypes = [vp, vp, vp, vp, vp, f64, i64, i64, i64, vp, i64, vp, i32]
             lib.orc_mlp.restype = i32
+            lib.orc_swiglu_typed.argtypes = [vp, vp, vp, i32, f64, i64, i64, i64, vp, i64, vp,
+                                             i64, vp, i32]
+            lib.orc_swiglu_typed.restype = i32
+            lib.orc_interleave_t8.argtypes = [vp, vp, vp, i64, i64]
+            lib.orc_interleave_t8.restype = None
+            lib.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+            lib.orc_e4m3_to_f64.restype = f64
             lib.orc_interleave.argtypes = [vp, vp, vp, i64, i64]
             lib.orc_interleave.restype = None
             lib.orc_silu.argtypes = [f64]
@@ -97,8 +108,14 @@ def _as_buffer(x, kind: str) -> np.ndarray:
         t = x.detach().contiguous()
         if t.dtype in (torch.float16, torch.bfloat16):
             t = t.view(torch.int16)
+        elif t.dtype == getattr(torch, "float8_e4m3fn", None):
+            t = t.view(torch.uint8)
         x = t.numpy()
     a = np.ascontiguousarray(x)
+    if kind == "e4m3":
+        if a.dtype.itemsize != 1:
+            raise TypeError(f"e4m3 operand must hold 8-bit patterns, got {a.dtype}")
+        return a.view(np.uint8)
     if kind in ("f16", "bf16"):
         if a.dtype.itemsize != 2:
             raise TypeError(f"{kind} operand must hold 16-bit patterns, got {a.dtype}")
@@ -183,6 +200,37 @@ def mlp(A, W1, W2, Wd, M: int, N: int, K: int, beta: float = 0.0, Out_old=None, 
     if rc != 0:
         raise ValueError("oracle mlp rejected its arguments")
     return out
+
+
+def swiglu_typed(A, W1, W2, M: int, N: int, K: int, in_type: str = "e4m3",
+                 scale: float = 1.0, rows=None, cols=None, threads: int = 0) -> np.ndarray:
+    """Y = SiLU(scale * A W1) (.) (scale * A W2) in double for operands of
+    storage type in_type (e.g. e4m3) with a per-tensor dequantisation scale."""
+    lib = _load()
+    a, w1, w2 = (_as_buffer(x, in_type) for x in (A, W1, W2))
+    r, n_rows = _rows(rows, M)
+    cs, n_cols = _rows(cols, N)
+    out = np.empty((n_rows, n_cols), dtype=np.float64)
+    rc = lib.orc_swiglu_typed(_ptr(a), _ptr(w1), _ptr(w2), TYPES[in_type], float(scale), M, N,
+                              K, _ptr(r), n_rows, _ptr(cs), n_cols, out.ctypes.data,
+                              int(threads))
+    if rc != 0:
+        raise ValueError("oracle swiglu_typed rejected its arguments")
+    return out
+
+
+def interleave_t8(W1, W2, K: int, N: int) -> np.ndarray:
+    """2N x K uint8 patterns: row 2n = W1 column n, row 2n+1 = W2 column n."""
+    lib = _load()
+    w1 = _as_buffer(W1, "e4m3")
+    w2 = _as_buffer(W2, "e4m3")
+    out = np.empty((2 * N, K), dtype=np.uint8)
+    lib.orc_interleave_t8(_ptr(w1), _ptr(w2), out.ctypes.data, K, N)
+    return out
+
+
+def e4m3_to_f64(bits: int) -> float:
+    return _load().orc_e4m3_to_f64(int(bits) & 0xFF)
 
 
 def interleave(W1, W2, K: int, N: int) -> np.ndarray:

@@ -43,7 +43,7 @@
 #include <string.h>
 #include <unistd.h>
 
-enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_F32 = 2 };
+enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_F32 = 2, ORC_E4M3 = 3 };
 
 /* ---- exact widening of the stored formats ---------------------------- */
 
@@ -80,11 +80,30 @@ double orc_bf16_to_f64(uint16_t b)
     return sign ? -v : v;
 }
 
+/* e4m3: 1 sign, 4 exponent bits (bias 7), 3 fraction bits; no infinities,
+ * exponent and fraction all ones is NaN, so the largest value is
+ * 1.75 * 2^8 = 448 ("GEMM o Coração Matemático", §12.4 on 8-bit formats). */
+double orc_e4m3_to_f64(uint8_t b)
+{
+    int sign = (b >> 7) & 1;
+    int e = (b >> 3) & 0xf;
+    int f = b & 0x7;
+    double v;
+    if (e == 0)                    /* zero or subnormal: f * 2^-9 */
+        v = ldexp((double)f, -9);
+    else if (e == 15 && f == 7)
+        v = NAN;
+    else                           /* (8 + f) * 2^(e - 7 - 3) */
+        v = ldexp((double)(8 + f), e - 10);
+    return sign ? -v : v;
+}
+
 static double load_elem(const void *base, int64_t idx, int type)
 {
     switch (type) {
     case ORC_F16:  return orc_f16_to_f64(((const uint16_t *)base)[idx]);
     case ORC_BF16: return orc_bf16_to_f64(((const uint16_t *)base)[idx]);
+    case ORC_E4M3: return orc_e4m3_to_f64(((const uint8_t *)base)[idx]);
     default:       return (double)((const float *)base)[idx];
     }
 }
@@ -303,4 +322,49 @@ int orc_mlp(const uint16_t *A, const uint16_t *W1, const uint16_t *W2,
     }
     free(Y);
     return rc;
+}
+
+/* ---- quantised SwiGLU -------------------------------------------------- */
+
+/* Y = SiLU(scale * G) * (scale * U), G = A W1, U = A W2, for A (M x K, row
+ * stride K) and W1, W2 (K x N, row stride N) of storage type `type`; scale is
+ * the product of the per-tensor dequantisation scales of A and W.  The same
+ * SwiGLU as orc_swiglu, on quantised operands ("GEMM o Coração Matemático",
+ * §12.4). */
+int orc_swiglu_typed(const void *A, const void *W1, const void *W2, int type,
+                     double scale, int64_t M, int64_t N, int64_t K,
+                     const int64_t *rows, int64_t n_rows, const int64_t *cols,
+                     int64_t n_cols, double *Y, int n_threads)
+{
+    if (!rows && n_rows != M) return -1;
+    if (!cols && n_cols != N) return -1;
+    if (n_rows == 0 || n_cols == 0) return 0;
+    double *G = (double *)malloc(sizeof(double) * (size_t)(n_rows * n_cols));
+    double *U = (double *)malloc(sizeof(double) * (size_t)(n_rows * n_cols));
+    int rc = (G && U) ? 0 : -1;
+    if (rc == 0)
+        rc = orc_gemm(0, 0, M, N, K, 1.0, A, K, type, W1, N, type, 0.0, NULL, 0,
+                      type, rows, n_rows, cols, n_cols, G, n_threads);
+    if (rc == 0)
+        rc = orc_gemm(0, 0, M, N, K, 1.0, A, K, type, W2, N, type, 0.0, NULL, 0,
+                      type, rows, n_rows, cols, n_cols, U, n_threads);
+    if (rc == 0)
+        for (int64_t e = 0; e < n_rows * n_cols; ++e)
+            Y[e] = orc_silu(scale * G[e]) * (scale * U[e]);
+    free(G);
+    free(U);
+    return rc;
+}
+
+/* Transposed interleave for 8-bit weights: Wt (2N x K, row stride K) with
+ * row 2n = W1 column n (Gate) and row 2n+1 = W2 column n (Up), from W1, W2
+ * (K x N, row stride N).  Same column order as orc_interleave. */
+void orc_interleave_t8(const uint8_t *W1, const uint8_t *W2, uint8_t *Wt,
+                       int64_t K, int64_t N)
+{
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k) {
+            Wt[(2 * n) * K + k] = W1[k * N + n];
+            Wt[(2 * n + 1) * K + k] = W2[k * N + n];
+        }
 }

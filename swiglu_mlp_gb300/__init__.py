@@ -17,14 +17,15 @@ import os
 import threading
 
 __all__ = [
-    "SwgError", "OP_N", "OP_T", "F16_F32OUT", "BF16", "F16", "BF16_F32OUT",
+    "SwgError", "OP_N", "OP_T", "F16_F32OUT", "BF16", "F16", "BF16_F32OUT", "E4M3_BF16OUT",
+    "E4M3_F32OUT", "swiglu_mlp_fp8",
     "gemm", "gemm_ex", "gemm_splitk_noalloc", "swiglu_mlp", "swiglu_mlp_dual", "swiglu_mlp_forward", "swiglu_interleave", "status_string",
     "get_device_error", "launch_count", "shutdown", "gemm_into",
     "swiglu_mlp_into", "interleave_weights", "library_path", "load",
 ]
 
 OP_N, OP_T = 0, 1
-F16_F32OUT, BF16, F16, BF16_F32OUT = 0, 1, 2, 3
+F16_F32OUT, BF16, F16, BF16_F32OUT, E4M3_BF16OUT, E4M3_F32OUT = 0, 1, 2, 3, 4, 5
 STATUS = {0: "SWG_OK", 1: "SWG_ERR_INVALID_ARG", 2: "SWG_ERR_MISALIGNED",
           3: "SWG_ERR_UNSUPPORTED", 4: "SWG_ERR_CUDA", 5: "SWG_ERR_NO_MEMORY",
           6: "SWG_ERR_DEVICE_TIMEOUT"}
@@ -67,6 +68,8 @@ def load():
         lib.gemm_splitk_noalloc.restype = i32
         lib.swiglu_mlp.argtypes = [vp, vp, vp, i64, i64, i64, vp]
         lib.swiglu_mlp.restype = i32
+        lib.swiglu_mlp_fp8.argtypes = [vp, vp, vp, i64, i64, i64, f32, vp]
+        lib.swiglu_mlp_fp8.restype = i32
         lib.swiglu_mlp_dual.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
         lib.swiglu_mlp_dual.restype = i32
         lib.swiglu_mlp_forward.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, f32, vp]
@@ -140,6 +143,13 @@ def swiglu_mlp(A, W_fused, Y, M, N, K, stream=None):
     """Y = SiLU(A W1) (.) (A W2) over the interleaved W_fused (see the C header)."""
     return _check(load().swiglu_mlp(_ptr(A), _ptr(W_fused), _ptr(Y), int(M), int(N), int(K),
                                     _stream(stream)), "swiglu_mlp")
+
+
+def swiglu_mlp_fp8(A, W_fused_t, Y, M, N, K, scale, stream=None):
+    """Y = SiLU(s A W1) (.) (s A W2) from e4m3 A [M, K] and the transposed
+    interleaved e4m3 weight [2N, K] (see the C header)."""
+    return _check(load().swiglu_mlp_fp8(_ptr(A), _ptr(W_fused_t), _ptr(Y), int(M), int(N),
+                                        int(K), float(scale), _stream(stream)), "swiglu_mlp_fp8")
 
 
 def swiglu_mlp_dual(A, W1, W2, Y, M, N, K, stream=None):

@@ -154,9 +154,27 @@ bool make_tmap(CUtensorMap *m, const void *ptr, bool bf16, int64_t inner, int64_
     return r == CUDA_SUCCESS;
 }
 
+// Row-major matrix of 8-bit elements (e4m3), boxes of 128 x box_outer: one
+// 128-byte swizzle row per box row, as for the 16-bit maps.
+bool make_tmap_u8(CUtensorMap *m, const void *ptr, int64_t inner, int64_t outer, int64_t ld,
+                  int box_outer)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    cuuint64_t strides[1] = {(cuuint64_t)ld};
+    cuuint32_t box[2] = {128u, (cuuint32_t)box_outer};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // tcgen05 instruction descriptor, kind::f16: D=F32 (bits 4-5 = 1), A/B type
 // (bits 7-9, 10-12: 0 = f16, 1 = bf16), A/B major (bits 15, 16: 1 = MN-major),
-// N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+// N >> 3 (bits 17-22), M >> 4 (bits 24-28).  With bf16 = false the same
+// bits describe kind::f8f6f4 with e4m3 A and B (format code 0).
 uint32_t make_idesc(bool bf16, bool a_mn, bool b_mn, int m, int n)
 {
     const uint32_t t = bf16 ? 1u : 0u;
@@ -189,7 +207,8 @@ int pick_bn(int64_t M, int64_t N, int sms, const int *cands, int ncand)
 }
 
 // Resident CTA pairs of a pair kernel (kind 0 = GEMM store, 1 = SwiGLU,
-// 2 = split-K partials, 3 = SwiGLU from separate weights).
+// 2 = split-K partials, 3 = SwiGLU from separate weights, 4 = FP8 GEMM,
+// 5 = FP8 SwiGLU).
 int max_pairs(DeviceState *d, int kind, int bn)
 {
     const int key = kind * 1024 + bn;
@@ -201,7 +220,9 @@ int max_pairs(DeviceState *d, int kind, int bn)
     const int n = kind == 0   ? swg::max_active_pairs_store(bn, d->sms)
                   : kind == 1 ? swg::max_active_pairs_swiglu(bn, d->sms)
                   : kind == 2 ? swg::max_active_pairs_splitk(bn, d->sms)
-                              : swg::max_active_pairs_dual(bn, d->sms);
+                  : kind == 3 ? swg::max_active_pairs_dual(bn, d->sms)
+                  : kind == 4 ? swg::max_active_pairs_fp8(0, bn, d->sms)
+                              : swg::max_active_pairs_fp8(1, bn, d->sms);
     std::lock_guard<std::mutex> lk(g_mu);
     d->max_pairs[key] = n;
     return n;
@@ -314,6 +335,7 @@ int splitk_swapped(DeviceState *d, const TypeInfo &ti, int transA, int transB, i
     p.m_blocks = (int)cdiv(N, swg::BM);
     p.n_blocks = (int)cdiv(M, bn);
     p.k_blocks = (int)kb;
+    p.bk = swg::BK;
     p.tiles = p.m_blocks * p.n_blocks;
     p.splits = splits;
     p.kb_per_split = kbps;
@@ -419,10 +441,76 @@ const char *swg_status_string(int status)
 
 uint64_t swg_launch_count(void) { return g_launches.load(); }
 
+// GEMM with e4m3 A and B (kind::f8f6f4): A stored M x K and B stored N x K,
+// both K-major; per-tensor dequantisation scales are folded into alpha.
+static int gemm_fp8(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
+                    const void *A, int64_t lda, const void *B, int64_t ldb, float beta, void *C,
+                    int64_t ldc, int out_kind, int out_bytes, int split_k, void *stream)
+{
+    if ((transA != SWG_OP_N && transA != SWG_OP_T) || (transB != SWG_OP_N && transB != SWG_OP_T))
+        return SWG_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0 || split_k < 0) return SWG_ERR_INVALID_ARG;
+    if (transA != SWG_OP_N || transB != SWG_OP_T || split_k > 1) return SWG_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return SWG_OK;
+    if (C == nullptr || ldc < N) return SWG_ERR_INVALID_ARG;
+    if (K > 0 && (A == nullptr || B == nullptr || lda < K || ldb < K)) return SWG_ERR_INVALID_ARG;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim || ldc > kMaxDim || lda > kMaxDim ||
+        ldb > kMaxDim)
+        return SWG_ERR_UNSUPPORTED;
+    if (!aligned16(C) || (ldc * out_bytes) % 16 != 0) return SWG_ERR_MISALIGNED;
+    if (K > 0 && (!aligned16(A) || !aligned16(B) || lda % 16 != 0 || ldb % 16 != 0))
+        return SWG_ERR_MISALIGNED;
+
+    DeviceState *d = nullptr;
+    if (int rc = device_state(d)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        scale_kernel<<<grid_for(M * N, d->sms), 256, 0, s>>>(C, ldc, (int)M, (int)N, beta, out_kind);
+        g_launches++;
+        return cudaGetLastError() == cudaSuccess ? SWG_OK : SWG_ERR_CUDA;
+    }
+    static const int cands[] = {256, 128};
+    const TileChoice tc = choose_tiles(d, 4, M, N, cands, 2);
+    const int bn = tc.bn;
+    const bool pair = tc.pair;
+    CUtensorMap ta, tb;
+    if (!make_tmap_u8(&ta, A, K, M, lda, swg::BM) ||
+        !make_tmap_u8(&tb, B, K, N, ldb, pair ? bn / 2 : bn))
+        return SWG_ERR_CUDA;
+    TileParams p{};
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.m_blocks = (int)cdiv(M, pair ? 2 * swg::BM : swg::BM);
+    p.n_blocks = (int)cdiv(N, bn);
+    p.k_blocks = (int)cdiv(K, 128);
+    p.bk = 128;
+    p.tiles = p.m_blocks * p.n_blocks;
+    p.splits = 1;
+    p.kb_per_split = p.k_blocks;
+    p.units = p.tiles;
+    p.group_m = pair ? 8 : 16;
+    p.idesc = make_idesc(false, false, false, pair ? 2 * swg::BM : swg::BM, bn);
+    p.alpha = alpha;
+    p.beta = beta;
+    p.D = C;
+    p.ldd = ldc;
+    p.out_kind = out_kind;
+    p.err = d->err;
+    if (swg::launch_tc_store_fp8(bn, pair, ta, tb, p, tc.units, s) != cudaSuccess)
+        return SWG_ERR_CUDA;
+    g_launches++;
+    return SWG_OK;
+}
+
 int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha, const void *A,
             int64_t lda, const void *B, int64_t ldb, float beta, void *C, int64_t ldc, int dtype,
             int split_k, void *stream)
 {
+    if (dtype == SWG_E4M3_BF16OUT || dtype == SWG_E4M3_F32OUT)
+        return gemm_fp8(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                        dtype == SWG_E4M3_BF16OUT ? swg::OUT_BF16 : swg::OUT_F32,
+                        dtype == SWG_E4M3_BF16OUT ? 2 : 4, split_k, stream);
     TypeInfo ti;
     if (!type_info(dtype, ti)) return SWG_ERR_UNSUPPORTED;
     if ((transA != SWG_OP_N && transA != SWG_OP_T) || (transB != SWG_OP_N && transB != SWG_OP_T))
@@ -500,6 +588,7 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
     p.m_blocks = (int)(pair ? cdiv(M, 2 * swg::BM) : mblk);
     p.n_blocks = (int)cdiv(N, bn);
     p.k_blocks = (int)kb;
+    p.bk = swg::BK;
     p.tiles = p.m_blocks * p.n_blocks;
     p.splits = splits;
     p.kb_per_split = kbps;
@@ -586,6 +675,7 @@ int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M, int64_t N
     p.m_blocks = (int)cdiv(M, pair ? 2 * swg::BM : swg::BM);
     p.n_blocks = (int)cdiv(N2, bn);
     p.k_blocks = (int)cdiv(K, swg::BK);
+    p.bk = swg::BK;
     p.tiles = p.m_blocks * p.n_blocks;
     p.splits = 1;
     p.kb_per_split = p.k_blocks;
@@ -601,6 +691,62 @@ int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M, int64_t N
     p.out_kind = swg::OUT_BF16;
     p.err = d->err;
     if (swg::launch_tc_swiglu(bn, pair, ta, tb, p, tc.units, s) != cudaSuccess)
+        return SWG_ERR_CUDA;
+    g_launches++;
+    return SWG_OK;
+}
+
+int swiglu_mlp_fp8(const void *A, const void *W_fused_t, void *Y, int64_t M, int64_t N,
+                   int64_t K, float scale, void *stream)
+{
+    if (M < 0 || N < 0 || K < 0) return SWG_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return SWG_OK;
+    if (Y == nullptr || (K > 0 && (A == nullptr || W_fused_t == nullptr)))
+        return SWG_ERR_INVALID_ARG;
+    if (M > kMaxDim || 2 * N > kMaxDim || K > kMaxDim) return SWG_ERR_UNSUPPORTED;
+    if (!aligned16(Y) || N % 8 != 0) return SWG_ERR_MISALIGNED;
+    if (K > 0 && (!aligned16(A) || !aligned16(W_fused_t) || K % 16 != 0))
+        return SWG_ERR_MISALIGNED;
+
+    DeviceState *d = nullptr;
+    if (int rc = device_state(d)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        scale_kernel<<<grid_for(M * N, d->sms), 256, 0, s>>>(Y, N, (int)M, (int)N, 0.0f,
+                                                              swg::OUT_BF16);
+        g_launches++;
+        return cudaGetLastError() == cudaSuccess ? SWG_OK : SWG_ERR_CUDA;
+    }
+    const int64_t N2 = 2 * N;
+    static const int cands[] = {256, 128, 64};
+    const TileChoice tc = choose_tiles(d, 5, M, N2, cands, 3);
+    const int bn = tc.bn;
+    const bool pair = tc.pair;
+    CUtensorMap ta, tb;
+    if (!make_tmap_u8(&ta, A, K, M, K, swg::BM) ||
+        !make_tmap_u8(&tb, W_fused_t, K, N2, K, pair ? bn / 2 : bn))
+        return SWG_ERR_CUDA;
+    TileParams p{};
+    p.M = (int)M;
+    p.N = (int)N2;
+    p.K = (int)K;
+    p.m_blocks = (int)cdiv(M, pair ? 2 * swg::BM : swg::BM);
+    p.n_blocks = (int)cdiv(N2, bn);
+    p.k_blocks = (int)cdiv(K, 128);
+    p.bk = 128;
+    p.tiles = p.m_blocks * p.n_blocks;
+    p.splits = 1;
+    p.kb_per_split = p.k_blocks;
+    p.units = p.tiles;
+    p.group_m = pair ? 8 : 16;
+    p.idesc = make_idesc(false, false, false, pair ? 2 * swg::BM : swg::BM, bn);
+    p.alpha = scale;
+    p.beta = 0.0f;
+    p.D = Y;
+    p.ldd = N;
+    p.out_kind = swg::OUT_BF16;
+    p.err = d->err;
+    if (swg::launch_tc_swiglu_fp8(bn, pair, ta, tb, p, tc.units, s) != cudaSuccess)
         return SWG_ERR_CUDA;
     g_launches++;
     return SWG_OK;
@@ -645,6 +791,7 @@ int swiglu_mlp_dual(const void *A, const void *W1, const void *W2, void *Y, int6
     p.m_blocks = (int)cdiv(M, pair ? 2 * swg::BM : swg::BM);
     p.n_blocks = (int)cdiv(N, bn / 2);
     p.k_blocks = (int)cdiv(K, swg::BK);
+    p.bk = swg::BK;
     p.tiles = p.m_blocks * p.n_blocks;
     p.splits = 1;
     p.kb_per_split = p.k_blocks;
@@ -856,6 +1003,7 @@ int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N, int64_t K,
     p.m_blocks = (int)cdiv(M, swg::BM);
     p.n_blocks = (int)cdiv(N, bn);
     p.k_blocks = (int)kb;
+    p.bk = swg::BK;
     p.tiles = p.m_blocks * p.n_blocks;
     p.splits = splits;
     p.kb_per_split = kbps;

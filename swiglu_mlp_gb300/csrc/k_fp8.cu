@@ -1,0 +1,49 @@
+// k_fp8.cu — instantiations of the tcgen05 GEMM with 8-bit (e4m3) operands
+// and kind::f8f6f4 MMAs: the plain GEMM epilogue and the interleaved SwiGLU
+// epilogue.  Per-tensor dequantisation scales arrive folded into alpha.
+// Quantised operands: "GEMM o Coração Matemático", §12.4; the SwiGLU page
+// ("Sobreposição de Ativação ...", Definição do Problema) notes that FP8 /
+// INT4 raise the relative cost of the memory-bound activation step.
+#include "launch_impl.cuh"
+
+namespace swg {
+cudaError_t launch_tc_store_fp8(int bn, bool pair, const CUtensorMap &ta, const CUtensorMap &tb,
+                                const TileParams &p, int units, cudaStream_t s)
+{
+    if (pair) {
+        switch (bn) {
+        case 256: return launch_tc_impl<256, EPI_STORE, true, true>(ta, tb, p, units, s);
+        default: return cudaErrorInvalidValue;
+        }
+    }
+    switch (bn) {
+    case 128: return launch_tc_impl<128, EPI_STORE, false, true>(ta, tb, p, units, s);
+    case 256: return launch_tc_impl<256, EPI_STORE, false, true>(ta, tb, p, units, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_tc_swiglu_fp8(int bn, bool pair, const CUtensorMap &ta, const CUtensorMap &tb,
+                                 const TileParams &p, int units, cudaStream_t s)
+{
+    if (pair) {
+        switch (bn) {
+        case 256: return launch_tc_impl<256, EPI_SWIGLU, true, true>(ta, tb, p, units, s);
+        default: return cudaErrorInvalidValue;
+        }
+    }
+    switch (bn) {
+    case 64: return launch_tc_impl<64, EPI_SWIGLU, false, true>(ta, tb, p, units, s);
+    case 128: return launch_tc_impl<128, EPI_SWIGLU, false, true>(ta, tb, p, units, s);
+    case 256: return launch_tc_impl<256, EPI_SWIGLU, false, true>(ta, tb, p, units, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+int max_active_pairs_fp8(int kind, int bn, int sms)
+{
+    if (bn != 256) return 0;
+    return kind == 0 ? max_active_pairs_impl<256, EPI_STORE, true>(sms)
+                     : max_active_pairs_impl<256, EPI_SWIGLU, true>(sms);
+}
+}  // namespace swg

@@ -32,6 +32,13 @@ cudaError_t launch_tc_swiglu_dual(int bn, bool pair, const CUtensorMap &ta, cons
                                   cudaStream_t s);
 int max_active_pairs_dual(int bn, int sms);
 
+// 8-bit (e4m3) operands, kind::f8f6f4 MMAs, K-major A and B only.
+cudaError_t launch_tc_store_fp8(int bn, bool pair, const CUtensorMap &ta, const CUtensorMap &tb,
+                                const TileParams &p, int units, cudaStream_t s);
+cudaError_t launch_tc_swiglu_fp8(int bn, bool pair, const CUtensorMap &ta, const CUtensorMap &tb,
+                                 const TileParams &p, int units, cudaStream_t s);
+int max_active_pairs_fp8(int kind, int bn, int sms);   // kind 0 = GEMM, 1 = SwiGLU
+
 // Resident CTA pairs for the pair variants (0 if unknown or not instantiated).
 int max_active_pairs_store(int bn, int sms);
 int max_active_pairs_swiglu(int bn, int sms);

@@ -10,7 +10,7 @@ namespace swg {
 // Opts the kernel into its dynamic shared memory once per device and
 // launches it.  `units` is the number of CTAs (1-CTA mode) or of CTA pairs
 // (PAIR: launched as clusters of two).
-template <int BN, int EPI, bool PAIR>
+template <int BN, int EPI, bool PAIR, bool FP8 = false>
 cudaError_t launch_tc_impl(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tb2,
                            const TileParams &p, int units, cudaStream_t s)
 {
@@ -20,7 +20,7 @@ cudaError_t launch_tc_impl(const CUtensorMap &ta, const CUtensorMap &tb, const C
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
-    auto kernel = tc_gemm_kernel<BN, EPI, PAIR>;
+    auto kernel = tc_gemm_kernel<BN, EPI, PAIR, FP8>;
     if (!(configured.load() & bit)) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::SMEM_BYTES);
@@ -47,20 +47,20 @@ cudaError_t launch_tc_impl(const CUtensorMap &ta, const CUtensorMap &tb, const C
 }
 
 // Kernels with one B operand: the second B map is unused (passed again).
-template <int BN, int EPI, bool PAIR>
+template <int BN, int EPI, bool PAIR, bool FP8 = false>
 cudaError_t launch_tc_impl(const CUtensorMap &ta, const CUtensorMap &tb, const TileParams &p,
                            int units, cudaStream_t s)
 {
-    return launch_tc_impl<BN, EPI, PAIR>(ta, tb, tb, p, units, s);
+    return launch_tc_impl<BN, EPI, PAIR, FP8>(ta, tb, tb, p, units, s);
 }
 
 // How many CTA pairs of this kernel can be resident at once (clusters of two
 // need two free SMs in one GPC); 0 on error.
-template <int BN, int EPI>
+template <int BN, int EPI, bool FP8 = false>
 int max_active_pairs_impl(int sms)
 {
     using C = Cfg<BN, true>;
-    auto kernel = tc_gemm_kernel<BN, EPI, true>;
+    auto kernel = tc_gemm_kernel<BN, EPI, true, FP8>;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES) != cudaSuccess)
         return 0;

@@ -84,6 +84,7 @@ struct TileParams {
     int units;                   // tiles * splits
     int group_m;                 // raster: m-blocks per group
     uint32_t idesc;              // tcgen05 instruction descriptor
+    int bk;                      // elements per 128-byte K block: 64 (16-bit) or 128 (fp8)
     int a_mn_major;              // op(A) stored M-contiguous (transA = T)
     int b_mn_major;              // op(B) stored N-contiguous (transB = N)
     float alpha, beta;
@@ -293,10 +294,13 @@ __device__ __forceinline__ void epi_chunk(const TileParams &p, const uint32_t (&
         // Column pair (2j, 2j+1) of the 2N-space is (Gate_j, Up_j); output
         // column n/2 + j.
         const long long off = (long long)m * p.ldd + n / 2;
+        // alpha = product of per-tensor dequantisation scales (1 for bf16),
+        // applied to Gate and Up before the SiLU.
         float y[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-            y[j] = silu_f32(__uint_as_float(r[2 * j])) * __uint_as_float(r[2 * j + 1]);
+            y[j] = silu_f32(p.alpha * __uint_as_float(r[2 * j])) *
+                   (p.alpha * __uint_as_float(r[2 * j + 1]));
         __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.D) + off;
         if (cnt == 32) {
             uint32_t w[8];
@@ -327,7 +331,10 @@ __device__ __forceinline__ void epi_chunk(const TileParams &p, const uint32_t (&
     }
 }
 
-template <int BN, int EPI, bool PAIR>
+// FP8: operands are 8-bit (e4m3/e5m2) and the MMA is kind::f8f6f4.  In bytes
+// nothing else changes: a 128-byte swizzled stage row holds 128 elements and
+// each MMA (K = 32) consumes 32 bytes of it, as a kind::f16 MMA (K = 16) does.
+template <int BN, int EPI, bool PAIR, bool FP8 = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmB2, const TileParams p)
@@ -439,7 +446,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     const uint32_t a_dst = smem_u32(sA + stage * C::A_BYTES);
                     const uint32_t b_dst = smem_u32(sB + stage * C::B_BYTES);
-                    const int k0 = kb * BK;
+                    const int k0 = kb * p.bk;
                     auto load = [&](uint32_t dst, const CUtensorMap *tm, int x, int y) {
                         if (PAIR)
                             tma_load_2d_pair(dst, tm, fb, x, y);
@@ -531,8 +538,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint64_t ad = smem_desc(a_base + kk * a_kstep, a_lbo, 1024);
                         const uint64_t bd = smem_desc(b_base + kk * b_kstep, b_lbo, 1024);
                         const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
-                        if (PAIR)
+                        if (PAIR && FP8)
+                            tc_mma_f8_pair(d_tmem, ad, bd, p.idesc, accum);
+                        else if (PAIR)
                             tc_mma_f16_pair(d_tmem, ad, bd, p.idesc, accum);
+                        else if (FP8)
+                            tc_mma_f8(d_tmem, ad, bd, p.idesc, accum);
                         else
                             tc_mma_f16(d_tmem, ad, bd, p.idesc, accum);
                     }

@@ -87,3 +87,25 @@ def skinny(M: int, N: int = 4096, K: int = 16384, seed: int = 4):
     B = normal((K, N), g)
     C = normal((M, N), g)
     return A, B, C
+
+
+def to_e4m3(x: torch.Tensor):
+    """Per-tensor scaled e4m3 copy of x: returns (q, scale) with q = x / scale
+    rounded to e4m3 (round to nearest even) and scale = max|x| / 448, so the
+    largest magnitude maps to e4m3's largest finite value."""
+    amax = float(x.abs().max())
+    scale = amax / 448.0 if amax > 0 else 1.0
+    return (x / scale).to(torch.float8_e4m3fn), scale
+
+
+def swiglu_e4m3(M: int, K: int, N: int, seed: int = 3, w_std: float = 0.02):
+    """e4m3 A (N(0,1) fits without a scale) and e4m3 W1, W2 sharing one
+    per-tensor scale (the interleaved weight is one tensor): returns
+    (A, W1, W2, scale_w)."""
+    g = generator(seed)
+    A = torch.randn(M, K, generator=g).to(torch.float8_e4m3fn)
+    W1 = torch.randn(K, N, generator=g) * w_std
+    W2 = torch.randn(K, N, generator=g) * w_std
+    amax = max(float(W1.abs().max()), float(W2.abs().max()))
+    scale = amax / 448.0 if amax > 0 else 1.0
+    return A, (W1 / scale).to(torch.float8_e4m3fn), (W2 / scale).to(torch.float8_e4m3fn), scale

@@ -335,3 +335,50 @@ def test_mlp_down_projection_bruteforce():
                 s += Y[i, n] * Wdf[n][k]
             assert out[i, k] == s
     assert np.array_equal(oracle.mlp(A, W1, W2, (2 * Wd).to(torch.bfloat16), M, N, K), 2 * out)
+
+
+
+def test_e4m3_decoder_all_patterns():
+    bits = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = bits.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_to_f64(int(b)) for b in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert oracle.e4m3_to_f64(0x7E) == 448.0          # largest finite value
+
+
+@pytest.mark.parametrize("shape", [(3, 5, 7), (9, 16, 33)])
+def test_e4m3_gemm_bruteforce_exact(shape):
+    """Small integers are exact in e4m3 (|x| <= 16) and in every partial sum."""
+    M, N, K = shape
+    g = synth.generator(M + N + K + 500)
+    A = synth.small_ints((M, K), g, -6, 6, dtype=torch.float32).to(torch.float8_e4m3fn)
+    Bt = synth.small_ints((N, K), g, -6, 6, dtype=torch.float32).to(torch.float8_e4m3fn)
+    Ai = A.to(torch.float64).tolist()
+    Bi = Bt.to(torch.float64).tolist()
+    D = oracle.gemm(0, 1, M, N, K, 0.5, A, K, Bt, K, 0.0, in_type="e4m3")
+    for i in range(M):
+        for j in range(N):
+            assert D[i, j] == 0.5 * sum(Ai[i][p] * Bi[j][p] for p in range(K))
+
+
+def test_swiglu_typed_matches_swiglu_and_scales():
+    M, K, N = 5, 24, 7
+    A, W1, W2 = synth.swiglu(M, K, N, seed=41, w_std=0.2)
+    ref = oracle.swiglu(A, W1, W2, M, N, K)
+    assert np.array_equal(oracle.swiglu_typed(A, W1, W2, M, N, K, in_type="bf16", scale=1.0), ref)
+    # scale s on both products: SiLU(s g) s u; with s = 2 and W halved it is unchanged
+    W1h = (W1.to(torch.float32) / 2).to(torch.bfloat16)
+    W2h = (W2.to(torch.float32) / 2).to(torch.bfloat16)
+    got = oracle.swiglu_typed(A, W1h, W2h, M, N, K, in_type="bf16", scale=2.0)
+    assert np.allclose(got, ref, rtol=1e-15, atol=1e-15)
+
+
+def test_interleave_t8_hand_example():
+    W1 = torch.tensor([[1, 2], [3, 4]], dtype=torch.float32).to(torch.float8_e4m3fn)
+    W2 = torch.tensor([[5, 6], [7, 8]], dtype=torch.float32).to(torch.float8_e4m3fn)
+    Wt = oracle.interleave_t8(W1, W2, 2, 2)
+    got = torch.from_numpy(Wt).view(torch.float8_e4m3fn).to(torch.int64).tolist()
+    # rows: W1 col 0, W2 col 0, W1 col 1, W2 col 1
+    assert got == [[1, 3], [5, 7], [2, 4], [6, 8]]
