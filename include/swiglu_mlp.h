@@ -258,6 +258,18 @@ SWG_API const char *swg_status_string(int status);
  */
 SWG_API int swg_get_device_error(void *stream);
 
+/*
+ * swg_selftest_wait_timeout — diagnostic: exercises the bounded-wait path the
+ * pipeline kernels use, on purpose.  Launches one small kernel that waits, with
+ * the kernels' own wait routine, on a barrier nothing ever completes; after
+ * limit_ns (1 ns .. 1 s) it gives up, records SWG_ERR_DEVICE_TIMEOUT in the
+ * device error word and exits, leaving the context usable.  The next
+ * swg_get_device_error() on that stream returns SWG_ERR_DEVICE_TIMEOUT (and
+ * clears it).  No counterpart on the pages: it tests this library's failure
+ * reporting without faulting or hanging the GPU.
+ */
+SWG_API int swg_selftest_wait_timeout(int64_t limit_ns, void *stream);
+
 /* Number of kernels this library has launched in this process (all devices). */
 SWG_API uint64_t swg_launch_count(void);
 

@@ -20,7 +20,7 @@ __all__ = [
     "SwgError", "OP_N", "OP_T", "F16_F32OUT", "BF16", "F16", "BF16_F32OUT", "E4M3_BF16OUT",
     "E4M3_F32OUT", "swiglu_mlp_fp8",
     "gemm", "gemm_ex", "gemm_splitk_noalloc", "swiglu_mlp", "swiglu_mlp_dual", "swiglu_mlp_forward", "swiglu_interleave", "status_string",
-    "get_device_error", "launch_count", "shutdown", "gemm_into",
+    "get_device_error", "launch_count", "shutdown", "gemm_into", "selftest_wait_timeout",
     "swiglu_mlp_into", "interleave_weights", "library_path", "load",
 ]
 
@@ -80,6 +80,8 @@ def load():
         lib.swg_status_string.restype = ctypes.c_char_p
         lib.swg_get_device_error.argtypes = [vp]
         lib.swg_get_device_error.restype = i32
+        lib.swg_selftest_wait_timeout.argtypes = [i64, vp]
+        lib.swg_selftest_wait_timeout.restype = i32
         lib.swg_launch_count.argtypes = []
         lib.swg_launch_count.restype = ctypes.c_uint64
         lib.swg_shutdown.argtypes = []
@@ -177,6 +179,12 @@ def status_string(status: int) -> str:
 def get_device_error(stream=None) -> int:
     """Synchronises the stream and returns (and clears) the device error word."""
     return load().swg_get_device_error(_stream(stream))
+
+
+def selftest_wait_timeout(limit_ns: int, stream=None) -> int:
+    """Runs a kernel whose bounded wait is made to run out (see the C header)."""
+    return _check(load().swg_selftest_wait_timeout(int(limit_ns), _stream(stream)),
+                  "swg_selftest_wait_timeout")
 
 
 def launch_count() -> int:

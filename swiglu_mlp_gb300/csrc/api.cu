@@ -410,6 +410,27 @@ __global__ void interleave_kernel(const uint16_t *W1, const uint16_t *W2, uint16
     }
 }
 
+// One warp waits, through the pipeline kernels' own bounded wait, on an
+// mbarrier that nothing ever arrives on; after limit_ns it records
+// SWG_ERR_DEVICE_TIMEOUT in the error word and returns, like a pipeline
+// kernel whose partner never shows up.
+__global__ void selftest_wait_kernel(int *err, unsigned long long limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        swg::mbar_init(swg::smem_u32(&bar), 1);
+        abort_flag = 0;
+        swg::fence_barrier_init();
+    }
+    __syncthreads();
+    bool ok = true;
+    if (threadIdx.x == 0)
+        ok = swg::wait_bounded(swg::smem_u32(&bar), 0, &abort_flag, err, true, limit_ns);
+    __syncthreads();
+    (void)ok;
+}
+
 int grid_for(long long work, int sms)
 {
     long long g = cdiv(work, 256);
@@ -440,6 +461,17 @@ const char *swg_status_string(int status)
 }
 
 uint64_t swg_launch_count(void) { return g_launches.load(); }
+
+int swg_selftest_wait_timeout(int64_t limit_ns, void *stream)
+{
+    if (limit_ns <= 0 || limit_ns > 1000000000) return SWG_ERR_INVALID_ARG;
+    DeviceState *d = nullptr;
+    if (int rc = device_state(d)) return rc;
+    selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        d->err, (unsigned long long)limit_ns);
+    g_launches++;
+    return cudaGetLastError() == cudaSuccess ? SWG_OK : SWG_ERR_CUDA;
+}
 
 // GEMM with e4m3 A and B (kind::f8f6f4): A stored M x K and B stored N x K,
 // both K-major; per-tensor dequantisation scales are folded into alpha.

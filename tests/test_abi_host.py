@@ -125,3 +125,9 @@ def test_python_binding_raises(lib):
 def test_shutdown_is_idempotent(lib):
     swg.shutdown()
     swg.shutdown()
+
+
+def test_selftest_timeout_argument_checks(lib):
+    assert lib.swg_selftest_wait_timeout(0, None) == INVALID
+    assert lib.swg_selftest_wait_timeout(-5, None) == INVALID
+    assert lib.swg_selftest_wait_timeout(2_000_000_000, None) == INVALID
