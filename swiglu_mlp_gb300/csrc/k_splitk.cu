@@ -21,6 +21,9 @@ __global__ void __launch_bounds__(256)
                          float alpha, float beta, void *D, long long ldd, int out_kind)
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // A GEMM queued behind this reduction may set up meanwhile; it waits for
+    // this grid's completion before it touches global memory.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int quads = (N + 3) / 4;
     const long long total = (long long)M * quads;
     const long long split_stride = (long long)M * ld_ws;

@@ -31,14 +31,20 @@ cudaError_t launch_tc_impl(const CUtensorMap &ta, const CUtensorMap &tb, const C
     cfg.blockDim = dim3(NUM_THREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    // Programmatic stream serialisation: this grid may be scheduled once the
+    // kernel before it on the stream has triggered its dependents; it waits
+    // for that kernel's completion (griddepcontrol.wait) after its set-up.
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (PAIR) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
         cfg.gridDim = dim3(2 * units);
     } else {
         cfg.gridDim = dim3(units);

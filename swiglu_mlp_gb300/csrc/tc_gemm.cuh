@@ -365,10 +365,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int first_unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
     const int unit_step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
-    // Split-K: let the reduction kernel queued behind this one be scheduled
-    // now; it waits (griddepcontrol.wait) until this grid has completed.
-    if (EPI == EPI_SPLITK || EPI == EPI_SPLITK_T)
-        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Programmatic dependent launch: the kernel queued behind this one on the
+    // stream (the split-K reduction, or the next GEMM of a chain) may be
+    // scheduled from now on.  It runs its set-up as SMs free up and then waits
+    // (griddepcontrol.wait) until this grid has completed and its writes are
+    // visible.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -412,6 +414,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     tc_fence_after();
     const uint32_t tmem_base = (PAIR || warp != 0) ? *tmem_holder : 0u;
+    // Everything above touches only this CTA's own resources and the kernel
+    // parameters.  Global memory is read and written only after the grid this
+    // one was launched behind (if any) has completed: a no-op without one.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
