@@ -13,8 +13,10 @@ The same JSON line carries, measured in the same run:
   e2e           the same metric with A, B copied from pinned host memory and
                 the four D read back inside the timed region;
   cpu_baseline  the FP64 oracle on the host cores over a bounded row sample;
-  components    fused SwiGLU (small-model and 8B shapes) and skinny split-K
-                timings with an L2 flush between repetitions;
+  components    fused SwiGLU (small-model and 8B shapes), skinny split-K and
+                the other workloads, each timed in isolation with an L2 flush
+                between repetitions and back to back over input copies larger
+                than L2 ("stream");
   clocks        SM clocks and throttle reasons sampled during the timed region.
 
 ``--impl reference`` times the FP64 oracle instead (rank 0 only), as the
@@ -63,7 +65,7 @@ def kernel_source_digest() -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "swiglu_mlp_gb300", "csrc")
-    for name in ("tc_gemm.cuh", "ptx.cuh", "api.cu"):
+    for name in ("tc_gemm.cuh", "ptx.cuh", "launch_impl.cuh", "api.cu"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -521,9 +523,34 @@ def build_case(kind, M, K, N, dev, stream):
     raise ValueError(kind)
 
 
+L2_BYTES = 129 * 1000 * 1000        # GB300 L2 capacity
+
+
+def time_stream(fns, min_calls, stream, dev):
+    """Mean time per call of back-to-back calls cycling over `fns` (one per
+    input set), one event pair around the whole run: consecutive launches
+    overlap as they do in a serving loop."""
+    import torch
+    for f in fns:
+        f()
+    rounds = max(1, -(-min_calls // len(fns)))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(rounds):
+        for f in fns:
+            f()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / (rounds * len(fns))
+
+
 def run_components(args, dev, stream):
-    """SwiGLU and skinny split-K timings: median of reps, each after an L2
-    flush and (skinny) a restore of C, both outside the CUDA events."""
+    """Per workload, two timings.  Isolated: median of reps, each after an L2
+    flush and (beta = 1 cases) a restore of C, both outside the CUDA events.
+    Back-to-back: mean per call over calls cycling through enough copies of the
+    inputs that every call's data was last touched at least 2 x L2 bytes
+    earlier (inputs larger than L2 instead of a flush)."""
     import torch
 
     import swiglu_mlp_gb300 as swg
@@ -536,6 +563,10 @@ def run_components(args, dev, stream):
     res = {}
     for name, kind, M, K, N in component_cases():
         fn, reset, flops, byts = build_case(kind, M, K, N, dev, stream)
+        n_sets = min(16, max(1, -(-2 * L2_BYTES // byts)))
+        sets = [fn] + [build_case(kind, M, K, N, dev, stream)[0] for _ in range(n_sets - 1)]
+        stream_ms = time_stream(sets, max(20, args.component_reps), stream, dev)
+        del sets
         for _ in range(3):
             fn()
         times = []
@@ -558,10 +589,13 @@ def run_components(args, dev, stream):
         entry = {"median_us": round(med * 1e3, 2), "min_us": round(ms[0] * 1e3, 2),
                  "tflops": round(flops / med / 1e9, 1), "gbs": round(byts / med / 1e6, 1),
                  "roofline_frac": round(max(t_tensor, t_hbm) / (med / 1e3), 4),
-                 "bound": "tensor" if t_tensor > t_hbm else "hbm"}
+                 "bound": "tensor" if t_tensor > t_hbm else "hbm",
+                 "stream": {"us_per_call": round(stream_ms * 1e3, 2), "input_sets": n_sets,
+                            "roofline_frac": round(max(t_tensor, t_hbm) / (stream_ms / 1e3), 4)}}
         if kind in ("skinny", "gemv"):
             entry["hbm_frac"] = round(byts / med / 1e6 / bw, 4)
         res[name] = entry
+        torch.cuda.empty_cache()
     if swg.get_device_error(stream) != 0:
         raise RuntimeError("device error word set during the component timings")
     return res
