@@ -171,6 +171,30 @@ bool make_tmap_u8(CUtensorMap *m, const void *ptr, int64_t inner, int64_t outer,
     return r == CUDA_SUCCESS;
 }
 
+// Output map of the staged last-tile stores: `cols` x `rows` elements of
+// `esize` (2 or 4) bytes with a row stride of `ld` elements -- and with
+// `depth` > 0, a third dimension of that many slices `dstride` elements
+// apart (the split-K workspace).  Box: 128 bytes x 128 rows, 128-byte swizzle.
+// Stores are clipped at the map's bounds, but along a row only at 16-byte
+// granules: callers use the map only where cols * esize is a multiple of 16
+// or the row's padding up to the next granule is scratch.
+bool make_tmap_store(CUtensorMap *m, void *ptr, int esize, int64_t cols, int64_t rows, int64_t ld,
+                     int64_t depth = 0, int64_t dstride = 0)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint32_t rank = depth > 0 ? 3u : 2u;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)(depth > 0 ? depth : 1)};
+    cuuint64_t strides[2] = {(cuuint64_t)(ld * esize), (cuuint64_t)(dstride * esize)};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / esize), 128u, 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = fn(m, esize == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16,
+                    rank, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // tcgen05 instruction descriptor, kind::f16: D=F32 (bits 4-5 = 1), A/B type
 // (bits 7-9, 10-12: 0 = f16, 1 = bf16), A/B major (bits 15, 16: 1 = MN-major),
 // N >> 3 (bits 17-22), M >> 4 (bits 24-28).  With bf16 = false the same
@@ -529,7 +553,14 @@ static int gemm_fp8(int transA, int transB, int64_t M, int64_t N, int64_t K, flo
     p.ldd = ldc;
     p.out_kind = out_kind;
     p.err = d->err;
-    if (swg::launch_tc_store_fp8(bn, pair, ta, tb, p, tc.units, s) != cudaSuccess)
+    CUtensorMap td;
+    if (beta == 0.0f && (N * (out_kind == swg::OUT_F32 ? 4 : 2)) % 16 == 0) {
+        if (!make_tmap_store(&td, C, out_kind == swg::OUT_F32 ? 4 : 2, N, M, ldc))
+            return SWG_ERR_CUDA;
+        p.tma_store = 1;
+    }
+    if (swg::launch_tc_store_fp8(bn, pair, ta, tb, p, tc.units, s, p.tma_store ? &td : nullptr) !=
+        cudaSuccess)
         return SWG_ERR_CUDA;
     g_launches++;
     return SWG_OK;
@@ -648,13 +679,26 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
             return rc;
         p.ws = static_cast<float *>(w->base);
         p.ld_ws = ld_ws;
-        e = swg::launch_tc_splitk(bn, pair, ta, tb, p, units, s);
+        // Each CTA's last partial tile leaves through shared memory and TMA
+        // stores into ws viewed as [splits][M][ld_ws].
+        CUtensorMap tw;
+        if (!make_tmap_store(&tw, p.ws, 4, N, M, ld_ws, splits, M * ld_ws)) return SWG_ERR_CUDA;
+        p.tma_store = 1;
+        e = swg::launch_tc_splitk(bn, pair, ta, tb, p, units, s, &tw);
         if (e == cudaSuccess) {
             g_launches++;
             e = swg::launch_splitk_reduce(p, d->sms, s);
         }
     } else {
-        e = swg::launch_tc_store(bn, pair, ta, tb, p, tc.units, s);
+        // beta = 0: each CTA's last tile leaves through shared memory and TMA
+        // stores (beta != 0 reads C and keeps the direct stores).  TMA clips
+        // a row only at 16-byte granules, so N must end on one.
+        CUtensorMap td;
+        if (beta == 0.0f && (N * ti.out_bytes) % 16 == 0) {
+            if (!make_tmap_store(&td, C, ti.out_bytes, N, M, ldc)) return SWG_ERR_CUDA;
+            p.tma_store = 1;
+        }
+        e = swg::launch_tc_store(bn, pair, ta, tb, p, tc.units, s, p.tma_store ? &td : nullptr);
     }
     if (e != cudaSuccess) return SWG_ERR_CUDA;
     g_launches++;
@@ -722,7 +766,15 @@ int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M, int64_t N
     p.ldd = N;
     p.out_kind = swg::OUT_BF16;
     p.err = d->err;
-    if (swg::launch_tc_swiglu(bn, pair, ta, tb, p, tc.units, s) != cudaSuccess)
+    // Each CTA's last tile leaves through shared memory and TMA stores (whole
+    // 128-byte boxes: 64 output columns per tile, so bn >= 128).
+    CUtensorMap ty;
+    if (bn >= 128) {
+        if (!make_tmap_store(&ty, Y, 2, N, M, N)) return SWG_ERR_CUDA;
+        p.tma_store = 1;
+    }
+    if (swg::launch_tc_swiglu(bn, pair, ta, tb, p, tc.units, s, p.tma_store ? &ty : nullptr) !=
+        cudaSuccess)
         return SWG_ERR_CUDA;
     g_launches++;
     return SWG_OK;
@@ -778,7 +830,13 @@ int swiglu_mlp_fp8(const void *A, const void *W_fused_t, void *Y, int64_t M, int
     p.ldd = N;
     p.out_kind = swg::OUT_BF16;
     p.err = d->err;
-    if (swg::launch_tc_swiglu_fp8(bn, pair, ta, tb, p, tc.units, s) != cudaSuccess)
+    CUtensorMap ty;
+    if (bn >= 128) {
+        if (!make_tmap_store(&ty, Y, 2, N, M, N)) return SWG_ERR_CUDA;
+        p.tma_store = 1;
+    }
+    if (swg::launch_tc_swiglu_fp8(bn, pair, ta, tb, p, tc.units, s, p.tma_store ? &ty : nullptr) !=
+        cudaSuccess)
         return SWG_ERR_CUDA;
     g_launches++;
     return SWG_OK;

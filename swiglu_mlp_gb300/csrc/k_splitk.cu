@@ -106,18 +106,19 @@ __global__ void __launch_bounds__(256)
 }
 
 cudaError_t launch_tc_splitk(int bn, bool pair, const CUtensorMap &ta, const CUtensorMap &tb,
-                             const TileParams &p, int units, cudaStream_t s)
+                             const TileParams &p, int units, cudaStream_t s,
+                             const CUtensorMap *tout)
 {
     if (pair) {
         switch (bn) {
-        case 128: return launch_tc_impl<128, EPI_SPLITK, true>(ta, tb, p, units, s);
-        case 256: return launch_tc_impl<256, EPI_SPLITK, true>(ta, tb, p, units, s);
+        case 128: return launch_tc_impl<128, EPI_SPLITK, true>(ta, tb, p, units, s, tout);
+        case 256: return launch_tc_impl<256, EPI_SPLITK, true>(ta, tb, p, units, s, tout);
         default: return cudaErrorInvalidValue;
         }
     }
     switch (bn) {
-    case 128: return launch_tc_impl<128, EPI_SPLITK, false>(ta, tb, p, units, s);
-    case 256: return launch_tc_impl<256, EPI_SPLITK, false>(ta, tb, p, units, s);
+    case 128: return launch_tc_impl<128, EPI_SPLITK, false>(ta, tb, p, units, s, tout);
+    case 256: return launch_tc_impl<256, EPI_SPLITK, false>(ta, tb, p, units, s, tout);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -4,19 +4,20 @@
 
 namespace swg {
 cudaError_t launch_tc_store(int bn, bool pair, const CUtensorMap &ta, const CUtensorMap &tb,
-                            const TileParams &p, int units, cudaStream_t s)
+                            const TileParams &p, int units, cudaStream_t s,
+                            const CUtensorMap *tout)
 {
     if (pair) {
         switch (bn) {
-        case 128: return launch_tc_impl<128, EPI_STORE, true>(ta, tb, p, units, s);
-        case 256: return launch_tc_impl<256, EPI_STORE, true>(ta, tb, p, units, s);
+        case 128: return launch_tc_impl<128, EPI_STORE, true>(ta, tb, p, units, s, tout);
+        case 256: return launch_tc_impl<256, EPI_STORE, true>(ta, tb, p, units, s, tout);
         default: return cudaErrorInvalidValue;
         }
     }
     switch (bn) {
-    case 64: return launch_tc_impl<64, EPI_STORE, false>(ta, tb, p, units, s);
-    case 128: return launch_tc_impl<128, EPI_STORE, false>(ta, tb, p, units, s);
-    case 256: return launch_tc_impl<256, EPI_STORE, false>(ta, tb, p, units, s);
+    case 64: return launch_tc_impl<64, EPI_STORE, false>(ta, tb, p, units, s, tout);
+    case 128: return launch_tc_impl<128, EPI_STORE, false>(ta, tb, p, units, s, tout);
+    case 256: return launch_tc_impl<256, EPI_STORE, false>(ta, tb, p, units, s, tout);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -13,12 +13,16 @@ namespace swg {
 // of the tile widths the TU instantiates (anything else returns
 // cudaErrorInvalidValue without launching); `pair` selects the CTA-pair
 // (cta_group::2, 256-row tile) variant, for which `units` counts pairs.
+// `tout`: output map of the staged last-tile stores, when p.tma_store is set.
 cudaError_t launch_tc_store(int bn, bool pair, const CUtensorMap &ta, const CUtensorMap &tb,
-                            const TileParams &p, int units, cudaStream_t s);
+                            const TileParams &p, int units, cudaStream_t s,
+                            const CUtensorMap *tout = nullptr);
 cudaError_t launch_tc_swiglu(int bn, bool pair, const CUtensorMap &ta, const CUtensorMap &tb,
-                             const TileParams &p, int units, cudaStream_t s);
+                             const TileParams &p, int units, cudaStream_t s,
+                             const CUtensorMap *tout = nullptr);
 cudaError_t launch_tc_splitk(int bn, bool pair, const CUtensorMap &ta, const CUtensorMap &tb,
-                             const TileParams &p, int units, cudaStream_t s);
+                             const TileParams &p, int units, cudaStream_t s,
+                             const CUtensorMap *tout = nullptr);
 
 // Split-K with swapped operands (the kernel computes the transposed product;
 // `bn` 16, 32 or 64 is the width of the original rows it covers).
@@ -34,9 +38,11 @@ int max_active_pairs_dual(int bn, int sms);
 
 // 8-bit (e4m3) operands, kind::f8f6f4 MMAs, K-major A and B only.
 cudaError_t launch_tc_store_fp8(int bn, bool pair, const CUtensorMap &ta, const CUtensorMap &tb,
-                                const TileParams &p, int units, cudaStream_t s);
+                                const TileParams &p, int units, cudaStream_t s,
+                                const CUtensorMap *tout = nullptr);
 cudaError_t launch_tc_swiglu_fp8(int bn, bool pair, const CUtensorMap &ta, const CUtensorMap &tb,
-                                 const TileParams &p, int units, cudaStream_t s);
+                                 const TileParams &p, int units, cudaStream_t s,
+                                 const CUtensorMap *tout = nullptr);
 int max_active_pairs_fp8(int kind, int bn, int sms);   // kind 0 = GEMM, 1 = SwiGLU
 
 // Resident CTA pairs for the pair variants (0 if unknown or not instantiated).

@@ -11,7 +11,7 @@ namespace swg {
 // launches it.  `units` is the number of CTAs (1-CTA mode) or of CTA pairs
 // (PAIR: launched as clusters of two).
 template <int BN, int EPI, bool PAIR, bool FP8 = false>
-cudaError_t launch_tc_impl(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tb2,
+cudaError_t launch_tc_impl(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tx,
                            const TileParams &p, int units, cudaStream_t s)
 {
     using C = Cfg<BN, PAIR>;
@@ -49,15 +49,16 @@ cudaError_t launch_tc_impl(const CUtensorMap &ta, const CUtensorMap &tb, const C
     } else {
         cfg.gridDim = dim3(units);
     }
-    return cudaLaunchKernelEx(&cfg, kernel, ta, tb, tb2, p);
+    return cudaLaunchKernelEx(&cfg, kernel, ta, tb, tx, p);
 }
 
-// Kernels with one B operand: the second B map is unused (passed again).
+// Kernels with one B operand: the third map slot carries the output map of
+// the staged last-tile stores (p.tma_store), or B again when there is none.
 template <int BN, int EPI, bool PAIR, bool FP8 = false>
 cudaError_t launch_tc_impl(const CUtensorMap &ta, const CUtensorMap &tb, const TileParams &p,
-                           int units, cudaStream_t s)
+                           int units, cudaStream_t s, const CUtensorMap *tout = nullptr)
 {
-    return launch_tc_impl<BN, EPI, PAIR, FP8>(ta, tb, tb, p, units, s);
+    return launch_tc_impl<BN, EPI, PAIR, FP8>(ta, tb, tout ? *tout : tb, p, units, s);
 }
 
 // How many CTA pairs of this kernel can be resident at once (clusters of two

@@ -85,6 +85,11 @@ struct TileParams {
     int group_m;                 // raster: m-blocks per group
     uint32_t idesc;              // tcgen05 instruction descriptor
     int bk;                      // elements per 128-byte K block: 64 (16-bit) or 128 (fp8)
+    // 1: each CTA writes its last tile through shared memory with TMA stores
+    // via the output map passed in the kernel's third tensor-map slot (D, Y,
+    // or the 3-D split-K workspace); only with beta = 0 and whole 128-byte
+    // output boxes.
+    int tma_store;
     int a_mn_major;              // op(A) stored M-contiguous (transA = T)
     int b_mn_major;              // op(B) stored N-contiguous (transB = N)
     float alpha, beta;
@@ -110,12 +115,14 @@ struct Cfg {
     // and shrank L1), at most 12.
     static constexpr int STAGES_RAW = (192 * 1024) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
-    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int NUM_BARS = 2 * STAGES + 6;
     static constexpr int TMEM_COLS = (2 * BN) <= 32 ? 32 : (2 * BN) <= 64 ? 64
                                    : (2 * BN) <= 128 ? 128 : (2 * BN) <= 256 ? 256 : 512;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 64;
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "BN must be a multiple of 16, <= 256");
     static_assert(!PAIR || BN % 128 == 0, "pair tiles split B in 64-column boxes per CTA");
+    static_assert(STAGES * STAGE_BYTES >= BM * BN * 4 || BN < 64,
+                  "the stage area holds a staged FP32 output tile");
 };
 
 // Tile coordinates of work unit u (grouped raster: walk GROUP m-blocks down a
@@ -331,13 +338,104 @@ __device__ __forceinline__ void epi_chunk(const TileParams &p, const uint32_t (&
     }
 }
 
+// ------------------------------------------------ staged last-tile stores
+// A CTA's last tile is written to shared memory (the pipeline stages, all
+// consumed by then) as boxes of 128 rows x 128 bytes -- 64 16-bit or 32 FP32
+// output columns -- and stored with TMA: whole cache lines instead of one
+// 16-byte piece of 32 different rows per warp store.  Within a box, row r's
+// eight 16-byte chunks sit at chunk (j XOR r mod 8): the tensor map's 128-byte
+// swizzle, which also spreads a warp's writes of one chunk over all banks.
+__device__ __forceinline__ void stage16(uint32_t base, int row, int byte_col, uint4 v)
+{
+    const int box = byte_col >> 7;
+    const int j = (byte_col >> 4) & 7;
+    st_shared_v4(base + (uint32_t)(box * 16384 + row * 128 + ((j ^ (row & 7)) << 4)), v);
+}
+
+__device__ __forceinline__ uint4 f32x4(float a, float b, float c, float d)
+{
+    return make_uint4(__float_as_uint(a), __float_as_uint(b), __float_as_uint(c),
+                      __float_as_uint(d));
+}
+
+// Output values of one 32-column accumulator chunk (tile columns
+// [c0, c0 + 32)) of tile row `row`, staged: the same arithmetic as epi_chunk
+// with beta = 0.
+template <int EPI>
+__device__ __forceinline__ void stage_epi_chunk(const TileParams &p, const uint32_t (&r)[32],
+                                                uint32_t base, int row, int c0)
+{
+    if (EPI == EPI_STORE) {
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[j]);
+        if (p.out_kind == OUT_F32) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                stage16(base, row, (c0 + 4 * q) * 4,
+                        f32x4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                stage16(base, row, (c0 + 8 * q) * 2,
+                        make_uint4(pack2(v[8 * q], v[8 * q + 1], p.out_kind),
+                                   pack2(v[8 * q + 2], v[8 * q + 3], p.out_kind),
+                                   pack2(v[8 * q + 4], v[8 * q + 5], p.out_kind),
+                                   pack2(v[8 * q + 6], v[8 * q + 7], p.out_kind)));
+        }
+    } else if (EPI == EPI_SWIGLU) {
+        float y[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            y[j] = silu_f32(p.alpha * __uint_as_float(r[2 * j])) *
+                   (p.alpha * __uint_as_float(r[2 * j + 1]));
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+            stage16(base, row, (c0 / 2 + 8 * q) * 2,
+                    make_uint4(pack2(y[8 * q], y[8 * q + 1], OUT_BF16),
+                               pack2(y[8 * q + 2], y[8 * q + 3], OUT_BF16),
+                               pack2(y[8 * q + 4], y[8 * q + 5], OUT_BF16),
+                               pack2(y[8 * q + 6], y[8 * q + 7], OUT_BF16)));
+    } else {   // EPI_SPLITK: the raw FP32 partial
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            stage16(base, row, (c0 + 4 * q) * 4,
+                    f32x4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                          __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])));
+    }
+}
+
+// TMA stores of the staged boxes of tile (mb, nb) for this CTA's rows [m0,
+// m0 + 128): boxes wholly right of the output's last column are skipped,
+// the rest are clipped by the tensor map.
+template <int EPI, int BN>
+__device__ __forceinline__ void store_staged(const TileParams &p, const CUtensorMap *tm,
+                                             uint32_t base, int m0, int nb, int split)
+{
+    const int esize = (EPI == EPI_SPLITK || (EPI == EPI_STORE && p.out_kind == OUT_F32)) ? 4 : 2;
+    const int out_cols = EPI == EPI_SWIGLU ? BN / 2 : BN;
+    const int n_out = EPI == EPI_SWIGLU ? p.N / 2 : p.N;
+    const int box_cols = 128 / esize;
+    const int x0 = nb * out_cols;
+    for (int b = 0; b < out_cols / box_cols; ++b) {
+        const int x = x0 + b * box_cols;
+        if (x >= n_out) break;
+        if (EPI == EPI_SPLITK)
+            tma_store_3d(tm, base + b * 16384, x, m0, split);
+        else
+            tma_store_2d(tm, base + b * 16384, x, m0);
+    }
+    bulk_commit_group();
+    bulk_wait_all();
+}
+
 // FP8: operands are 8-bit (e4m3/e5m2) and the MMA is kind::f8f6f4.  In bytes
 // nothing else changes: a 128-byte swizzled stage row holds 128 elements and
 // each MMA (K = 32) consumes 32 bytes of it, as a kind::f16 MMA (K = 16) does.
 template <int BN, int EPI, bool PAIR, bool FP8 = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmB2, const TileParams p)
+                   const __grid_constant__ CUtensorMap tmX, const TileParams p)
 {
     using C = Cfg<BN, PAIR>;
     constexpr int S = C::STAGES;
@@ -353,6 +451,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t *acc_full = bars + 2 * S;
     uint64_t *acc_empty = bars + 2 * S + 2;
     uint64_t *mma_done = bars + 2 * S + 4;
+    uint64_t *staged = bars + 2 * S + 5;     // last tile written to shared memory
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + C::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
@@ -383,11 +482,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(smem_u32(&acc_empty[b]), NUM_EPI_WARPS * (PAIR ? 2 : 1));
         }
         mbar_init(smem_u32(mma_done), 1);
+        mbar_init(smem_u32(staged), NUM_EPI_WARPS);
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        if (EPI == EPI_SWIGLU_DUAL) tma_prefetch_desc(&tmB2);
+        if (EPI == EPI_SWIGLU_DUAL || p.tma_store) tma_prefetch_desc(&tmX);
     }
     if (warp == 1) {
         if (PAIR) {
@@ -474,7 +574,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         for (int c = 0; c < C::B_COLS / 64; ++c) {
                             const bool up = PAIR ? (rank != 0) : (c >= BN / 128);
                             const int cc = PAIR ? c : (c % (BN / 128));
-                            load(b_dst + c * 8192, up ? &tmB2 : &tmB, nd + cc * 64, k0);
+                            load(b_dst + c * 8192, up ? &tmX : &tmB, nd + cc * 64, k0);
                         }
                     } else if (!p.b_mn_major) {
                         load(b_dst, &tmB, k0, n0);                          // box {64 K, B_COLS N}
@@ -699,6 +799,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
             const int m = mb * C::TILE_M + (int)rank * BM + row;
             const bool row_ok = m < p.M;
+            // The CTA's last tile goes through shared memory (see
+            // stage_epi_chunk); earlier tiles overlap the next main loop and
+            // are stored directly.
+            const bool stage_out = p.tma_store && u + unit_step >= p.units;
+            const uint32_t sbase = smem_u32(smem);
+            auto emit = [&](const uint32_t(&r)[32], int c) {
+                if (stage_out)
+                    stage_epi_chunk<EPI>(p, r, sbase, row, c * 32);
+                else if (row_ok)
+                    epi_chunk<EPI>(p, r, m, nb * BN + c * 32, split);
+            };
             // Two register buffers: the load of chunk c+1 is in flight while
             // chunk c is converted and stored (tcgen05.wait::ld waits for all
             // earlier loads, so each wait retires exactly the older chunk).
@@ -708,17 +819,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int c = c_begin; c < c_end; c += 2) {
                 tmem_ld_wait(ra);
                 if (c + 1 < c_end) tmem_ld_32cols(t_row + (c + 1) * 32, rb);
-                if (row_ok) epi_chunk<EPI>(p, ra, m, nb * BN + c * 32, split);
+                emit(ra, c);
                 if (c + 1 < c_end) {
                     tmem_ld_wait(rb);
                     if (c + 2 < c_end) tmem_ld_32cols(t_row + (c + 2) * 32, ra);
-                    if (row_ok) epi_chunk<EPI>(p, rb, m, nb * BN + (c + 1) * 32, split);
+                    emit(rb, c + 1);
                 }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (stage_out) {
+                // This warp's rows are staged: publish them to the TMA (async
+                // proxy) and count the warp in.  Warp 2's lane 0 waits, with
+                // a bound, for all eight warps and issues the stores.
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(staged));
+                if (warp == EPI_WARP0 && lane == 0 &&
+                    wait_bounded(smem_u32(staged), 0, abort_flag, p.err))
+                    store_staged<EPI, BN>(p, &tmX, sbase, mb * C::TILE_M + (int)rank * BM, nb,
+                                          split);
+                __syncwarp();
             }
             // Accumulator drained: hand it back to the MMA warp (the leader's
             // barrier in pair mode), one arrival per warp.
-            tc_fence_before();
-            __syncwarp();
             if (lane == 0) {
                 if (PAIR)
                     mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[acc]), 0));

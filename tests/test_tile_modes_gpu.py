@@ -88,3 +88,36 @@ def test_split_k_both_tile_shapes(tile_mode, split_k, tA, tB):
     assert swg.get_device_error() == 0
     yhat = oracle.gemm(tA, tB, M, N, K, 0.75, Ap, lda, Bp, ldb, 0.5, C, N)
     check_half(to_f64(Cd), yhat, f"{tile_mode} split={split_k} tA={tA} tB={tB}")
+
+
+@pytest.mark.parametrize("tile_mode", MODES, indirect=True)
+@pytest.mark.parametrize("code", ["BF16", "BF16_F32OUT"])
+@pytest.mark.parametrize("shape", [(300, 520, 200), (129, 392, 72), (1000, 648, 1024),
+                                   (17, 136, 64), (300, 517, 200), (260, 130, 96)])
+def test_beta_zero_edges_and_padding(tile_mode, code, shape):
+    """beta = 0: each CTA's last tile is staged in shared memory and written
+    with TMA stores clipped at the output's bounds (rows ending mid-granule,
+    N * size not a multiple of 16 bytes, keep the direct stores).  Ragged M
+    and N with a padded ldc: every output element matches the oracle and no
+    byte of the padding columns changes."""
+    M, N, K = shape
+    dt = getattr(swg, code)
+    g = synth.generator(900 + M + N + K + dt)
+    A = synth.normal((M, K), g)
+    B = synth.normal((K, N), g)
+    out_t = torch.float32 if dt == swg.BF16_F32OUT else torch.bfloat16
+    ldb = round_up(N, 8)
+    Bp = padded(B, ldb, 3.0)
+    ldc = round_up(N + 24, 8)
+    D0 = torch.full((M, ldc), 7.0, dtype=out_t)
+    Dd = D0.cuda()
+    swg.gemm(0, 0, M, N, K, 1.0, A.cuda(), K, Bp.cuda(), ldb, 0.0, Dd, ldc, dt)
+    assert swg.get_device_error() == 0
+    out = Dd.cpu()
+    assert torch.equal(out[:, N:], D0[:, N:])
+    yhat = oracle.gemm(0, 0, M, N, K, 1.0, A, K, Bp, ldb, 0.0)
+    if dt == swg.BF16_F32OUT:
+        from helpers import check_f32
+        check_f32(to_f64(out[:, :N]), yhat, K, f"{tile_mode} {shape} f32 out")
+    else:
+        check_half(to_f64(out[:, :N]), yhat, f"{tile_mode} {shape} bf16 out")
