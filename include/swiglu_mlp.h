@@ -96,9 +96,16 @@ typedef enum {
  *                   the partial sums are reduced in a fixed order, so repeated
  *                   calls give bit-identical results.  The FP32 partials live
  *                   in a library-owned workspace, allocated (cudaMalloc) on
- *                   first use per (device, stream), grown when a larger split
- *                   needs it, and freed by swg_shutdown().  Two kernels are
+ *                   first use per (device, stream) and replaced by a larger
+ *                   one when a larger split needs it; replaced workspaces stay
+ *                   allocated (queued work or a captured graph may still use
+ *                   them) until swg_shutdown() frees them all.  Two kernels are
  *                   launched: the GEMM and a dependent reduction.
+ *   Graph capture   every call can be captured into a CUDA graph on a stream
+ *                   once the same call (or one needing at least as much
+ *                   workspace) has run on that stream; a call that would have
+ *                   to allocate while its stream is capturing returns
+ *                   SWG_ERR_UNSUPPORTED and launches nothing.
  */
 SWG_API int gemm(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
          const void *A, int64_t lda, const void *B, int64_t ldb, float beta,
@@ -273,8 +280,10 @@ SWG_API int swg_selftest_wait_timeout(int64_t limit_ns, void *stream);
 /* Number of kernels this library has launched in this process (all devices). */
 SWG_API uint64_t swg_launch_count(void);
 
-/* Frees every library-owned workspace on every device.  Safe to call twice;
- * later calls allocate afresh.  Call only when no library work is in flight. */
+/* Frees every library-owned workspace on every device, including replaced
+ * ones.  Safe to call twice; later calls allocate afresh.  Call only when no
+ * library work is in flight and no captured graph that used them will be
+ * replayed. */
 SWG_API void swg_shutdown(void);
 
 #ifdef __cplusplus

@@ -58,6 +58,10 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct Workspace {
     void *base = nullptr;   // split-K FP32 partials
     size_t bytes = 0;
+    // Smaller workspaces this one replaced.  Work already queued, or a CUDA
+    // graph captured earlier, may still address them, so they are freed only
+    // by swg_shutdown.
+    std::vector<void *> retired;
 };
 
 struct DeviceState {
@@ -96,16 +100,17 @@ int workspace(DeviceState *d, cudaStream_t s, size_t bytes, Workspace *&out)
     std::lock_guard<std::mutex> lk(g_mu);
     Workspace &w = d->ws[s];
     if (w.base == nullptr || w.bytes < bytes) {
-        if (w.base) {
-            if (cudaStreamSynchronize(s) != cudaSuccess) return SWG_ERR_CUDA;
-            cudaFree(w.base);
-            w = Workspace{};
-        }
+        // No allocation while the stream is being captured into a graph:
+        // the caller runs the call once before capturing.
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return SWG_ERR_CUDA;
+        if (cs != cudaStreamCaptureStatusNone) return SWG_ERR_UNSUPPORTED;
         void *p = nullptr;
         if (cudaMalloc(&p, bytes) != cudaSuccess) {
             cudaGetLastError();
             return SWG_ERR_NO_MEMORY;
         }
+        if (w.base) w.retired.push_back(w.base);
         w.base = p;
         w.bytes = bytes;
     }
@@ -964,8 +969,10 @@ void swg_shutdown(void)
         for (auto &kv : dv.second.ws) any = any || kv.second.base != nullptr;
         if (!any) continue;
         if (cudaSetDevice(dv.first) != cudaSuccess) continue;
-        for (auto &kv : dv.second.ws)
+        for (auto &kv : dv.second.ws) {
             if (kv.second.base) cudaFree(kv.second.base);
+            for (void *r : kv.second.retired) cudaFree(r);
+        }
         dv.second.ws.clear();
     }
     if (have_cur) cudaSetDevice(cur);
