@@ -277,6 +277,15 @@ SWG_API int swg_get_device_error(void *stream);
  */
 SWG_API int swg_selftest_wait_timeout(int64_t limit_ns, void *stream);
 
+/* Why the calling thread's most recent call returned SWG_ERR_CUDA: the CUDA
+ * runtime error code (cudaError_t), or 10000 + the driver's CUresult when
+ * encoding a tensor map failed; 0 if no call of this thread has failed that
+ * way.  Thread-local; a later successful call does not clear it. */
+SWG_API int swg_last_cuda_error(void);
+
+/* Name of a code returned by swg_last_cuda_error (static storage). */
+SWG_API const char *swg_cuda_error_name(int code);
+
 /* Number of kernels this library has launched in this process (all devices). */
 SWG_API uint64_t swg_launch_count(void);
 

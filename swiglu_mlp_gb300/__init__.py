@@ -37,9 +37,16 @@ _lib = None
 
 
 class SwgError(RuntimeError):
-    def __init__(self, status: int, where: str):
+    """A non-zero status from the C ABI; for SWG_ERR_CUDA the message also
+    names the CUDA error behind it (swg_last_cuda_error)."""
+
+    def __init__(self, status: int, where: str, cuda_error: int = 0, cuda_name: str = ""):
         self.status = int(status)
-        super().__init__(f"{where}: {STATUS.get(self.status, 'SWG_ERR_UNKNOWN')} ({self.status})")
+        self.cuda_error = int(cuda_error)
+        msg = f"{where}: {STATUS.get(self.status, 'SWG_ERR_UNKNOWN')} ({self.status})"
+        if self.cuda_error:
+            msg += f" [CUDA {self.cuda_error}: {cuda_name}]"
+        super().__init__(msg)
 
 
 def library_path() -> str:
@@ -86,6 +93,10 @@ def load():
         lib.swg_launch_count.restype = ctypes.c_uint64
         lib.swg_shutdown.argtypes = []
         lib.swg_shutdown.restype = None
+        lib.swg_last_cuda_error.argtypes = []
+        lib.swg_last_cuda_error.restype = i32
+        lib.swg_cuda_error_name.argtypes = [i32]
+        lib.swg_cuda_error_name.restype = ctypes.c_char_p
         _lib = lib
         return lib
 
@@ -111,7 +122,11 @@ def _stream(s):
 
 def _check(rc: int, where: str) -> int:
     if rc != 0:
-        raise SwgError(rc, where)
+        code, name = 0, ""
+        if rc == 4:                     # SWG_ERR_CUDA
+            code = load().swg_last_cuda_error()
+            name = load().swg_cuda_error_name(code).decode()
+        raise SwgError(rc, where, code, name)
     return rc
 
 

@@ -24,6 +24,43 @@ namespace {
 
 using swg::TileParams;
 
+// Why this thread's most recent call failed with SWG_ERR_CUDA: the CUDA
+// runtime error, or 10000 + the driver result of a failed tensor-map encoding.
+thread_local int t_last_cuda_error = 0;
+
+// Records the runtime's pending error of this thread (if any) and returns
+// SWG_ERR_CUDA.
+int cuda_fail()
+{
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) t_last_cuda_error = (int)e;
+    return SWG_ERR_CUDA;
+}
+
+// The calling thread's current device, with that device's primary context
+// made current to the thread (once per thread and device): the tensor-map
+// encoder is a driver call and fails without a current context, which a
+// thread that has made no runtime call yet does not have.
+int current_device(int &dev)
+{
+    thread_local int t_bound = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cuda_fail();
+    if (t_bound != dev) {
+        if (cudaSetDevice(dev) != cudaSuccess) return cuda_fail();
+        t_bound = dev;
+    }
+    return SWG_OK;
+}
+
+// SWG_OK if the launches just made left no error, else SWG_ERR_CUDA (recorded).
+int launch_status()
+{
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) return SWG_OK;
+    t_last_cuda_error = (int)e;
+    return SWG_ERR_CUDA;
+}
+
 std::atomic<uint64_t> g_launches{0};
 std::mutex g_mu;
 
@@ -77,14 +114,14 @@ std::map<int, DeviceState> g_dev;
 int device_state(DeviceState *&out)
 {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return SWG_ERR_CUDA;
+    if (int rc = current_device(dev)) return rc;
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceState &d = g_dev[dev];
     if (!d.ready) {
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return SWG_ERR_CUDA;
+            return cuda_fail();
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return SWG_ERR_CUDA;
+        if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return cuda_fail();
         d.err = static_cast<int *>(p);
         d.ready = true;
     }
@@ -103,7 +140,7 @@ int workspace(DeviceState *d, cudaStream_t s, size_t bytes, Workspace *&out)
         // No allocation while the stream is being captured into a graph:
         // the caller runs the call once before capturing.
         cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-        if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return SWG_ERR_CUDA;
+        if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return cuda_fail();
         if (cs != cudaStreamCaptureStatusNone) return SWG_ERR_UNSUPPORTED;
         void *p = nullptr;
         if (cudaMalloc(&p, bytes) != cudaSuccess) {
@@ -147,7 +184,10 @@ bool make_tmap(CUtensorMap *m, const void *ptr, bool bf16, int64_t inner, int64_
                int64_t ld, int box_outer)
 {
     EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
+    if (!fn) {
+        t_last_cuda_error = 10000 + (int)CUDA_ERROR_NOT_FOUND;
+        return false;
+    }
     cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
     cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
     cuuint32_t box[2] = {64u, (cuuint32_t)box_outer};
@@ -156,6 +196,7 @@ bool make_tmap(CUtensorMap *m, const void *ptr, bool bf16, int64_t inner, int64_
                     const_cast<void *>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) t_last_cuda_error = 10000 + (int)r;
     return r == CUDA_SUCCESS;
 }
 
@@ -165,7 +206,10 @@ bool make_tmap_u8(CUtensorMap *m, const void *ptr, int64_t inner, int64_t outer,
                   int box_outer)
 {
     EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
+    if (!fn) {
+        t_last_cuda_error = 10000 + (int)CUDA_ERROR_NOT_FOUND;
+        return false;
+    }
     cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
     cuuint64_t strides[1] = {(cuuint64_t)ld};
     cuuint32_t box[2] = {128u, (cuuint32_t)box_outer};
@@ -173,6 +217,7 @@ bool make_tmap_u8(CUtensorMap *m, const void *ptr, int64_t inner, int64_t outer,
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) t_last_cuda_error = 10000 + (int)r;
     return r == CUDA_SUCCESS;
 }
 
@@ -187,7 +232,10 @@ bool make_tmap_store(CUtensorMap *m, void *ptr, int esize, int64_t cols, int64_t
                      int64_t depth = 0, int64_t dstride = 0)
 {
     EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
+    if (!fn) {
+        t_last_cuda_error = 10000 + (int)CUDA_ERROR_NOT_FOUND;
+        return false;
+    }
     const cuuint32_t rank = depth > 0 ? 3u : 2u;
     cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)(depth > 0 ? depth : 1)};
     cuuint64_t strides[2] = {(cuuint64_t)(ld * esize), (cuuint64_t)(dstride * esize)};
@@ -197,6 +245,7 @@ bool make_tmap_store(CUtensorMap *m, void *ptr, int esize, int64_t cols, int64_t
                     rank, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) t_last_cuda_error = 10000 + (int)r;
     return r == CUDA_SUCCESS;
 }
 
@@ -350,7 +399,7 @@ int splitk_swapped(DeviceState *d, const TypeInfo &ti, int transA, int transB, i
                     : make_tmap(&ta, B, ti.in_bf16, K, N, ldb, swg::BM);
     ok = ok && (bT_mn ? make_tmap(&tb, A, ti.in_bf16, M, K, lda, 64)
                       : make_tmap(&tb, A, ti.in_bf16, K, M, lda, bn));
-    if (!ok) return SWG_ERR_CUDA;
+    if (!ok) return cuda_fail();
 
     const int64_t ld_ws = cdiv(N, 4) * 4;
     Workspace *w = nullptr;
@@ -377,7 +426,7 @@ int splitk_swapped(DeviceState *d, const TypeInfo &ti, int transA, int transB, i
     p.ld_ws = ld_ws;
     p.err = d->err;
     const int grid = (int)std::min<int64_t>(p.units, d->sms);
-    if (swg::launch_tc_splitk_t(bn, ta, tb, p, grid, s) != cudaSuccess) return SWG_ERR_CUDA;
+    if (swg::launch_tc_splitk_t(bn, ta, tb, p, grid, s) != cudaSuccess) return cuda_fail();
     g_launches++;
 
     TileParams r{};           // the reduction works in the output's frame
@@ -391,7 +440,7 @@ int splitk_swapped(DeviceState *d, const TypeInfo &ti, int transA, int transB, i
     r.out_kind = ti.out_kind;
     r.ws = p.ws;
     r.ld_ws = ld_ws;
-    if (swg::launch_splitk_reduce(r, d->sms, s) != cudaSuccess) return SWG_ERR_CUDA;
+    if (swg::launch_splitk_reduce(r, d->sms, s) != cudaSuccess) return cuda_fail();
     g_launches++;
     return SWG_OK;
 }
@@ -499,7 +548,7 @@ int swg_selftest_wait_timeout(int64_t limit_ns, void *stream)
     selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
         d->err, (unsigned long long)limit_ns);
     g_launches++;
-    return cudaGetLastError() == cudaSuccess ? SWG_OK : SWG_ERR_CUDA;
+    return launch_status();
 }
 
 // GEMM with e4m3 A and B (kind::f8f6f4): A stored M x K and B stored N x K,
@@ -528,7 +577,7 @@ static int gemm_fp8(int transA, int transB, int64_t M, int64_t N, int64_t K, flo
     if (K == 0) {
         scale_kernel<<<grid_for(M * N, d->sms), 256, 0, s>>>(C, ldc, (int)M, (int)N, beta, out_kind);
         g_launches++;
-        return cudaGetLastError() == cudaSuccess ? SWG_OK : SWG_ERR_CUDA;
+        return launch_status();
     }
     static const int cands[] = {256, 128};
     const TileChoice tc = choose_tiles(d, 4, M, N, cands, 2);
@@ -537,7 +586,7 @@ static int gemm_fp8(int transA, int transB, int64_t M, int64_t N, int64_t K, flo
     CUtensorMap ta, tb;
     if (!make_tmap_u8(&ta, A, K, M, lda, swg::BM) ||
         !make_tmap_u8(&tb, B, K, N, ldb, pair ? bn / 2 : bn))
-        return SWG_ERR_CUDA;
+        return cuda_fail();
     TileParams p{};
     p.M = (int)M;
     p.N = (int)N;
@@ -561,12 +610,12 @@ static int gemm_fp8(int transA, int transB, int64_t M, int64_t N, int64_t K, flo
     CUtensorMap td;
     if (beta == 0.0f && (N * (out_kind == swg::OUT_F32 ? 4 : 2)) % 16 == 0) {
         if (!make_tmap_store(&td, C, out_kind == swg::OUT_F32 ? 4 : 2, N, M, ldc))
-            return SWG_ERR_CUDA;
+            return cuda_fail();
         p.tma_store = 1;
     }
     if (swg::launch_tc_store_fp8(bn, pair, ta, tb, p, tc.units, s, p.tma_store ? &td : nullptr) !=
         cudaSuccess)
-        return SWG_ERR_CUDA;
+        return cuda_fail();
     g_launches++;
     return SWG_OK;
 }
@@ -604,7 +653,7 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
         scale_kernel<<<grid_for(M * N, d->sms), 256, 0, s>>>(C, ldc, (int)M, (int)N, beta,
                                                               ti.out_kind);
         g_launches++;
-        return cudaGetLastError() == cudaSuccess ? SWG_OK : SWG_ERR_CUDA;
+        return launch_status();
     }
 
     const int64_t kb = cdiv(K, swg::BK);
@@ -647,7 +696,7 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
                    : make_tmap(&ta, A, ti.in_bf16, K, M, lda, swg::BM);
     ok = ok && (b_mn ? make_tmap(&tb, B, ti.in_bf16, N, K, ldb, 64)
                      : make_tmap(&tb, B, ti.in_bf16, K, N, ldb, pair ? bn / 2 : bn));
-    if (!ok) return SWG_ERR_CUDA;
+    if (!ok) return cuda_fail();
 
     TileParams p{};
     p.M = (int)M;
@@ -687,7 +736,7 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
         // Each CTA's last partial tile leaves through shared memory and TMA
         // stores into ws viewed as [splits][M][ld_ws].
         CUtensorMap tw;
-        if (!make_tmap_store(&tw, p.ws, 4, N, M, ld_ws, splits, M * ld_ws)) return SWG_ERR_CUDA;
+        if (!make_tmap_store(&tw, p.ws, 4, N, M, ld_ws, splits, M * ld_ws)) return cuda_fail();
         p.tma_store = 1;
         e = swg::launch_tc_splitk(bn, pair, ta, tb, p, units, s, &tw);
         if (e == cudaSuccess) {
@@ -700,12 +749,12 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
         // a row only at 16-byte granules, so N must end on one.
         CUtensorMap td;
         if (beta == 0.0f && (N * ti.out_bytes) % 16 == 0) {
-            if (!make_tmap_store(&td, C, ti.out_bytes, N, M, ldc)) return SWG_ERR_CUDA;
+            if (!make_tmap_store(&td, C, ti.out_bytes, N, M, ldc)) return cuda_fail();
             p.tma_store = 1;
         }
         e = swg::launch_tc_store(bn, pair, ta, tb, p, tc.units, s, p.tma_store ? &td : nullptr);
     }
-    if (e != cudaSuccess) return SWG_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_fail();
     g_launches++;
     return SWG_OK;
 }
@@ -737,7 +786,7 @@ int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M, int64_t N
         scale_kernel<<<grid_for(M * N, d->sms), 256, 0, s>>>(Y, N, (int)M, (int)N, 0.0f,
                                                               swg::OUT_BF16);
         g_launches++;
-        return cudaGetLastError() == cudaSuccess ? SWG_OK : SWG_ERR_CUDA;
+        return launch_status();
     }
 
     const int64_t N2 = 2 * N;
@@ -747,7 +796,7 @@ int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M, int64_t N
     const bool pair = tc.pair;
     CUtensorMap ta, tb;
     if (!make_tmap(&ta, A, true, K, M, K, swg::BM) || !make_tmap(&tb, W_fused, true, N2, K, N2, 64))
-        return SWG_ERR_CUDA;
+        return cuda_fail();
 
     TileParams p{};
     p.M = (int)M;
@@ -775,12 +824,12 @@ int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M, int64_t N
     // 128-byte boxes: 64 output columns per tile, so bn >= 128).
     CUtensorMap ty;
     if (bn >= 128) {
-        if (!make_tmap_store(&ty, Y, 2, N, M, N)) return SWG_ERR_CUDA;
+        if (!make_tmap_store(&ty, Y, 2, N, M, N)) return cuda_fail();
         p.tma_store = 1;
     }
     if (swg::launch_tc_swiglu(bn, pair, ta, tb, p, tc.units, s, p.tma_store ? &ty : nullptr) !=
         cudaSuccess)
-        return SWG_ERR_CUDA;
+        return cuda_fail();
     g_launches++;
     return SWG_OK;
 }
@@ -804,7 +853,7 @@ int swiglu_mlp_fp8(const void *A, const void *W_fused_t, void *Y, int64_t M, int
         scale_kernel<<<grid_for(M * N, d->sms), 256, 0, s>>>(Y, N, (int)M, (int)N, 0.0f,
                                                               swg::OUT_BF16);
         g_launches++;
-        return cudaGetLastError() == cudaSuccess ? SWG_OK : SWG_ERR_CUDA;
+        return launch_status();
     }
     const int64_t N2 = 2 * N;
     static const int cands[] = {256, 128, 64};
@@ -814,7 +863,7 @@ int swiglu_mlp_fp8(const void *A, const void *W_fused_t, void *Y, int64_t M, int
     CUtensorMap ta, tb;
     if (!make_tmap_u8(&ta, A, K, M, K, swg::BM) ||
         !make_tmap_u8(&tb, W_fused_t, K, N2, K, pair ? bn / 2 : bn))
-        return SWG_ERR_CUDA;
+        return cuda_fail();
     TileParams p{};
     p.M = (int)M;
     p.N = (int)N2;
@@ -837,12 +886,12 @@ int swiglu_mlp_fp8(const void *A, const void *W_fused_t, void *Y, int64_t M, int
     p.err = d->err;
     CUtensorMap ty;
     if (bn >= 128) {
-        if (!make_tmap_store(&ty, Y, 2, N, M, N)) return SWG_ERR_CUDA;
+        if (!make_tmap_store(&ty, Y, 2, N, M, N)) return cuda_fail();
         p.tma_store = 1;
     }
     if (swg::launch_tc_swiglu_fp8(bn, pair, ta, tb, p, tc.units, s, p.tma_store ? &ty : nullptr) !=
         cudaSuccess)
-        return SWG_ERR_CUDA;
+        return cuda_fail();
     g_launches++;
     return SWG_OK;
 }
@@ -866,7 +915,7 @@ int swiglu_mlp_dual(const void *A, const void *W1, const void *W2, void *Y, int6
         scale_kernel<<<grid_for(M * N, d->sms), 256, 0, s>>>(Y, N, (int)M, (int)N, 0.0f,
                                                               swg::OUT_BF16);
         g_launches++;
-        return cudaGetLastError() == cudaSuccess ? SWG_OK : SWG_ERR_CUDA;
+        return launch_status();
     }
 
     // Tiles are chosen in the 2N-wide Gate|Up column space, as for swiglu_mlp.
@@ -877,7 +926,7 @@ int swiglu_mlp_dual(const void *A, const void *W1, const void *W2, void *Y, int6
     CUtensorMap ta, tw1, tw2;
     if (!make_tmap(&ta, A, true, K, M, K, swg::BM) || !make_tmap(&tw1, W1, true, N, K, N, 64) ||
         !make_tmap(&tw2, W2, true, N, K, N, 64))
-        return SWG_ERR_CUDA;
+        return cuda_fail();
 
     TileParams p{};
     p.M = (int)M;
@@ -902,7 +951,7 @@ int swiglu_mlp_dual(const void *A, const void *W1, const void *W2, void *Y, int6
     p.out_kind = swg::OUT_BF16;
     p.err = d->err;
     if (swg::launch_tc_swiglu_dual(bn, pair, ta, tw1, tw2, p, tc.units, s) != cudaSuccess)
-        return SWG_ERR_CUDA;
+        return cuda_fail();
     g_launches++;
     return SWG_OK;
 }
@@ -942,21 +991,30 @@ int swiglu_interleave(const void *W1, const void *W2, void *W_fused, int64_t K, 
         static_cast<const uint16_t *>(W1), static_cast<const uint16_t *>(W2),
         static_cast<uint16_t *>(W_fused), K, N);
     g_launches++;
-    return cudaGetLastError() == cudaSuccess ? SWG_OK : SWG_ERR_CUDA;
+    return launch_status();
 }
 
 int swg_get_device_error(void *stream)
 {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaStreamSynchronize(s) != cudaSuccess) return SWG_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return cuda_fail();
     int v = 0;
-    if (cudaMemcpyFromSymbol(&v, g_err_word, sizeof(int)) != cudaSuccess) return SWG_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(&v, g_err_word, sizeof(int)) != cudaSuccess) return cuda_fail();
     if (v != 0) {
         const int zero = 0;
-        if (cudaMemcpyToSymbol(g_err_word, &zero, sizeof(int)) != cudaSuccess) return SWG_ERR_CUDA;
+        if (cudaMemcpyToSymbol(g_err_word, &zero, sizeof(int)) != cudaSuccess) return cuda_fail();
         return v;
     }
     return SWG_OK;
+}
+
+int swg_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char *swg_cuda_error_name(int code)
+{
+    if (code == 0) return "none";
+    if (code >= 10000) return "tensor-map encoding failed (driver result = code - 10000)";
+    return cudaGetErrorName(static_cast<cudaError_t>(code));
 }
 
 void swg_shutdown(void)
@@ -1011,16 +1069,16 @@ int g_noalloc_sms[kNoallocMaxDevices];
 // are host-side stand-ins, so kernels must be given these addresses instead.
 int noalloc_setup(int &dev)
 {
-    if (cudaGetDevice(&dev) != cudaSuccess) return SWG_ERR_CUDA;
+    if (int rc = current_device(dev)) return rc;
     if (dev < 0 || dev >= kNoallocMaxDevices) return SWG_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     if (g_noalloc_ready[dev]) return SWG_OK;
     void *scratch = nullptr, *err = nullptr;
-    if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess) return SWG_ERR_CUDA;
-    if (cudaGetSymbolAddress(&err, g_err_word) != cudaSuccess) return SWG_ERR_CUDA;
+    if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess) return cuda_fail();
+    if (cudaGetSymbolAddress(&err, g_err_word) != cudaSuccess) return cuda_fail();
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return SWG_ERR_CUDA;
+        return cuda_fail();
     g_noalloc_ptr[dev] = static_cast<float *>(scratch);
     g_noalloc_err[dev] = static_cast<int *>(err);
     g_noalloc_sms[dev] = sms;
@@ -1080,7 +1138,7 @@ int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N, int64_t K,
         scale_kernel<<<grid_for(M * N, sms), 256, 0, s>>>(C, ldc, (int)M, (int)N, beta,
                                                            ti.out_kind);
         g_launches++;
-        return cudaGetLastError() == cudaSuccess ? SWG_OK : SWG_ERR_CUDA;
+        return launch_status();
     }
 
     const int bn = 256;
@@ -1091,7 +1149,7 @@ int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N, int64_t K,
                    : make_tmap(&ta, A, ti.in_bf16, K, M, lda, swg::BM);
     ok = ok && (b_mn ? make_tmap(&tb, B, ti.in_bf16, N, K, ldb, 64)
                      : make_tmap(&tb, B, ti.in_bf16, K, N, ldb, bn));
-    if (!ok) return SWG_ERR_CUDA;
+    if (!ok) return cuda_fail();
 
     TileParams p{};
     p.M = (int)M;
@@ -1118,9 +1176,9 @@ int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N, int64_t K,
     p.ld_ws = ld_ws;
     p.err = g_noalloc_err[dev];
     const int grid = (int)std::min<int64_t>(p.units, sms);
-    if (swg::launch_tc_splitk(bn, false, ta, tb, p, grid, s) != cudaSuccess) return SWG_ERR_CUDA;
+    if (swg::launch_tc_splitk(bn, false, ta, tb, p, grid, s) != cudaSuccess) return cuda_fail();
     g_launches++;
-    if (swg::launch_splitk_reduce(p, sms, s) != cudaSuccess) return SWG_ERR_CUDA;
+    if (swg::launch_splitk_reduce(p, sms, s) != cudaSuccess) return cuda_fail();
     g_launches++;
     return SWG_OK;
 }

@@ -93,6 +93,22 @@ def _has_gpu():
 @pytest.mark.skipif(_has_gpu(), reason="checks the no-GPU path")
 def test_valid_call_without_gpu_reports_cuda_error(lib):
     assert g(lib) == CUDA_ERR
+    # The runtime error behind it is recorded for this thread and named.
+    code = lib.swg_last_cuda_error()
+    assert code not in (0, 10000)
+    name = lib.swg_cuda_error_name(code).decode()
+    assert name.startswith("cuda") and "Error" in name
+    assert lib.swg_cuda_error_name(0).decode() == "none"
+
+
+@pytest.mark.skipif(_has_gpu(), reason="checks the no-GPU path")
+def test_binding_error_names_the_cuda_error():
+    import swiglu_mlp_gb300 as swg
+    with pytest.raises(swg.SwgError) as info:
+        swg.gemm(0, 0, 128, 128, 64, 1.0, P, 64, P, 128, 0.0, P, 128, swg.BF16)
+    assert info.value.status == CUDA_ERR
+    assert info.value.cuda_error != 0
+    assert "[CUDA" in str(info.value)
 
 
 def test_swiglu_validation(lib):
