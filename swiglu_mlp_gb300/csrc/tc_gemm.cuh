@@ -23,7 +23,18 @@
 //                                 sums the partials in split order and stores
 //                                 alpha*sum + beta*C.
 // The double TMEM accumulator lets the epilogue of tile t overlap the main
-// loop of tile t+1.
+// loop of tile t+1.  A CTA's last tile, when every pipeline stage has been
+// consumed, is written into the stage area in the 128-byte swizzle layout and
+// stored with TMA bulk stores (whole lines, clipped at the matrix edges).
+//
+// CTA pairs (PAIR): clusters of two CTAs share one cta_group::2 MMA of
+// 256 x BN; each CTA loads its 128 rows of A and half of B, and receives its
+// own 128 accumulator rows.  EPI_SPLITK_T and EPI_SWIGLU_DUAL are described
+// at the EpiKind enumeration.
+//
+// Programmatic dependent launch: the kernel lets the next kernel on the stream
+// be scheduled as soon as it starts, and touches global memory only after
+// griddepcontrol.wait, so consecutive calls overlap set-up and tail safely.
 //
 // Every barrier wait is bounded (about two seconds): on expiry the thread
 // records SWG_ERR_DEVICE_TIMEOUT in the error word, raises a CTA-wide abort
