@@ -57,7 +57,10 @@ typedef enum { SWG_OP_N = 0, SWG_OP_T = 1 } swg_op;
  * Coração Matemático", §12.4); per-tensor dequantisation scales are applied by
  * folding them into alpha (alpha * scale_A * scale_B).  They require
  * op(A) = A and op(B) = B^T, i.e. A stored M x K and B stored N x K (both
- * K-contiguous), lda and ldb multiples of 16, and no split-K; other
+ * K-contiguous), and lda and ldb multiples of 16.  Split-K exists for them
+ * only with M <= 64 (few rows, e.g. decode): such calls run the transposed
+ * product with the K loop split, automatically or with split_k > 1, and
+ * reduce the partials in split order; split_k > 1 with M > 64 and other op
  * combinations return SWG_ERR_UNSUPPORTED. */
 typedef enum {
     SWG_F16_F32OUT = 0,   /* A, B binary16;  C, D binary32 */

@@ -373,11 +373,16 @@ TileChoice choose_tiles(DeviceState *d, int kind, int64_t M, int64_t N, const in
 // D^T = op(B)^T op(A)^T with op(B)^T (N x K) as its 128-row operand and
 // op(A)^T as its BN-column operand, writes transposed FP32 partials
 // ws[split][m][n], and the usual in-order reduction forms D.
+// With fp8 (e4m3 A and B; op(A) = A and op(B) = B^T, both K-major) the
+// K blocks are 128 elements, the same 128-byte rows, and the MMA is
+// kind::f8f6f4; everything else is shared.
 int splitk_swapped(DeviceState *d, const TypeInfo &ti, int transA, int transB, int64_t M,
                    int64_t N, int64_t K, float alpha, const void *A, int64_t lda, const void *B,
-                   int64_t ldb, float beta, void *C, int64_t ldc, int split_k, cudaStream_t s)
+                   int64_t ldb, float beta, void *C, int64_t ldc, int split_k, cudaStream_t s,
+                   bool fp8 = false)
 {
-    const int64_t kb = cdiv(K, swg::BK);
+    const int bk = fp8 ? 128 : swg::BK;
+    const int64_t kb = cdiv(K, bk);
     // op(A)^T is the kernel's B operand: K-major when A is stored M x K
     // (op N), MN-major (one 64-wide atom) when stored K x M (op T).
     const bool bT_mn = transA == SWG_OP_T;
@@ -395,10 +400,15 @@ int splitk_swapped(DeviceState *d, const TypeInfo &ti, int transA, int transB, i
     // op(B)^T is the kernel's A operand: MN-major when B is stored K x N (op N).
     const bool aT_mn = transB == SWG_OP_N;
     CUtensorMap ta, tb;
-    bool ok = aT_mn ? make_tmap(&ta, B, ti.in_bf16, N, K, ldb, 64)
-                    : make_tmap(&ta, B, ti.in_bf16, K, N, ldb, swg::BM);
-    ok = ok && (bT_mn ? make_tmap(&tb, A, ti.in_bf16, M, K, lda, 64)
-                      : make_tmap(&tb, A, ti.in_bf16, K, M, lda, bn));
+    bool ok;
+    if (fp8) {
+        ok = make_tmap_u8(&ta, B, K, N, ldb, swg::BM) && make_tmap_u8(&tb, A, K, M, lda, bn);
+    } else {
+        ok = aT_mn ? make_tmap(&ta, B, ti.in_bf16, N, K, ldb, 64)
+                   : make_tmap(&ta, B, ti.in_bf16, K, N, ldb, swg::BM);
+        ok = ok && (bT_mn ? make_tmap(&tb, A, ti.in_bf16, M, K, lda, 64)
+                          : make_tmap(&tb, A, ti.in_bf16, K, M, lda, bn));
+    }
     if (!ok) return cuda_fail();
 
     const int64_t ld_ws = cdiv(N, 4) * 4;
@@ -413,20 +423,22 @@ int splitk_swapped(DeviceState *d, const TypeInfo &ti, int transA, int transB, i
     p.m_blocks = (int)cdiv(N, swg::BM);
     p.n_blocks = (int)cdiv(M, bn);
     p.k_blocks = (int)kb;
-    p.bk = swg::BK;
+    p.bk = bk;
     p.tiles = p.m_blocks * p.n_blocks;
     p.splits = splits;
     p.kb_per_split = kbps;
     p.units = p.tiles * splits;
     p.group_m = 16;
-    p.idesc = make_idesc(ti.in_bf16, aT_mn, bT_mn, swg::BM, bn);
+    p.idesc = make_idesc(fp8 ? false : ti.in_bf16, aT_mn, bT_mn, swg::BM, bn);
     p.a_mn_major = aT_mn;
     p.b_mn_major = bT_mn;
     p.ws = static_cast<float *>(w->base);
     p.ld_ws = ld_ws;
     p.err = d->err;
     const int grid = (int)std::min<int64_t>(p.units, d->sms);
-    if (swg::launch_tc_splitk_t(bn, ta, tb, p, grid, s) != cudaSuccess) return cuda_fail();
+    if ((fp8 ? swg::launch_tc_splitk_t_fp8(bn, ta, tb, p, grid, s)
+             : swg::launch_tc_splitk_t(bn, ta, tb, p, grid, s)) != cudaSuccess)
+        return cuda_fail();
     g_launches++;
 
     TileParams r{};           // the reduction works in the output's frame
@@ -560,7 +572,8 @@ static int gemm_fp8(int transA, int transB, int64_t M, int64_t N, int64_t K, flo
     if ((transA != SWG_OP_N && transA != SWG_OP_T) || (transB != SWG_OP_N && transB != SWG_OP_T))
         return SWG_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0 || split_k < 0) return SWG_ERR_INVALID_ARG;
-    if (transA != SWG_OP_N || transB != SWG_OP_T || split_k > 1) return SWG_ERR_UNSUPPORTED;
+    if (transA != SWG_OP_N || transB != SWG_OP_T) return SWG_ERR_UNSUPPORTED;
+    if (split_k > 1 && M > 64) return SWG_ERR_UNSUPPORTED;   // FP8 split-K: few rows only
     if (M == 0 || N == 0) return SWG_OK;
     if (C == nullptr || ldc < N) return SWG_ERR_INVALID_ARG;
     if (K > 0 && (A == nullptr || B == nullptr || lda < K || ldb < K)) return SWG_ERR_INVALID_ARG;
@@ -578,6 +591,17 @@ static int gemm_fp8(int transA, int transB, int64_t M, int64_t N, int64_t K, flo
         scale_kernel<<<grid_for(M * N, d->sms), 256, 0, s>>>(C, ldc, (int)M, (int)N, beta, out_kind);
         g_launches++;
         return launch_status();
+    }
+    // Few rows (decode): the transposed product with the K loop split, as
+    // for 16-bit inputs, unless the caller asked for no split.
+    if (M <= 64 && split_k != 1) {
+        const int64_t kb = cdiv(K, 128);
+        const int64_t swapped_tiles = cdiv(N, swg::BM);
+        if (split_k > 1 || (kb >= 8 && swapped_tiles * 2 <= d->sms)) {
+            TypeInfo ti{false, out_kind, out_bytes};
+            return splitk_swapped(d, ti, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta,
+                                  C, ldc, split_k, s, true);
+        }
     }
     static const int cands[] = {256, 128};
     const TileChoice tc = choose_tiles(d, 4, M, N, cands, 2);

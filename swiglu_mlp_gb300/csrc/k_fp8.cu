@@ -1,6 +1,7 @@
 // k_fp8.cu — instantiations of the tcgen05 GEMM with 8-bit (e4m3) operands
-// and kind::f8f6f4 MMAs: the plain GEMM epilogue and the interleaved SwiGLU
-// epilogue.  Per-tensor dequantisation scales arrive folded into alpha.
+// and kind::f8f6f4 MMAs: the plain GEMM epilogue, the interleaved SwiGLU
+// epilogue, and the swapped-operand split-K partials for few rows (decode).
+// Per-tensor dequantisation scales arrive folded into alpha.
 // Quantised operands: "GEMM o Coração Matemático", §12.4; the SwiGLU page
 // ("Sobreposição de Ativação ...", Definição do Problema) notes that FP8 /
 // INT4 raise the relative cost of the memory-bound activation step.
@@ -38,6 +39,17 @@ cudaError_t launch_tc_swiglu_fp8(int bn, bool pair, const CUtensorMap &ta, const
     case 64: return launch_tc_impl<64, EPI_SWIGLU, false, true>(ta, tb, p, units, s, tout);
     case 128: return launch_tc_impl<128, EPI_SWIGLU, false, true>(ta, tb, p, units, s, tout);
     case 256: return launch_tc_impl<256, EPI_SWIGLU, false, true>(ta, tb, p, units, s, tout);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_tc_splitk_t_fp8(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
+                                   const TileParams &p, int units, cudaStream_t s)
+{
+    switch (bn) {
+    case 16: return launch_tc_impl<16, EPI_SPLITK_T, false, true>(ta, tb, p, units, s);
+    case 32: return launch_tc_impl<32, EPI_SPLITK_T, false, true>(ta, tb, p, units, s);
+    case 64: return launch_tc_impl<64, EPI_SPLITK_T, false, true>(ta, tb, p, units, s);
     default: return cudaErrorInvalidValue;
     }
 }

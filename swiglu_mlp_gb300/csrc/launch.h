@@ -44,6 +44,9 @@ cudaError_t launch_tc_swiglu_fp8(int bn, bool pair, const CUtensorMap &ta, const
                                  const TileParams &p, int units, cudaStream_t s,
                                  const CUtensorMap *tout = nullptr);
 int max_active_pairs_fp8(int kind, int bn, int sms);   // kind 0 = GEMM, 1 = SwiGLU
+// Swapped-operand split-K with e4m3 operands (both K-major), BN = 16, 32, 64.
+cudaError_t launch_tc_splitk_t_fp8(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
+                                   const TileParams &p, int units, cudaStream_t s);
 
 // Resident CTA pairs for the pair variants (0 if unknown or not instantiated).
 int max_active_pairs_store(int bn, int sms);

@@ -77,10 +77,11 @@ def test_fp8_square_8192_sampled():
 def test_fp8_layout_rules():
     P = 0x10000
     lib = swg.load()
-    # only op(A) = A, op(B) = B^T; no split-K
+    # only op(A) = A, op(B) = B^T; split-K only for M <= 64 (rejected before
+    # any CUDA call, so the fake pointers are never used)
     assert lib.gemm_ex(0, 0, 16, 16, 16, 1.0, P, 16, P, 16, 0.0, P, 16, swg.E4M3_BF16OUT, 0, None) == 3
     assert lib.gemm_ex(1, 1, 16, 16, 16, 1.0, P, 16, P, 16, 0.0, P, 16, swg.E4M3_BF16OUT, 0, None) == 3
-    assert lib.gemm_ex(0, 1, 16, 16, 16, 1.0, P, 16, P, 16, 0.0, P, 16, swg.E4M3_BF16OUT, 4, None) == 3
+    assert lib.gemm_ex(0, 1, 65, 16, 16, 1.0, P, 16, P, 16, 0.0, P, 16, swg.E4M3_BF16OUT, 4, None) == 3
     assert lib.gemm_ex(0, 1, 16, 16, 24, 1.0, P, 24, P, 24, 0.0, P, 16, swg.E4M3_BF16OUT, 0, None) == 2
 
 
@@ -110,3 +111,45 @@ def test_fp8_swiglu_8b_sampled():
     rows = [0, 255, 256, M - 1]
     yhat = oracle.swiglu_typed(A, W1, W2, M, N, K, in_type="e4m3", scale=sw, rows=rows)
     check_half(to_f64(Y)[rows], yhat, "fp8 swiglu 8B")
+
+
+@pytest.mark.parametrize("M", [1, 7, 16, 33, 64])
+@pytest.mark.parametrize("split_k", [0, 3])
+def test_fp8_few_rows_split_k(M, split_k):
+    """Few rows (decode): the transposed product with the K loop split and the
+    partials reduced in split order; ragged N, beta != 0, bf16 output."""
+    N, K = 520, 4096
+    g = synth.generator(1300 + M + split_k)
+    A = _e4m3((M, K), g)
+    Bt = _e4m3((N, K), g)
+    C = synth.normal((M, N), g)
+    ldc = 528
+    Cp = torch.zeros((M, ldc), dtype=torch.bfloat16)
+    Cp[:, :N] = C
+    Cd = Cp.cuda()
+    swg.gemm_ex(0, 1, M, N, K, 1.0 / 32, A.cuda(), K, Bt.cuda(), K, 0.5, Cd, ldc,
+                swg.E4M3_BF16OUT, split_k)
+    assert swg.get_device_error() == 0
+    out = Cd.cpu()
+    assert torch.all(out[:, N:] == 0)
+    yhat = oracle.gemm(0, 1, M, N, K, 1.0 / 32, A, K, Bt, K, 0.5, C, N, in_type="e4m3")
+    check_half(to_f64(out[:, :N]), yhat, f"fp8 few rows M={M} split={split_k}")
+
+
+def test_fp8_decode_gemv_f32_out_deterministic():
+    """M = 1 against a 4096 x 4096 e4m3 weight, FP32 output: repeated calls give
+    identical bits (fixed reduction order) and match the oracle."""
+    M, N, K = 1, 4096, 4096
+    g = synth.generator(1310)
+    A = _e4m3((M, K), g)
+    Bt = _e4m3((N, K), g, std=0.5)
+    Ad, Bd = A.cuda(), Bt.cuda()
+    outs = []
+    for _ in range(3):
+        D = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        swg.gemm(0, 1, M, N, K, 0.25, Ad, K, Bd, K, 0.0, D, N, swg.E4M3_F32OUT)
+        outs.append(D.cpu())
+    assert swg.get_device_error() == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    yhat = oracle.gemm(0, 1, M, N, K, 0.25, A, K, Bt, K, 0.0, in_type="e4m3", c_type="f32")
+    check_f32(to_f64(outs[0]), yhat, K, "fp8 decode f32")
