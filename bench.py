@@ -446,6 +446,8 @@ def component_cases():
     cases += [("mlp_small_M2048", "mlp", 2048, 896, 4864), ("mlp_8b_M2048", "mlp", 2048, 4096, 14336)]
     cases += [("swiglu_dual_small_M2048", "dual", 2048, 896, 4864),
               ("swiglu_dual_8b_M2048", "dual", 2048, 4096, 14336)]
+    cases += [("fp8_decode_gemv_M1", "fp8gemm", 1, 4096, 4096),
+              ("fp8_skinny_splitk_M16", "fp8gemm", 16, 16384, 4096)]
     cases += [("fp8_gemm_8192", "fp8gemm", 8192, 8192, 8192),
               ("fp8_swiglu_8b_M2048", "fp8swiglu", 2048, 4096, 14336),
               ("fp8_swiglu_8b_M8192", "fp8swiglu", 8192, 4096, 14336)]
@@ -624,7 +626,7 @@ def run_components(args, dev, stream):
         if hot_ms is not None:
             entry["hot_l2"] = {"us_per_call": round(hot_ms * 1e3, 2),
                                "roofline_frac": round(max(t_tensor, t_hbm) / (hot_ms / 1e3), 4)}
-        if kind in ("skinny", "gemv"):
+        if kind in ("skinny", "gemv") or name.startswith(("fp8_decode", "fp8_skinny")):
             entry["hbm_frac"] = round(byts / med / 1e6 / bw, 4)
         res[name] = entry
         torch.cuda.empty_cache()
