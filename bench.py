@@ -630,9 +630,39 @@ def run_components(args, dev, stream):
             entry["hbm_frac"] = round(byts / med / 1e6 / bw, 4)
         res[name] = entry
         torch.cuda.empty_cache()
+    res["launch_floor"] = launch_floor(args, dev, stream, flush)
     if swg.get_device_error(stream) != 0:
         raise RuntimeError("device error word set during the component timings")
     return res
+
+
+def launch_floor(args, dev, stream, flush):
+    """Context for the isolated figures: what the same protocol (L2 flush,
+    then an event pair around the call) measures for an empty event pair and
+    for a one-element fill kernel.  Every isolated time above includes this
+    fixed cost of recording events and launching one kernel."""
+    import torch
+
+    x = torch.zeros(1, dtype=torch.float32, device=dev)
+
+    def median_us(fn):
+        for _ in range(3):
+            fn()
+        times = []
+        for _ in range(args.component_reps):
+            l2_flush(flush)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            times.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        return round(statistics.median(a.elapsed_time(b) for a, b in times) * 1e3, 2)
+
+    return {"empty_event_pair_us": median_us(lambda: None),
+            "one_element_fill_us": median_us(lambda: x.fill_(1.0)),
+            "note": "same isolation protocol as the components; not a kernel of this library"}
 
 
 def run_profile_case(args):
