@@ -438,7 +438,9 @@ def time_reps(fn, reps, dev, stream, flush_buf):
 
 
 def component_cases():
-    """(name, kind, M, K, N) of the fused-SwiGLU and skinny split-K workloads."""
+    """(name, kind, M, K, N) of the other workloads: fused SwiGLU, skinny split-K,
+    decode, the full MLP, the square bf16 GEMM at 4096 (all op combinations),
+    the 256^3 FP16-in / FP32-out GEMM with alpha = 1.5, beta = 0.5, and FP8."""
     cases = [(f"swiglu_small_M{m}", "swiglu", m, 896, 4864) for m in (128, 512, 2048)]
     cases += [(f"swiglu_8b_M{m}", "swiglu", m, 4096, 14336) for m in (512, 2048, 8192)]
     cases += [(f"skinny_splitk_M{m}", "skinny", m, 16384, 4096) for m in (16, 32, 64)]
@@ -448,6 +450,8 @@ def component_cases():
               ("swiglu_dual_8b_M2048", "dual", 2048, 4096, 14336)]
     cases += [("fp8_decode_gemv_M1", "fp8gemm", 1, 4096, 4096),
               ("fp8_skinny_splitk_M16", "fp8gemm", 16, 16384, 4096)]
+    cases += [(f"gemm_4096_{t}", f"gemm_{t}", 4096, 4096, 4096) for t in ("nn", "nt", "tn", "tt")]
+    cases += [("gemm_f16_f32out_256", "gemm_f16_small", 256, 256, 256)]
     cases += [("fp8_gemm_8192", "fp8gemm", 8192, 8192, 8192),
               ("fp8_swiglu_8b_M2048", "fp8swiglu", 2048, 4096, 14336),
               ("fp8_swiglu_8b_M8192", "fp8swiglu", 8192, 4096, 14336)]
@@ -535,6 +539,18 @@ def build_case(kind, M, K, N, dev, stream):
         def fn():
             swg.gemm(0, 0, M, N, K, 1.0, A, K, B, N, 0.0, D, N, swg.BF16, stream=stream)
         return fn, None, 2.0 * M * N * K, (M * K + K * N + M * N) * 2
+    if kind == "gemm_f16_small":
+        # D = 1.5 A B + 0.5 C: fp16 A, B ~ U(-1, 1), fp32 C ~ U(-1, 1), seed 0
+        A, B, C = synth.gemm_f16_small(seed=0, M=M, N=N, K=K)
+        Ad, Bd, C0 = A.to(dev), B.to(dev), C.to(dev)
+        Cd = C0.clone()
+
+        def fn():
+            swg.gemm(0, 0, M, N, K, 1.5, Ad, K, Bd, N, 0.5, Cd, N, swg.F16_F32OUT, stream=stream)
+
+        def reset():
+            Cd.copy_(C0)
+        return fn, reset, 2.0 * M * N * K, (M * K + K * N) * 2 + 2 * M * N * 4
     if kind.startswith("gemm"):
         tA, tB = {"gemm_nn": (0, 0), "gemm_nt": (0, 1), "gemm_tn": (1, 0),
                   "gemm_tt": (1, 1)}[kind]
