@@ -109,12 +109,28 @@ def _ptr(x):
     return x.data_ptr()
 
 
+_raw_stream = None    # torch's accessor of the current raw stream handle, once found
+
+
+def _current_stream():
+    """The calling thread's current torch stream on the current device as a
+    raw handle (None without CUDA).  torch's raw accessor is used when it has
+    one: building a torch.cuda.Stream object per call costs several
+    microseconds of host time."""
+    global _raw_stream
+    import torch
+    if _raw_stream is None:
+        if not torch.cuda.is_available():
+            return None
+        get = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        _raw_stream = get if get is not None else (
+            lambda dev: torch.cuda.current_stream(dev).cuda_stream)
+    return _raw_stream(torch.cuda.current_device())
+
+
 def _stream(s):
     if s is None:
-        import torch
-        if torch.cuda.is_available():
-            return torch.cuda.current_stream().cuda_stream
-        return None
+        return _current_stream()
     if isinstance(s, int):
         return s
     return s.cuda_stream

@@ -687,6 +687,20 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
     // shape can keep resident ("为什么 GEMM 是 CUDA 的必修课", 关键技术 item 5).
     static const int cands[] = {256, 128};
     TileChoice tc = choose_tiles(d, 0, M, N, cands, 2);
+    // A small output with a short K (no split below): when its tiles would
+    // occupy at most a quarter of the SMs, 128 x 64 single-CTA tiles spread
+    // the main loop and the epilogue's C reads and D writes over more SMs
+    // (a 256^3 GEMM: 8 CTAs instead of one CTA pair).
+    int forced_bn = 0;
+    if (kb < 8 && forced_tile_mode(&forced_bn) == 0) {
+        const int64_t sms_used = tc.pair ? 2 * (int64_t)tc.units : (int64_t)tc.units;
+        const int64_t narrow = mblk * cdiv(N, 64);
+        if (sms_used * 4 <= d->sms && narrow > sms_used) {
+            tc.pair = false;
+            tc.bn = 64;
+            tc.units = (int)std::min<int64_t>(narrow, d->sms);
+        }
+    }
     const bool pair = tc.pair;
     const int bn = tc.bn;
     const int64_t tiles = (pair ? cdiv(M, 2 * swg::BM) : mblk) * cdiv(N, bn);

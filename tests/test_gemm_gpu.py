@@ -196,3 +196,18 @@ def test_square_bf16_sampled(size, tA, tB):
     rows = sorted({0, 127, 128, M - 1, *rng.integers(0, M, 4).tolist()})
     yhat = oracle.gemm(tA, tB, M, N, K, 1.0, A, A.shape[1], B, B.shape[1], 0.0, rows=rows)
     check_half(to_f64(D)[rows], yhat, f"{size}^3 tA={tA} tB={tB}")
+
+
+def test_default_stream_is_torch_current_stream():
+    """Calls without a stream go on torch's current stream of the current
+    device, also inside a `torch.cuda.stream` context."""
+    s = torch.cuda.Stream()
+    assert swg._stream(None) == torch.cuda.current_stream().cuda_stream
+    with torch.cuda.stream(s):
+        assert swg._stream(None) == s.cuda_stream
+        A = torch.ones((128, 64), dtype=torch.bfloat16, device="cuda")
+        D = torch.empty((128, 128), dtype=torch.bfloat16, device="cuda")
+        swg.gemm(0, 0, 128, 128, 64, 1.0, A, 64, A.t().contiguous(), 128, 0.0, D, 128, swg.BF16)
+    s.synchronize()
+    assert torch.all(D == 64.0)
+    assert swg._stream(None) == torch.cuda.current_stream().cuda_stream
