@@ -155,6 +155,14 @@ int workspace(DeviceState *d, cudaStream_t s, size_t bytes, Workspace *&out)
     return SWG_OK;
 }
 
+// Tuning and testing: SWG_MN_3D=0 keeps two 2-D boxes per MN-major operand
+// and stage instead of one 3-D box.
+bool mn_3d_disabled()
+{
+    const char *v = std::getenv("SWG_MN_3D");
+    return v && v[0] == '0';
+}
+
 // ----------------------------------------------------------------- tensor maps
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -197,6 +205,29 @@ bool make_tmap(CUtensorMap *m, const void *ptr, bool bf16, int64_t inner, int64_
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) t_last_cuda_error = 10000 + (int)r;
+    return r == CUDA_SUCCESS;
+}
+
+// MN-major operand whose MN extent `mn` is a multiple of 64, viewed in 3-D
+// as (64 contiguous MN elements, K rows at the row stride, mn / 64 atoms 128
+// bytes apart): one box of {64, 64, atoms} fills `atoms` consecutive 8 KB
+// swizzle atoms of a stage, the layout two 2-D {64, 64} boxes give, with one
+// TMA instruction.  Rows past K read as zero; with mn a multiple of 64 no box
+// reaches past a row's last element.  Returns false (and the caller keeps the
+// 2-D map) if the driver declines the encoding.
+bool make_tmap_mn3(CUtensorMap *m, const void *ptr, bool bf16, int64_t mn, int64_t k, int64_t ld,
+                   int atoms)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || mn % 64 != 0 || mn_3d_disabled()) return false;
+    cuuint64_t dims[3] = {64u, (cuuint64_t)k, (cuuint64_t)(mn / 64)};
+    cuuint64_t strides[2] = {(cuuint64_t)ld * 2, 128u};
+    cuuint32_t box[3] = {64u, 64u, (cuuint32_t)atoms};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                    const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -410,6 +441,12 @@ int splitk_swapped(DeviceState *d, const TypeInfo &ti, int transA, int transB, i
                           : make_tmap(&tb, A, ti.in_bf16, K, M, lda, bn));
     }
     if (!ok) return cuda_fail();
+    // MN-major operands: one 3-D box per stage where the extent allows.
+    CUtensorMap t3;
+    const bool a3 = !fp8 && aT_mn && make_tmap_mn3(&t3, B, ti.in_bf16, N, K, ldb, swg::BM / 64);
+    if (a3) ta = t3;
+    const bool b3 = !fp8 && bT_mn && make_tmap_mn3(&t3, A, ti.in_bf16, M, K, lda, bn / 64);
+    if (b3) tb = t3;
 
     const int64_t ld_ws = cdiv(N, 4) * 4;
     Workspace *w = nullptr;
@@ -417,6 +454,8 @@ int splitk_swapped(DeviceState *d, const TypeInfo &ti, int transA, int transB, i
         return rc;
 
     TileParams p{};           // in the kernel's (transposed) frame
+    p.a_mn3 = a3;
+    p.b_mn3 = b3;
     p.M = (int)N;
     p.N = (int)M;
     p.K = (int)K;
@@ -735,8 +774,16 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
     ok = ok && (b_mn ? make_tmap(&tb, B, ti.in_bf16, N, K, ldb, 64)
                      : make_tmap(&tb, B, ti.in_bf16, K, N, ldb, pair ? bn / 2 : bn));
     if (!ok) return cuda_fail();
+    // MN-major operands: one 3-D box per stage where the extent allows.
+    CUtensorMap t3;
+    const bool a3 = a_mn && make_tmap_mn3(&t3, A, ti.in_bf16, M, K, lda, swg::BM / 64);
+    if (a3) ta = t3;
+    const bool b3 = b_mn && make_tmap_mn3(&t3, B, ti.in_bf16, N, K, ldb, (pair ? bn / 2 : bn) / 64);
+    if (b3) tb = t3;
 
     TileParams p{};
+    p.a_mn3 = a3;
+    p.b_mn3 = b3;
     p.M = (int)M;
     p.N = (int)N;
     p.K = (int)K;
@@ -835,8 +882,13 @@ int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M, int64_t N
     CUtensorMap ta, tb;
     if (!make_tmap(&ta, A, true, K, M, K, swg::BM) || !make_tmap(&tb, W_fused, true, N2, K, N2, 64))
         return cuda_fail();
+    // W_fused is MN-major: one 3-D box per stage where 2N allows.
+    CUtensorMap t3;
+    const bool b3 = make_tmap_mn3(&t3, W_fused, true, N2, K, N2, (pair ? bn / 2 : bn) / 64);
+    if (b3) tb = t3;
 
     TileParams p{};
+    p.b_mn3 = b3;
     p.M = (int)M;
     p.N = (int)N2;
     p.K = (int)K;
@@ -965,8 +1017,19 @@ int swiglu_mlp_dual(const void *A, const void *W1, const void *W2, void *Y, int6
     if (!make_tmap(&ta, A, true, K, M, K, swg::BM) || !make_tmap(&tw1, W1, true, N, K, N, 64) ||
         !make_tmap(&tw2, W2, true, N, K, N, 64))
         return cuda_fail();
+    // W1 and W2 are MN-major: 3-D boxes of a pair CTA's whole half (or a
+    // single CTA's Gate or Up atoms) where N allows; both maps or neither.
+    CUtensorMap t31, t32;
+    const int w_atoms = bn / 128;
+    const bool w3 = make_tmap_mn3(&t31, W1, true, N, K, N, w_atoms) &&
+                    make_tmap_mn3(&t32, W2, true, N, K, N, w_atoms);
+    if (w3) {
+        tw1 = t31;
+        tw2 = t32;
+    }
 
     TileParams p{};
+    p.b_mn3 = w3;
     p.M = (int)M;
     p.N = (int)N;              // output columns; a tile covers bn/2 of them
     p.K = (int)K;

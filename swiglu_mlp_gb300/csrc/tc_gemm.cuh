@@ -103,6 +103,9 @@ struct TileParams {
     int tma_store;
     int a_mn_major;              // op(A) stored M-contiguous (transA = T)
     int b_mn_major;              // op(B) stored N-contiguous (transB = N)
+    // MN-major operand mapped in 3-D (64 MN x K rows x atoms): one box per
+    // stage fills all its 64-wide atoms (see make_tmap_mn3); 0: 2-D boxes.
+    int a_mn3, b_mn3;
     float alpha, beta;
     void *D;                     // output (also C when beta != 0)
     long long ldd;
@@ -570,8 +573,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         else
                             tma_load_2d(dst, tm, fb, x, y);
                     };
+                    auto load3 = [&](uint32_t dst, const CUtensorMap *tm, int y, int z) {
+                        if (PAIR)
+                            tma_load_3d_pair(dst, tm, fb, 0, y, z);
+                        else
+                            tma_load_3d(dst, tm, fb, 0, y, z);
+                    };
                     if (!p.a_mn_major) {
                         load(a_dst, &tmA, k0, m0);                          // box {64 K, 128 M}
+                    } else if (p.a_mn3) {
+                        load3(a_dst, &tmA, k0, m0 / 64);                    // box {64 M, 64 K, 2}
                     } else {
                         load(a_dst, &tmA, m0, k0);                          // box {64 M, 64 K}
                         load(a_dst + 8192, &tmA, m0 + 64, k0);
@@ -581,14 +592,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         // this CTA's B_COLS columns come from W1 (rank 0) or
                         // W2 (rank 1); single CTA: BN/2 from each.
                         const int nd = nb * (BN / 2);
+                        if (p.b_mn3 && PAIR) {
+                            // box {64 N, 64 K, B_COLS / 64} of this CTA's weight
+                            load3(b_dst, rank != 0 ? &tmX : &tmB, k0, nd / 64);
+                        } else if (p.b_mn3) {
+                            // boxes {64 N, 64 K, BN / 128}: Gate atoms, then Up atoms
+                            load3(b_dst, &tmB, k0, nd / 64);
+                            load3(b_dst + (BN / 128) * 8192, &tmX, k0, nd / 64);
+                        } else {
 #pragma unroll
-                        for (int c = 0; c < C::B_COLS / 64; ++c) {
-                            const bool up = PAIR ? (rank != 0) : (c >= BN / 128);
-                            const int cc = PAIR ? c : (c % (BN / 128));
-                            load(b_dst + c * 8192, up ? &tmX : &tmB, nd + cc * 64, k0);
+                            for (int c = 0; c < C::B_COLS / 64; ++c) {
+                                const bool up = PAIR ? (rank != 0) : (c >= BN / 128);
+                                const int cc = PAIR ? c : (c % (BN / 128));
+                                load(b_dst + c * 8192, up ? &tmX : &tmB, nd + cc * 64, k0);
+                            }
                         }
                     } else if (!p.b_mn_major) {
                         load(b_dst, &tmB, k0, n0);                          // box {64 K, B_COLS N}
+                    } else if (p.b_mn3) {
+                        load3(b_dst, &tmB, k0, n0 / 64);                    // box {64 N, 64 K, B_COLS / 64}
                     } else {
 #pragma unroll
                         for (int c = 0; c < C::B_COLS / 64; ++c)            // box {64 N, 64 K}

@@ -211,3 +211,83 @@ def test_default_stream_is_torch_current_stream():
     s.synchronize()
     assert torch.all(D == 64.0)
     assert swg._stream(None) == torch.cuda.current_stream().cuda_stream
+
+
+@pytest.mark.parametrize("tA,tB", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("shape", [(512, 768, 640), (256, 128, 1000), (384, 448, 72), (1024, 2048, 512)])
+def test_mn_major_3d_boxes_match_2d(monkeypatch, tA, tB, shape):
+    """An MN-major operand whose MN extent is a multiple of 64 is loaded with
+    one 3-D TMA box per stage instead of one 2-D box per 64-wide atom; the
+    stage contents, and so the outputs, must be identical (SWG_MN_3D=0 keeps
+    the 2-D boxes)."""
+    M, N, K = shape
+    g = synth.generator(900 + M + N + K + 2 * tA + tB)
+    A = synth.normal(synth.stored_shape(tA, M, K), g).cuda()
+    B = synth.normal(synth.stored_shape(tB, K, N), g).cuda()
+    C = synth.normal((M, N), g).cuda()
+    out = []
+    for flag in ("1", "0"):
+        monkeypatch.setenv("SWG_MN_3D", flag)
+        D = C.clone()
+        swg.gemm(tA, tB, M, N, K, 1.0, A, A.shape[1], B, B.shape[1], 0.5, D, N, swg.BF16)
+        out.append(D.cpu())
+    assert swg.get_device_error() == 0
+    assert torch.equal(out[0], out[1])
+    yhat = oracle.gemm(tA, tB, M, N, K, 1.0, A.cpu(), A.shape[1], B.cpu(), B.shape[1], 0.5,
+                       C.cpu(), N)
+    check_half(to_f64(out[0]), yhat, f"3-D boxes {shape} tA={tA} tB={tB}")
+
+
+@pytest.mark.parametrize("M,K,N", [(512, 896, 4864), (128, 512, 640)])
+def test_swiglu_3d_weight_boxes_match_2d(monkeypatch, M, K, N):
+    A, W1, W2 = synth.swiglu(M, K, N, seed=910 + M)
+    Ad = A.cuda()
+    Wf = swg.interleave_weights(W1.cuda(), W2.cuda())
+    out = []
+    for flag in ("1", "0"):
+        monkeypatch.setenv("SWG_MN_3D", flag)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        swg.swiglu_mlp(Ad, Wf, Y, M, N, K)
+        out.append(Y.cpu())
+    assert swg.get_device_error() == 0
+    assert torch.equal(out[0], out[1])
+
+
+@pytest.mark.parametrize("M", [16, 64])
+@pytest.mark.parametrize("tA,tB", [(0, 0), (1, 0), (1, 1)])
+def test_few_rows_3d_boxes_match_2d(monkeypatch, M, tA, tB):
+    """The few-rows split-K path (transposed product) with MN-major operands
+    in 3-D boxes gives the same bits as with 2-D boxes."""
+    N, K = 1024, 4096
+    g = synth.generator(920 + M + 2 * tA + tB)
+    A = synth.normal(synth.stored_shape(tA, M, K), g).cuda()
+    B = synth.normal(synth.stored_shape(tB, K, N), g).cuda()
+    C = synth.normal((M, N), g).cuda()
+    out = []
+    for flag in ("1", "0"):
+        monkeypatch.setenv("SWG_MN_3D", flag)
+        D = C.clone()
+        swg.gemm(tA, tB, M, N, K, 1.0, A, A.shape[1], B, B.shape[1], 1.0, D, N, swg.BF16)
+        out.append(D.cpu())
+    assert swg.get_device_error() == 0
+    assert torch.equal(out[0], out[1])
+    yhat = oracle.gemm(tA, tB, M, N, K, 1.0, A.cpu(), A.shape[1], B.cpu(), B.shape[1], 1.0,
+                       C.cpu(), N)
+    check_half(to_f64(out[0]), yhat, f"few rows 3-D M={M} tA={tA} tB={tB}")
+
+
+@pytest.mark.parametrize("M", [128, 512])
+def test_swiglu_dual_3d_boxes_match_2d(monkeypatch, M):
+    K, N = 640, 1536
+    A, W1, W2 = synth.swiglu(M, K, N, seed=930 + M)
+    Ad, W1d, W2d = A.cuda(), W1.cuda(), W2.cuda()
+    out = []
+    for flag in ("1", "0"):
+        monkeypatch.setenv("SWG_MN_3D", flag)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        swg.swiglu_mlp_dual(Ad, W1d, W2d, Y, M, N, K)
+        out.append(Y.cpu())
+    assert swg.get_device_error() == 0
+    assert torch.equal(out[0], out[1])
+    yhat = oracle.swiglu(A, W1, W2, M, N, K)
+    check_half(to_f64(out[0]), yhat, f"dual 3-D M={M}")
