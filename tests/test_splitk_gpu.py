@@ -2,9 +2,9 @@
 
 Skinny GEMM (M = 16, 32, 64; N = 4096; K = 16384; alpha = 1, beta = 1 with a
 bf16 C) runs with the K loop split across CTAs and the FP32 partials reduced
-by the last-arriving CTA in split order ("为什么 GEMM 是 CUDA 的必修课",
-关键技术 item 5).  The reduction order is fixed, so repeated calls must give
-identical bits.
+in split order by a second kernel ("为什么 GEMM 是 CUDA 的必修课", 关键技术
+item 5).  The reduction order is fixed, so repeated calls must give identical
+bits.
 """
 import numpy as np
 import pytest
