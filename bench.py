@@ -111,32 +111,52 @@ def profiled_traffic(profile_name: str):
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons (every 200 ms)."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampling of SM clocks, power and throttle reasons, started
+    before the warm-up (so that it is running when the timed region begins)
+    and every `interval_ms`; stop() keeps the samples whose timestamps fall
+    inside the timed window [t0, t1] (host wall clock)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, interval_ms: int = 20):
         self.gpu = gpu_index
+        self.interval_ms = interval_ms
         self.proc = None
         self.path = None
 
-    def start(self):
+    def start(self, wait_s: float = 5.0):
+        """Starts nvidia-smi and waits (at most wait_s) for its first row."""
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+            return
+        t_end = time.time() + wait_s
+        while time.time() < t_end:
+            self.out.flush()
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.01)
 
-    def stop(self):
+    @staticmethod
+    def _when(stamp: str):
+        import datetime
+        try:
+            return datetime.datetime.strptime(stamp.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
+    def stop(self, t0: float, t1: float):
         if self.proc is None:
             return None
-        time.sleep(0.25)
+        time.sleep(3 * self.interval_ms / 1000.0)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -147,25 +167,30 @@ class ClockSampler:
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
+                if len(parts) >= 10:
                     rows.append(parts)
         os.unlink(self.path)
-        if not rows:
+        inside = [r for r in rows if (lambda w: w is not None and t0 <= w <= t1)(self._when(r[0]))]
+        if not inside:
             return None
+
         def num(x):
             try:
                 return float(x)
             except ValueError:
                 return float("nan")
-        sm = [num(r[1]) for r in rows]
-        sm_max = max(num(r[2]) for r in rows)
+        sm = [num(r[2]) for r in inside if not math.isnan(num(r[2]))]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4)
-                          if r[5 + i].lower().startswith("active")})
-        load = [s for s in sm if not math.isnan(s)]
-        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": sm_max,
-                "reasons": reasons, "samples": len(rows),
-                "power_w_max": max(num(r[3]) for r in rows)}
+        reasons = sorted({names[i] for r in inside for i in range(4)
+                          if r[6 + i].lower().startswith("active")})
+        power = [num(r[4]) for r in inside if not math.isnan(num(r[4]))]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(num(r[3]) for r in inside),
+                "reasons": reasons, "samples": len(inside),
+                "interval_ms": self.interval_ms,
+                "window_s": round(t1 - t0, 3),
+                "power_w_median": statistics.median(power) if power else None,
+                "power_w_max": max(power) if power else None}
 
 
 def dist_env():
@@ -255,13 +280,14 @@ def run_ours(args):
             if events is not None:
                 events[i][1].record(stream)
 
+    sampler = ClockSampler(local)
+    sampler.start()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
     if swg.get_device_error(stream) != 0:
         raise RuntimeError("device error word set during warm-up")
 
-    sampler = ClockSampler(local)
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in TRANS] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
@@ -269,15 +295,16 @@ def run_ours(args):
     if dist_mod:
         dist_mod.barrier()
     torch.cuda.synchronize(dev)
-    sampler.start()
     launches0 = swg.launch_count()
+    w0 = time.time()
     t_start.record(stream)
     for s in range(args.steps):
         step(ev[s])
     t_end.record(stream)
     torch.cuda.synchronize(dev)
+    w1 = time.time()
     launches = swg.launch_count() - launches0
-    clocks = sampler.stop()
+    clocks = sampler.stop(w0, w1)
     if dist_mod:
         dist_mod.barrier()
     if swg.get_device_error(stream) != 0:
