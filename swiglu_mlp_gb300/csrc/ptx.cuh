@@ -279,10 +279,14 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
     return out;
 }
 
-// Arrive on an mbarrier anywhere in the cluster (release at cluster scope).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
+// Arrive on an mbarrier of another CTA of the cluster as a hand-off of tensor
+// memory: release at CTA scope only (the PTX default), so the arrival does
+// not wait for this thread's earlier global stores to become visible across
+// the cluster.  The tensor-memory reads it publishes are ordered before it by
+// tcgen05.fence::before_thread_sync, not by the release.
+__device__ __forceinline__ void mbar_arrive_remote_tmem(uint32_t cluster_addr)
 {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
 }
 

@@ -766,7 +766,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             __syncwarp();
             if (lane == 0) {
                 if (PAIR)
-                    mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[acc]), 0));
+                    mbar_arrive_remote_tmem(mapa_shared(smem_u32(&acc_empty[acc]), 0));
                 else
                     mbar_arrive(smem_u32(&acc_empty[acc]));
             }
@@ -878,7 +878,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // barrier in pair mode), one arrival per warp.
             if (lane == 0) {
                 if (PAIR)
-                    mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[acc]), 0));
+                    mbar_arrive_remote_tmem(mapa_shared(smem_u32(&acc_empty[acc]), 0));
                 else
                     mbar_arrive(smem_u32(&acc_empty[acc]));
             }
