@@ -6,7 +6,9 @@
 //                    free shared-memory stage, arms the stage's "full" barrier
 //                    with the byte count and issues the tile loads of op(A)
 //                    and op(B) (128-byte swizzle; the tensor map's box and the
-//                    operand's major-ness realise op = N / T without copies).
+//                    operand's major-ness realise op = N / T without copies;
+//                    an MN-major operand whose extent is a multiple of 64
+//                    arrives as one 3-D box holding all its 64-wide atoms).
 //   warp 1         : allocates tensor memory (TMEM); lane 0 issues
 //                    tcgen05.mma (M=128, N=BN, K=16, FP32 accumulate) into one
 //                    of two TMEM accumulators and commits each stage back to
@@ -29,8 +31,10 @@
 //
 // CTA pairs (PAIR): clusters of two CTAs share one cta_group::2 MMA of
 // 256 x BN; each CTA loads its 128 rows of A and half of B, and receives its
-// own 128 accumulator rows.  EPI_SPLITK_T and EPI_SWIGLU_DUAL are described
-// at the EpiKind enumeration.
+// own 128 accumulator rows.  Each epilogue warp hands a drained accumulator
+// back on the leader's barrier with a release at CTA scope only: the hand-off
+// orders tensor-memory reads, not the warp's global stores.  EPI_SPLITK_T and
+// EPI_SWIGLU_DUAL are described at the EpiKind enumeration.
 //
 // Programmatic dependent launch: the kernel lets the next kernel on the stream
 // be scheduled as soon as it starts, and touches global memory only after
