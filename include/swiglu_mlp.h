@@ -104,11 +104,19 @@ typedef enum {
  *                   allocated (queued work or a captured graph may still use
  *                   them) until swg_shutdown() frees them all.  Two kernels are
  *                   launched: the GEMM and a dependent reduction.
+ *   One or two rows M <= 2 with 16-bit A and B (decode of one or two tokens)
+ *                   K <= 8 * 8192 / M and N <= 2^30: one kernel on the FP32 pipes
+ *                   instead ("GEMM o Coração Matemático", §14: the product
+ *                   streams op(B) once and is bound by memory).  Its K split
+ *                   is summed inside the kernel, again in a fixed order; it
+ *                   uses no workspace.  Setting the environment variable
+ *                   SWG_GEMV=0 sends these calls to the tensor-core path.
  *   Graph capture   every call can be captured into a CUDA graph on a stream
  *                   once the same call (or one needing at least as much
  *                   workspace) has run on that stream; a call that would have
  *                   to allocate while its stream is capturing returns
- *                   SWG_ERR_UNSUPPORTED and launches nothing.
+ *                   SWG_ERR_UNSUPPORTED and launches nothing.  Calls of the
+ *                   one-or-two-rows kernel need no earlier run.
  */
 SWG_API int gemm(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
          const void *A, int64_t lda, const void *B, int64_t ldb, float beta,
@@ -116,7 +124,8 @@ SWG_API int gemm(int transA, int transB, int64_t M, int64_t N, int64_t K, float 
 
 /*
  * gemm_ex — gemm with an explicit split-K factor.
- *   split_k == 0  automatic choice (what gemm does);
+ *   split_k == 0  automatic choice (what gemm does, including the kernel for
+ *                 one or two rows);
  *   split_k == 1  no split;
  *   split_k >= 2  split the K loop into at most min(split_k, 16) contiguous
  *                 ranges (fewer when K has fewer 64-wide blocks).

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libswiglu_mlp.so")
-SOURCES = ["api.cu", "k_store.cu", "k_swiglu.cu", "k_splitk.cu", "k_fp8.cu"]
+SOURCES = ["api.cu", "k_store.cu", "k_swiglu.cu", "k_splitk.cu", "k_fp8.cu", "k_gemv.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE]

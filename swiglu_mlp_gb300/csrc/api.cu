@@ -496,6 +496,96 @@ int splitk_swapped(DeviceState *d, const TypeInfo &ti, int transA, int transB, i
     return SWG_OK;
 }
 
+// One or two rows of 16-bit inputs: one launch of the cluster kernel of
+// k_gemv.cu on the FP32 pipes (the product streams op(B) once; tensor-core
+// tiles would be almost all padding).  Measured on GB300 at 4096 x 4096: one
+// row 8.3 us back to back against 9.5-10.0 us for the split-K tensor-core
+// path; three or four rows were slower here (10.9-13.6 us) than there.  Blocks of 32 (B stored N x K) or 64
+// (B stored K x N) output columns.  K is cut into up to 8 ranges: as many as
+// bring the grid to about one CTA per SM, at least as many as keep the FP32
+// op(A) slice a CTA stages within kGemvSlice / rows elements, each range a
+// whole number of boxes (256 or 128 K elements) except the last.  The ring
+// of 16 KB boxes is as deep as 227 KB of shared memory allows (12 at most),
+// or half that when the grid is larger than the GPU (two CTAs per SM).
+// SWG_ERR_UNSUPPORTED, with nothing launched, when K needs more ranges, N
+// is beyond 2^30 or the tensor map cannot be encoded.
+constexpr int64_t kGemvMaxRows = 2;
+constexpr int64_t kGemvSlice = 8192;
+
+bool gemv_disabled()
+{
+    const char *v = std::getenv("SWG_GEMV");
+    return v && v[0] == '0';
+}
+
+// Row-major matrix of `outer` rows x `inner` contiguous 16-bit elements, read
+// without swizzle in boxes of box_inner x box_outer; past the edges reads zero.
+bool make_tmap_plain(CUtensorMap *m, const void *ptr, bool bf16, int64_t inner, int64_t outer,
+                     int64_t ld, int box_inner, int box_outer)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
+    cuuint32_t estr[2] = {1u, 1u};
+    return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+              const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int gemv_path(DeviceState *d, const TypeInfo &ti, int transA, int transB, int64_t M, int64_t N,
+              int64_t K, float alpha, const void *A, int64_t lda, const void *B, int64_t ldb,
+              float beta, void *C, int64_t ldc, cudaStream_t s)
+{
+    const int mr = M <= 1 ? 1 : 2;
+    const bool b_kn = transB == SWG_OP_N;
+    const int64_t ks = swg::gemv_k_per_stage(b_kn);
+    const int64_t blocks = cdiv(N, swg::gemv_cols_per_block(b_kn));
+    const int64_t kr_max = kGemvSlice / mr;          // a multiple of both box lengths
+    const int64_t s_min = cdiv(K, kr_max);
+    if (s_min > 8 || N > (int64_t(1) << 30)) return SWG_ERR_UNSUPPORTED;
+    int64_t ranges = std::min<int64_t>(8, std::max<int64_t>(1, d->sms / blocks));
+    ranges = std::min<int64_t>(ranges, cdiv(K, ks));
+    ranges = std::max<int64_t>(ranges, s_min);
+    const int64_t kr = cdiv(cdiv(K, ranges), ks) * ks;
+    ranges = cdiv(K, kr);
+    const int64_t budget = blocks * ranges > d->sms ? 115712 : swg::GV_MAX_SMEM;
+    const int64_t fixed = swg::gemv_smem_bytes(mr, b_kn, (int)kr, 0);
+    const int64_t per_stage = swg::gemv_smem_bytes(mr, b_kn, (int)kr, 1) - fixed;
+    const int64_t stages = std::min<int64_t>({12, cdiv(kr, ks), (budget - fixed) / per_stage});
+    if (stages < 1) return SWG_ERR_UNSUPPORTED;
+
+    CUtensorMap tm;
+    const bool ok = b_kn ? make_tmap_plain(&tm, B, ti.in_bf16, N, K, ldb, swg::gemv_box_inner(true),
+                                           swg::gemv_box_outer(true))
+                         : make_tmap_plain(&tm, B, ti.in_bf16, K, N, ldb, swg::gemv_box_inner(false),
+                                           swg::gemv_box_outer(false));
+    if (!ok) return SWG_ERR_UNSUPPORTED;
+
+    swg::GemvArgs g{};
+    g.A = static_cast<const uint16_t *>(A);
+    g.lda = lda;
+    g.a_t = transA == SWG_OP_T;
+    g.D = C;
+    g.ldd = ldc;
+    g.M = (int)M;
+    g.N = (int)N;
+    g.K = (int)K;
+    g.kr = (int)kr;
+    g.ranges = (int)ranges;
+    g.stages = (int)stages;
+    g.alpha = alpha;
+    g.beta = beta;
+    g.out_kind = ti.out_kind;
+    g.err = d->err;
+    if (swg::launch_gemv(tm, g, mr, b_kn, ti.in_bf16, (int)blocks, s) != cudaSuccess)
+        return cuda_fail();
+    g_launches++;
+    return SWG_OK;
+}
+
 // ----------------------------------------------------------------- small kernels
 
 __global__ void scale_kernel(void *D, long long ldd, int M, int N, float beta, int out_kind)
@@ -717,6 +807,12 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
                                                               ti.out_kind);
         g_launches++;
         return launch_status();
+    }
+
+    if (split_k == 0 && M <= kGemvMaxRows && !gemv_disabled()) {
+        const int rc = gemv_path(d, ti, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C,
+                                 ldc, s);
+        if (rc != SWG_ERR_UNSUPPORTED) return rc;
     }
 
     const int64_t kb = cdiv(K, swg::BK);

@@ -1,0 +1,483 @@
+// k_gemv.cu — the few-rows product (one or two rows of op(A): decode of one
+// or two tokens) on the FP32 pipes, in one launch per call.
+//
+// With M <= 2 every weight element is used at most twice, so the call costs
+// the time to stream op(B) from HBM once ("GEMM o Coração Matemático", §14:
+// about one FLOP per byte at M = 1), and a 128-row tensor-core tile would be
+// at least 98% padding.  (With three or four rows the FP32 work per byte no
+// longer hides under the stream; those calls stay on the tensor cores.)  The K loop is split across CTAs when the output has
+// too few columns to fill the GPU ("为什么 GEMM 是 CUDA 的必修课", 关键技术
+// item 5); here the S K ranges of one block of output columns run as ONE
+// thread-block cluster, and CTA 0 of the cluster sums the S partial blocks,
+// read from the other CTAs' shared memory in rank order.  The result is
+// bit-identical from run to run, and there is no workspace and no second
+// kernel.
+//
+// Streaming at HBM speed needs about 150-250 KB in flight per SM (the loaded
+// DRAM latency is several microseconds), more than registers can hold, so B
+// moves by TMA: warp 0 (one thread) loads 16 KB boxes of B into a ring of
+// shared-memory stages, up to 12 of them, and 8 consumer warps compute from
+// shared memory.  Boxes past the edges of B read as zero, so ragged N and K
+// need no extra code.  Per CTA: one block of output columns, one contiguous K
+// range.  The consumers first widen the range's slice of op(A) to FP32 in
+// shared memory (zero beyond the M rows and past K) while the first boxes are
+// in flight.  By the layout of B:
+//   op(B) = B^T (B stored N x K, K contiguous; a linear layer's weight):
+//     boxes of 256 K x 32 rows; each consumer warp owns 4 rows (output
+//     columns), lane l takes elements 8l..8l+7 of each row, and a shuffle
+//     butterfly sums the 32 lanes at the end;
+//   op(B) = B (B stored K x N, N contiguous): boxes of 64 columns x 128 K
+//     rows; 8 threads cover the 64 columns (8 each) and 32 row lanes take
+//     every 32nd row; the 4 row lanes of a warp are summed by shuffles, the 8
+//     warps in shared memory.
+// Every sum runs in a fixed order.  The output is D = alpha * sum + beta * C
+// with C read only when beta != 0.  Each wait on a stage barrier is bounded:
+// past the limit the CTA records ERR_TIMEOUT in the error word, the producer
+// waits (bounded again) for its boxes in flight, and the kernel returns.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "launch_impl.cuh"
+
+namespace swg {
+namespace {
+
+constexpr int GV_CONSUMERS = 256;                   // 8 consumer warps
+constexpr int GV_WARPS = GV_CONSUMERS / 32;
+constexpr int GV_THREADS = GV_CONSUMERS + 32;       // + the producer warp
+constexpr int GV_STAGE_BYTES = 16384;
+constexpr int GV_STAGE_ELEMS = GV_STAGE_BYTES / 2;
+constexpr int NK_CW = 32;                           // B stored N x K: rows per box
+constexpr int NK_KS = 256;                          //   K elements per box
+constexpr int NK_RPW = NK_CW / GV_WARPS;            //   rows per consumer warp (4)
+constexpr int KN_CW = 64;                           // B stored K x N: columns per box
+constexpr int KN_KS = 128;                          //   K rows per box
+constexpr int KN_RPT = KN_KS / 32;                  //   rows per thread and box (4)
+
+template <bool BF16>
+__device__ __forceinline__ float widen1(uint32_t bits16)
+{
+    if (BF16) return __uint_as_float(bits16 << 16);   // bfloat16 = top half of binary32
+    return __half2float(__ushort_as_half((unsigned short)bits16));
+}
+
+// The eight 16-bit values of one 16-byte load, widened to FP32 (exact).
+template <bool BF16>
+__device__ __forceinline__ void widen8(const uint4 &v, float (&f)[8])
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        if (BF16) {
+            f[2 * h] = __uint_as_float(w[h] << 16);
+            f[2 * h + 1] = __uint_as_float(w[h] & 0xffff0000u);
+        } else {
+            const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&w[h]));
+            f[2 * h] = t.x;
+            f[2 * h + 1] = t.y;
+        }
+    }
+}
+
+__device__ __forceinline__ uint4 ld16(const uint16_t *p)
+{
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+
+// Up to eight 16-bit values at p (cnt of them, the rest zero) as one uint4.
+__device__ __forceinline__ uint4 ld_partial(const uint16_t *p, int cnt)
+{
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        if (e < cnt) w[e >> 1] |= (uint32_t)__ldg(p + e) << (16 * (e & 1));
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// op(A)[m][k0 + kk] for m < MR, kk < kr, widened to FP32 into As, zero where
+// m >= M or kk >= klen.  M_MAJOR: As[m * kr + kk]; else As[kk * MR + m].
+// A stored M x K (a_t = 0) is read 8 elements per 16-byte load; A stored
+// K x M (a_t = 1) one element at a time.
+template <int MR, bool BF16, bool M_MAJOR>
+__device__ __forceinline__ void stage_a(float *As, const GemvArgs &g, int k0, int klen, int ct)
+{
+    const int kr = g.kr;
+    if (!g.a_t) {
+        const int per_row = kr >> 3;            // 8-element groups per row
+        const int groups = MR * per_row;
+        constexpr int U = 4;
+        for (int g0 = ct; g0 < groups; g0 += U * GV_CONSUMERS) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int q = g0 + u * GV_CONSUMERS;
+                const int m = q / per_row, kk = (q - m * per_row) * 8;
+                const int cnt = klen - kk;
+                v[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (q < groups && m < g.M && cnt > 0) {
+                    const uint16_t *p = g.A + (long long)m * g.lda + k0 + kk;
+                    v[u] = cnt >= 8 ? ld16(p) : ld_partial(p, cnt);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int q = g0 + u * GV_CONSUMERS;
+                if (q >= groups) break;
+                const int m = q / per_row, kk = (q - m * per_row) * 8;
+                float f[8];
+                widen8<BF16>(v[u], f);
+                if (M_MAJOR) {
+                    float4 *d = reinterpret_cast<float4 *>(As + m * kr + kk);
+                    d[0] = make_float4(f[0], f[1], f[2], f[3]);
+                    d[1] = make_float4(f[4], f[5], f[6], f[7]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) As[(kk + e) * MR + m] = f[e];
+                }
+            }
+        }
+    } else {
+        const int total = MR * kr;
+        constexpr int U = 8;
+        for (int i0 = ct; i0 < total; i0 += U * GV_CONSUMERS) {
+            uint32_t v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i = i0 + u * GV_CONSUMERS;
+                int m, kk;
+                if (M_MAJOR) { m = i / kr; kk = i - m * kr; }
+                else { kk = i / MR; m = i - kk * MR; }
+                v[u] = 0u;
+                if (i < total && m < g.M && kk < klen)
+                    v[u] = __ldg(g.A + (long long)(k0 + kk) * g.lda + m);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i = i0 + u * GV_CONSUMERS;
+                if (i < total) As[i] = widen1<BF16>(v[u]);
+            }
+        }
+    }
+}
+
+
+// Shared memory of one CTA, from a 128-byte aligned base: the ring of boxes,
+// the op(A) slice (MR x kr FP32), this CTA's partial block (MR x CW FP32),
+// the per-warp sums of the K x N layout (8 x MR x 64 FP32), the stage
+// barriers full[ns] and empty[ns], and the abort flag.
+struct GvLayout {
+    int as, part, red, bars, abort_off, total;
+};
+
+__host__ __device__ inline GvLayout gv_layout(int mr, bool b_kn, int kr, int ns)
+{
+    GvLayout L;
+    L.as = ns * GV_STAGE_BYTES;
+    L.part = L.as + 4 * mr * kr;
+    L.red = L.part + 4 * mr * (b_kn ? KN_CW : NK_CW);
+    L.bars = L.red + (b_kn ? 4 * GV_WARPS * mr * KN_CW : 0);
+    L.abort_off = L.bars + 16 * ns;
+    L.total = L.abort_off + 16 + 128;                  // + alignment slack
+    return L;
+}
+
+// The 8 warps of a box agree on whether to go on: a wait that ran out, or
+// the abort flag, stops all of them together.
+__device__ __forceinline__ bool stage_ready(const uint64_t *full, int s, int ns,
+                                            volatile int *abort_flag, int *err)
+{
+    const bool got = wait_bounded(smem_u32(&full[s % ns]), (uint32_t)((s / ns) & 1), abort_flag, err);
+    return __all_sync(0xffffffffu, got);
+}
+
+// B stored N x K.  Box s of the range holds rows n0..n0+31, K elements
+// k0 + 256 s .. + 255 (row-major, 512 bytes a row).
+template <int MR, bool BF16>
+__device__ __forceinline__ void consume_nk(const GemvArgs &g, const uint16_t *ring,
+                                           const uint64_t *full, uint64_t *empty,
+                                           volatile int *abort_flag, float *As, float *part,
+                                           int k0, int klen, int nst, int ct)
+{
+    stage_a<MR, BF16, true>(As, g, k0, klen, ct);
+    named_bar_sync(1, GV_CONSUMERS);
+    const int cw = ct >> 5, lane = ct & 31;
+    float acc[MR][NK_RPW];
+#pragma unroll
+    for (int m = 0; m < MR; ++m)
+#pragma unroll
+        for (int r = 0; r < NK_RPW; ++r) acc[m][r] = 0.0f;
+
+    for (int s = 0; s < nst; ++s) {
+        if (!stage_ready(full, s, g.stages, abort_flag, g.err)) break;
+        const int slot = s % g.stages;
+        const uint16_t *st = ring + slot * GV_STAGE_ELEMS + cw * NK_RPW * NK_KS + 8 * lane;
+        uint4 bv[NK_RPW];
+#pragma unroll
+        for (int r = 0; r < NK_RPW; ++r) bv[r] = *reinterpret_cast<const uint4 *>(st + r * NK_KS);
+        float a[MR][8];
+#pragma unroll
+        for (int m = 0; m < MR; ++m) {
+            const float *ap = As + m * g.kr + s * NK_KS + 8 * lane;
+            const float4 a0 = *reinterpret_cast<const float4 *>(ap);
+            const float4 a1 = *reinterpret_cast<const float4 *>(ap + 4);
+            a[m][0] = a0.x; a[m][1] = a0.y; a[m][2] = a0.z; a[m][3] = a0.w;
+            a[m][4] = a1.x; a[m][5] = a1.y; a[m][6] = a1.z; a[m][7] = a1.w;
+        }
+#pragma unroll
+        for (int r = 0; r < NK_RPW; ++r) {
+            float b[8];
+            widen8<BF16>(bv[r], b);
+#pragma unroll
+            for (int m = 0; m < MR; ++m)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[m][r] = fmaf(a[m][e], b[e], acc[m][r]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
+    }
+#pragma unroll
+    for (int m = 0; m < MR; ++m)
+#pragma unroll
+        for (int r = 0; r < NK_RPW; ++r) {
+            float v = acc[m][r];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            if (lane == 0) part[m * NK_CW + cw * NK_RPW + r] = v;
+        }
+}
+
+// B stored K x N.  Box s of the range holds K rows k0 + 128 s .. + 127,
+// columns n0..n0+63 (row-major, 128 bytes a row).
+template <int MR, bool BF16>
+__device__ __forceinline__ void consume_kn(const GemvArgs &g, const uint16_t *ring,
+                                           const uint64_t *full, uint64_t *empty,
+                                           volatile int *abort_flag, float *As, float *red,
+                                           float *part, int k0, int klen, int nst, int ct)
+{
+    stage_a<MR, BF16, false>(As, g, k0, klen, ct);
+    named_bar_sync(1, GV_CONSUMERS);
+    const int cx = ct & 7, rl = ct >> 3;               // 8 column threads x 32 row lanes
+    const int cw = ct >> 5, lane = ct & 31;
+    float acc[MR][8];
+#pragma unroll
+    for (int m = 0; m < MR; ++m)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[m][e] = 0.0f;
+
+    for (int s = 0; s < nst; ++s) {
+        if (!stage_ready(full, s, g.stages, abort_flag, g.err)) break;
+        const int slot = s % g.stages;
+        const uint16_t *st = ring + slot * GV_STAGE_ELEMS + 8 * cx;
+        uint4 bv[KN_RPT];
+#pragma unroll
+        for (int i = 0; i < KN_RPT; ++i)
+            bv[i] = *reinterpret_cast<const uint4 *>(st + (rl + 32 * i) * KN_CW);
+#pragma unroll
+        for (int i = 0; i < KN_RPT; ++i) {
+            const int kk = s * KN_KS + rl + 32 * i;
+            float a[MR];
+            if constexpr (MR == 2) {
+                const float2 t = *reinterpret_cast<const float2 *>(As + kk * 2);
+                a[0] = t.x; a[1] = t.y;
+            } else {
+                a[0] = As[kk];
+            }
+            float b[8];
+            widen8<BF16>(bv[i], b);
+#pragma unroll
+            for (int m = 0; m < MR; ++m)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[m][e] = fmaf(a[m], b[e], acc[m][e]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
+    }
+    // The 4 row lanes of this warp (lanes cx, cx + 8, cx + 16, cx + 24).
+#pragma unroll
+    for (int m = 0; m < MR; ++m)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            float v = acc[m][e];
+            v += __shfl_xor_sync(0xffffffffu, v, 8);
+            v += __shfl_xor_sync(0xffffffffu, v, 16);
+            if (lane < 8) red[(cw * MR + m) * KN_CW + 8 * lane + e] = v;
+        }
+    named_bar_sync(1, GV_CONSUMERS);
+    for (int t = ct; t < MR * KN_CW; t += GV_CONSUMERS) {
+        const int m = t / KN_CW, col = t - m * KN_CW;
+        float sum = 0.0f;
+#pragma unroll
+        for (int w = 0; w < GV_WARPS; ++w) sum += red[(w * MR + m) * KN_CW + col];
+        part[t] = sum;
+    }
+}
+
+// Grid: clusters of g.ranges CTAs, one cluster per block of output columns;
+// CTA rank r of a cluster covers K range [r kr, min(K, (r + 1) kr)).
+template <int MR, bool B_KN, bool BF16>
+__global__ void __launch_bounds__(GV_THREADS, 1)
+    gemv_kernel(const __grid_constant__ CUtensorMap tmB, const GemvArgs g)
+{
+    constexpr int CW = B_KN ? KN_CW : NK_CW;
+    constexpr int KS = B_KN ? KN_KS : NK_KS;
+    extern __shared__ uint8_t gv_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(gv_raw) + 127) & ~static_cast<uintptr_t>(127));
+    const GvLayout L = gv_layout(MR, B_KN, g.kr, g.stages);
+    const uint16_t *ring = reinterpret_cast<const uint16_t *>(base);
+    float *As = reinterpret_cast<float *>(base + L.as);
+    float *part = reinterpret_cast<float *>(base + L.part);
+    float *red = reinterpret_cast<float *>(base + L.red);
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + L.bars);
+    uint64_t *empty = full + g.stages;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base + L.abort_off);
+
+    const int rank = (int)cluster_ctarank();
+    const int block = blockIdx.x / g.ranges;
+    const int k0 = rank * g.kr;
+    const int klen = g.K - k0 < g.kr ? g.K - k0 : g.kr;
+    const int nst = (klen + KS - 1) / KS;
+    const int n0 = block * CW;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < g.stages; ++i) {
+            mbar_init(smem_u32(&full[i]), 1);
+            mbar_init(smem_u32(&empty[i]), GV_WARPS);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tmB);
+    }
+    __syncthreads();
+    // B and op(A) may come from the kernel before this one on the stream.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const int ns = g.stages;
+            int issued = 0;
+            for (int s = 0; s < nst; ++s) {
+                const int slot = s % ns;
+                if (s >= ns && !wait_bounded(smem_u32(&empty[slot]), (uint32_t)(((s / ns) - 1) & 1),
+                                             abort_flag, g.err))
+                    break;
+                const uint32_t fb = smem_u32(&full[slot]);
+                mbar_arrive_expect_tx(fb, GV_STAGE_BYTES);
+                const uint32_t dst = smem_u32(ring + slot * GV_STAGE_ELEMS);
+                if (B_KN)
+                    tma_load_2d(dst, &tmB, fb, n0, k0 + s * KS);
+                else
+                    tma_load_2d(dst, &tmB, fb, k0 + s * KS, n0);
+                issued = s + 1;
+            }
+            // Boxes still in flight (only after an abort) land before the CTA
+            // leaves; after a normal run every one of these phases is complete.
+            for (int s = issued > ns ? issued - ns : 0; s < issued; ++s)
+                wait_bounded(smem_u32(&full[s % ns]), (uint32_t)((s / ns) & 1), abort_flag, g.err,
+                             false, DRAIN_LIMIT_NS);
+        }
+    } else {
+        const int ct = threadIdx.x - 32;
+        if (B_KN)
+            consume_kn<MR, BF16>(g, ring, full, empty, abort_flag, As, red, part, k0, klen, nst, ct);
+        else
+            consume_nk<MR, BF16>(g, ring, full, empty, abort_flag, As, part, k0, klen, nst, ct);
+    }
+
+    cluster_sync_all();     // every partial block of the cluster is written
+    if (rank == 0 && warp > 0) {
+        const uint32_t part_s = smem_u32(part);
+        for (int t = threadIdx.x - 32; t < MR * CW; t += GV_CONSUMERS) {
+            const int m = t / CW, n = n0 + (t - m * CW);
+            if (m < g.M && n < g.N) {
+                float sum = 0.0f;
+                for (int r = 0; r < g.ranges; ++r)
+                    sum += ld_shared_cluster_f32(mapa_shared(part_s + 4u * (uint32_t)t, (uint32_t)r));
+                float v = g.alpha * sum;
+                const long long off = (long long)m * g.ldd + n;
+                if (g.beta != 0.0f) v += g.beta * load_out(g.D, off, g.out_kind);
+                store_out(g.D, off, v, g.out_kind);
+            }
+        }
+    }
+    cluster_sync_all();     // no CTA leaves while CTA 0 still reads its partials
+}
+
+template <int MR, bool B_KN, bool BF16>
+cudaError_t launch_gemv_impl(const CUtensorMap &tmB, const GemvArgs &g, int col_blocks,
+                             cudaStream_t s)
+{
+    static std::atomic<unsigned long long> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    auto kernel = gemv_kernel<MR, B_KN, BF16>;
+    if (!(configured.load() & bit)) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 GV_MAX_SMEM);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(col_blocks * g.ranges));
+    cfg.blockDim = dim3(GV_THREADS);
+    cfg.dynamicSmemBytes = (size_t)gv_layout(MR, B_KN, g.kr, g.stages).total;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)g.ranges;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kernel, tmB, g);
+}
+
+template <int MR>
+cudaError_t launch_gemv_mr(const CUtensorMap &tmB, const GemvArgs &g, bool b_kn, bool bf16,
+                           int col_blocks, cudaStream_t s)
+{
+    if (b_kn)
+        return bf16 ? launch_gemv_impl<MR, true, true>(tmB, g, col_blocks, s)
+                    : launch_gemv_impl<MR, true, false>(tmB, g, col_blocks, s);
+    return bf16 ? launch_gemv_impl<MR, false, true>(tmB, g, col_blocks, s)
+                : launch_gemv_impl<MR, false, false>(tmB, g, col_blocks, s);
+}
+
+}  // namespace
+
+int gemv_cols_per_block(bool b_kn) { return b_kn ? KN_CW : NK_CW; }
+int gemv_k_per_stage(bool b_kn) { return b_kn ? KN_KS : NK_KS; }
+int gemv_box_inner(bool b_kn) { return b_kn ? KN_CW : NK_KS; }
+int gemv_box_outer(bool b_kn) { return b_kn ? KN_KS : NK_CW; }
+
+int gemv_smem_bytes(int mr, bool b_kn, int kr, int stages)
+{
+    return gv_layout(mr, b_kn, kr, stages).total;
+}
+
+cudaError_t launch_gemv(const CUtensorMap &tmB, const GemvArgs &g, int mr, bool b_kn, bool bf16,
+                        int col_blocks, cudaStream_t s)
+{
+    switch (mr) {
+    case 1: return launch_gemv_mr<1>(tmB, g, b_kn, bf16, col_blocks, s);
+    case 2: return launch_gemv_mr<2>(tmB, g, b_kn, bf16, col_blocks, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace swg

@@ -57,4 +57,34 @@ int max_active_pairs_splitk(int bn, int sms);
 // launched as a programmatic dependent of the split-K GEMM on the same stream.
 cudaError_t launch_splitk_reduce(const TileParams &p, int sms, cudaStream_t s);
 
+// Few-rows product on the FP32 pipes (k_gemv.cu): D = alpha * op(A) op(B) +
+// beta * C for M <= 2, one launch; B streams through shared memory by TMA in
+// boxes (tensor map tmB: B stored N x K read as {K, N} in boxes of
+// gemv_box_inner x gemv_box_outer, or B stored K x N read as {N, K}); the K
+// ranges of a block of output columns are reduced inside a cluster.
+struct GemvArgs {
+    const uint16_t *A;           // 16-bit op(A) storage
+    long long lda;
+    int a_t;                     // 1: A stored K x M (op T)
+    void *D;                     // output (also C when beta != 0)
+    long long ldd;
+    int M, N, K;
+    int kr;                      // K elements per range, a multiple of gemv_k_per_stage
+    int ranges;                  // K ranges = CTAs per cluster (1..8)
+    int stages;                  // shared-memory ring depth (boxes of 16 KB)
+    float alpha, beta;
+    int out_kind;                // OutKind
+    int *err;                    // device error word
+};
+constexpr int GV_MAX_SMEM = 232448;          // 227 KB, the per-CTA maximum
+int gemv_cols_per_block(bool b_kn);          // output columns per cluster
+int gemv_k_per_stage(bool b_kn);             // K elements per box
+int gemv_box_inner(bool b_kn);               // box extent along the contiguous dimension
+int gemv_box_outer(bool b_kn);
+int gemv_smem_bytes(int mr, bool b_kn, int kr, int stages);
+// mr: 1 or 2 (rows the kernel computes; M <= mr); b_kn: B stored K x N
+// (op N); col_blocks: cdiv(N, gemv_cols_per_block(b_kn)).
+cudaError_t launch_gemv(const CUtensorMap &tmB, const GemvArgs &g, int mr, bool b_kn, bool bf16,
+                        int col_blocks, cudaStream_t s);
+
 }  // namespace swg
