@@ -135,7 +135,7 @@ __device__ __forceinline__ void stage_a(float *As, const GemvArgs &g, int k0, in
                 const int m = q / per_row, kk = (q - m * per_row) * 8;
                 float f[8];
                 widen8<BF16>(v[u], f);
-                if (M_MAJOR) {
+                if (M_MAJOR || MR == 1) {             // one row: the two layouts agree
                     float4 *d = reinterpret_cast<float4 *>(As + m * kr + kk);
                     d[0] = make_float4(f[0], f[1], f[2], f[3]);
                     d[1] = make_float4(f[4], f[5], f[6], f[7]);
