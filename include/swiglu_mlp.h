@@ -60,8 +60,9 @@ typedef enum { SWG_OP_N = 0, SWG_OP_T = 1 } swg_op;
  * K-contiguous), and lda and ldb multiples of 16.  Split-K exists for them
  * only with M <= 64 (few rows, e.g. decode): such calls run the transposed
  * product with the K loop split, automatically or with split_k > 1, and
- * reduce the partials in split order; split_k > 1 with M > 64 and other op
- * combinations return SWG_ERR_UNSUPPORTED. */
+ * reduce the partials in split order (one or two rows with split_k = 0 run
+ * the one-launch FP32-pipe kernel described under gemm); split_k > 1 with
+ * M > 64 and other op combinations return SWG_ERR_UNSUPPORTED. */
 typedef enum {
     SWG_F16_F32OUT = 0,   /* A, B binary16;  C, D binary32 */
     SWG_BF16 = 1,         /* A, B, C, D bfloat16            */
@@ -104,8 +105,8 @@ typedef enum {
  *                   allocated (queued work or a captured graph may still use
  *                   them) until swg_shutdown() frees them all.  Two kernels are
  *                   launched: the GEMM and a dependent reduction.
- *   One or two rows M <= 2 with 16-bit A and B (decode of one or two tokens)
- *                   K <= 8 * 8192 / M and N <= 2^30: one kernel on the FP32 pipes
+ *   One or two rows M <= 2 with 16-bit or e4m3 A and B (decode of one or two
+ *                   tokens), K <= 8 * 8192 / M and N <= 2^30: one kernel on the FP32 pipes
  *                   instead ("GEMM o Coração Matemático", §14: the product
  *                   streams op(B) once and is bound by memory).  Its K split
  *                   is summed inside the kernel, again in a fixed order; it

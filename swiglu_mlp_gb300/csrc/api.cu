@@ -518,31 +518,36 @@ bool gemv_disabled()
     return v && v[0] == '0';
 }
 
-// Row-major matrix of `outer` rows x `inner` contiguous 16-bit elements, read
-// without swizzle in boxes of box_inner x box_outer; past the edges reads zero.
-bool make_tmap_plain(CUtensorMap *m, const void *ptr, bool bf16, int64_t inner, int64_t outer,
+// Row-major matrix of `outer` rows x `inner` contiguous elements (in_kind 0
+// binary16, 1 bfloat16, 2 e4m3 as bytes), read without swizzle in boxes of
+// box_inner x box_outer; past the edges reads zero.
+bool make_tmap_plain(CUtensorMap *m, const void *ptr, int in_kind, int64_t inner, int64_t outer,
                      int64_t ld, int box_inner, int box_outer)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
+    const int esz = in_kind == 2 ? 1 : 2;
+    const CUtensorMapDataType dt = in_kind == 2   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : in_kind == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
-    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * esz)};
     cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
     cuuint32_t estr[2] = {1u, 1u};
-    return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-              const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return fn(m, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int gemv_path(DeviceState *d, const TypeInfo &ti, int transA, int transB, int64_t M, int64_t N,
-              int64_t K, float alpha, const void *A, int64_t lda, const void *B, int64_t ldb,
-              float beta, void *C, int64_t ldc, cudaStream_t s)
+// in_kind: 0 binary16, 1 bfloat16, 2 e4m3 (A stored M x K, B stored N x K).
+int gemv_path(DeviceState *d, int in_kind, int out_kind, int transA, int transB, int64_t M,
+              int64_t N, int64_t K, float alpha, const void *A, int64_t lda, const void *B,
+              int64_t ldb, float beta, void *C, int64_t ldc, cudaStream_t s)
 {
     const int mr = M <= 1 ? 1 : 2;
     const bool b_kn = transB == SWG_OP_N;
     const int64_t ks = swg::gemv_k_per_stage(b_kn);
-    const int64_t blocks = cdiv(N, swg::gemv_cols_per_block(b_kn));
+    const int64_t blocks = cdiv(N, swg::gemv_cols_per_block(b_kn, in_kind));
     const int64_t kr_max = kGemvSlice / mr;          // a multiple of both box lengths
     const int64_t s_min = cdiv(K, kr_max);
     if (s_min > 8 || N > (int64_t(1) << 30)) return SWG_ERR_UNSUPPORTED;
@@ -552,20 +557,20 @@ int gemv_path(DeviceState *d, const TypeInfo &ti, int transA, int transB, int64_
     const int64_t kr = cdiv(cdiv(K, ranges), ks) * ks;
     ranges = cdiv(K, kr);
     const int64_t budget = blocks * ranges > d->sms ? 115712 : swg::GV_MAX_SMEM;
-    const int64_t fixed = swg::gemv_smem_bytes(mr, b_kn, (int)kr, 0);
-    const int64_t per_stage = swg::gemv_smem_bytes(mr, b_kn, (int)kr, 1) - fixed;
+    const int64_t fixed = swg::gemv_smem_bytes(mr, b_kn, in_kind, (int)kr, 0);
+    const int64_t per_stage = swg::gemv_smem_bytes(mr, b_kn, in_kind, (int)kr, 1) - fixed;
     const int64_t stages = std::min<int64_t>({12, cdiv(kr, ks), (budget - fixed) / per_stage});
     if (stages < 1) return SWG_ERR_UNSUPPORTED;
 
     CUtensorMap tm;
-    const bool ok = b_kn ? make_tmap_plain(&tm, B, ti.in_bf16, N, K, ldb, swg::gemv_box_inner(true),
-                                           swg::gemv_box_outer(true))
-                         : make_tmap_plain(&tm, B, ti.in_bf16, K, N, ldb, swg::gemv_box_inner(false),
-                                           swg::gemv_box_outer(false));
+    const bool ok = b_kn ? make_tmap_plain(&tm, B, in_kind, N, K, ldb, swg::gemv_box_inner(true),
+                                           swg::gemv_box_outer(true, in_kind))
+                         : make_tmap_plain(&tm, B, in_kind, K, N, ldb, swg::gemv_box_inner(false),
+                                           swg::gemv_box_outer(false, in_kind));
     if (!ok) return SWG_ERR_UNSUPPORTED;
 
     swg::GemvArgs g{};
-    g.A = static_cast<const uint16_t *>(A);
+    g.A = A;
     g.lda = lda;
     g.a_t = transA == SWG_OP_T;
     g.D = C;
@@ -578,9 +583,9 @@ int gemv_path(DeviceState *d, const TypeInfo &ti, int transA, int transB, int64_
     g.stages = (int)stages;
     g.alpha = alpha;
     g.beta = beta;
-    g.out_kind = ti.out_kind;
+    g.out_kind = out_kind;
     g.err = d->err;
-    if (swg::launch_gemv(tm, g, mr, b_kn, ti.in_bf16, (int)blocks, s) != cudaSuccess)
+    if (swg::launch_gemv(tm, g, mr, b_kn, in_kind, (int)blocks, s) != cudaSuccess)
         return cuda_fail();
     g_launches++;
     return SWG_OK;
@@ -721,6 +726,13 @@ static int gemm_fp8(int transA, int transB, int64_t M, int64_t N, int64_t K, flo
         g_launches++;
         return launch_status();
     }
+    // One or two rows with an automatic split: the FP32-pipe kernel, as for
+    // 16-bit inputs (8-bit weights halve the bytes it streams).
+    if (split_k == 0 && M <= kGemvMaxRows && !gemv_disabled()) {
+        const int rc = gemv_path(d, 2, out_kind, transA, transB, M, N, K, alpha, A, lda, B, ldb,
+                                 beta, C, ldc, s);
+        if (rc != SWG_ERR_UNSUPPORTED) return rc;
+    }
     // Few rows (decode): the transposed product with the K loop split, as
     // for 16-bit inputs, unless the caller asked for no split.
     if (M <= 64 && split_k != 1) {
@@ -810,8 +822,8 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
     }
 
     if (split_k == 0 && M <= kGemvMaxRows && !gemv_disabled()) {
-        const int rc = gemv_path(d, ti, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C,
-                                 ldc, s);
+        const int rc = gemv_path(d, ti.in_bf16 ? 1 : 0, ti.out_kind, transA, transB, M, N, K,
+                                 alpha, A, lda, B, ldb, beta, C, ldc, s);
         if (rc != SWG_ERR_UNSUPPORTED) return rc;
     }
 

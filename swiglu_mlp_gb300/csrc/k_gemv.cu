@@ -36,8 +36,10 @@
 // waits (bounded again) for its boxes in flight, and the kernel returns.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "launch_impl.cuh"
 
@@ -48,52 +50,74 @@ constexpr int GV_CONSUMERS = 256;                   // 8 consumer warps
 constexpr int GV_WARPS = GV_CONSUMERS / 32;
 constexpr int GV_THREADS = GV_CONSUMERS + 32;       // + the producer warp
 constexpr int GV_STAGE_BYTES = 16384;
-constexpr int GV_STAGE_ELEMS = GV_STAGE_BYTES / 2;
-constexpr int NK_CW = 32;                           // B stored N x K: rows per box
-constexpr int NK_KS = 256;                          //   K elements per box
-constexpr int NK_RPW = NK_CW / GV_WARPS;            //   rows per consumer warp (4)
+constexpr int NK_KS = 256;                          // B stored N x K: K elements per box
 constexpr int KN_CW = 64;                           // B stored K x N: columns per box
 constexpr int KN_KS = 128;                          //   K rows per box
 constexpr int KN_RPT = KN_KS / 32;                  //   rows per thread and box (4)
 
-template <bool BF16>
-__device__ __forceinline__ float widen1(uint32_t bits16)
+// Input kinds: IK 0 = binary16, 1 = bfloat16, 2 = e4m3 (8-bit).
+template <int IK> using Elem = std::conditional_t<IK == 2, uint8_t, uint16_t>;
+template <int IK> using Vec8 = std::conditional_t<IK == 2, uint2, uint4>;   // 8 elements
+template <int IK> __host__ __device__ constexpr int esize() { return IK == 2 ? 1 : 2; }
+// B stored N x K: rows (output columns) per 16 KB box of NK_KS elements each.
+__host__ __device__ constexpr int nk_rows(int esz) { return GV_STAGE_BYTES / (NK_KS * esz); }
+
+template <int IK>
+__device__ __forceinline__ float widen1(uint32_t bits)
 {
-    if (BF16) return __uint_as_float(bits16 << 16);   // bfloat16 = top half of binary32
-    return __half2float(__ushort_as_half((unsigned short)bits16));
+    if constexpr (IK == 1) return __uint_as_float(bits << 16);   // bfloat16 = top half of binary32
+    if constexpr (IK == 0) return __half2float(__ushort_as_half((unsigned short)bits));
+    return __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)bits, __NV_E4M3)));
 }
 
-// The eight 16-bit values of one 16-byte load, widened to FP32 (exact).
-template <bool BF16>
-__device__ __forceinline__ void widen8(const uint4 &v, float (&f)[8])
+// The eight values of one 8-element load, widened to FP32 (exact: e4m3 and
+// binary16 both widen to binary16 without rounding, bfloat16 by a shift).
+template <int IK>
+__device__ __forceinline__ void widen8(const Vec8<IK> &v, float (&f)[8])
 {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if constexpr (IK == 2) {
+        const uint32_t w[2] = {v.x, v.y};
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-        if (BF16) {
-            f[2 * h] = __uint_as_float(w[h] << 16);
-            f[2 * h + 1] = __uint_as_float(w[h] & 0xffff0000u);
-        } else {
-            const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&w[h]));
+        for (int h = 0; h < 4; ++h) {
+            const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)(w[h >> 1] >> (16 * (h & 1)));
+            const __half2 t2 = __half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3));
+            const float2 t = __half22float2(t2);
             f[2 * h] = t.x;
             f[2 * h + 1] = t.y;
+        }
+    } else {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            if constexpr (IK == 1) {
+                f[2 * h] = __uint_as_float(w[h] << 16);
+                f[2 * h + 1] = __uint_as_float(w[h] & 0xffff0000u);
+            } else {
+                const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&w[h]));
+                f[2 * h] = t.x;
+                f[2 * h + 1] = t.y;
+            }
         }
     }
 }
 
-__device__ __forceinline__ uint4 ld16(const uint16_t *p)
+template <int IK>
+__device__ __forceinline__ Vec8<IK> ld8(const Elem<IK> *p)
 {
-    return __ldg(reinterpret_cast<const uint4 *>(p));
+    return __ldg(reinterpret_cast<const Vec8<IK> *>(p));
 }
 
-// Up to eight 16-bit values at p (cnt of them, the rest zero) as one uint4.
-__device__ __forceinline__ uint4 ld_partial(const uint16_t *p, int cnt)
+// Up to eight elements at p (cnt of them, the rest zero) as one 8-element vector.
+template <int IK>
+__device__ __forceinline__ Vec8<IK> ld_partial(const Elem<IK> *p, int cnt)
 {
+    constexpr int B = 8 * esize<IK>();                 // bits per element
     uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
     for (int e = 0; e < 8; ++e)
-        if (e < cnt) w[e >> 1] |= (uint32_t)__ldg(p + e) << (16 * (e & 1));
-    return make_uint4(w[0], w[1], w[2], w[3]);
+        if (e < cnt) w[(e * B) >> 5] |= (uint32_t)__ldg(p + e) << ((e * B) & 31);
+    if constexpr (IK == 2) return make_uint2(w[0], w[1]);
+    else return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr)
@@ -105,27 +129,29 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr)
 
 // op(A)[m][k0 + kk] for m < MR, kk < kr, widened to FP32 into As, zero where
 // m >= M or kk >= klen.  M_MAJOR: As[m * kr + kk]; else As[kk * MR + m].
-// A stored M x K (a_t = 0) is read 8 elements per 16-byte load; A stored
-// K x M (a_t = 1) one element at a time.
-template <int MR, bool BF16, bool M_MAJOR>
+// A stored M x K (a_t = 0) is read 8 elements per load; A stored K x M
+// (a_t = 1, 16-bit inputs only) one element at a time.  Runs on the 256
+// consumer threads (ct = 0..255).
+template <int MR, int IK, bool M_MAJOR>
 __device__ __forceinline__ void stage_a(float *As, const GemvArgs &g, int k0, int klen, int ct)
 {
+    const Elem<IK> *A = static_cast<const Elem<IK> *>(g.A);
     const int kr = g.kr;
     if (!g.a_t) {
         const int per_row = kr >> 3;            // 8-element groups per row
         const int groups = MR * per_row;
         constexpr int U = 4;
         for (int g0 = ct; g0 < groups; g0 += U * GV_CONSUMERS) {
-            uint4 v[U];
+            Vec8<IK> v[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int q = g0 + u * GV_CONSUMERS;
                 const int m = q / per_row, kk = (q - m * per_row) * 8;
                 const int cnt = klen - kk;
-                v[u] = make_uint4(0u, 0u, 0u, 0u);
+                v[u] = Vec8<IK>{};
                 if (q < groups && m < g.M && cnt > 0) {
-                    const uint16_t *p = g.A + (long long)m * g.lda + k0 + kk;
-                    v[u] = cnt >= 8 ? ld16(p) : ld_partial(p, cnt);
+                    const Elem<IK> *p = A + (long long)m * g.lda + k0 + kk;
+                    v[u] = cnt >= 8 ? ld8<IK>(p) : ld_partial<IK>(p, cnt);
                 }
             }
 #pragma unroll
@@ -134,7 +160,7 @@ __device__ __forceinline__ void stage_a(float *As, const GemvArgs &g, int k0, in
                 if (q >= groups) break;
                 const int m = q / per_row, kk = (q - m * per_row) * 8;
                 float f[8];
-                widen8<BF16>(v[u], f);
+                widen8<IK>(v[u], f);
                 if (M_MAJOR || MR == 1) {             // one row: the two layouts agree
                     float4 *d = reinterpret_cast<float4 *>(As + m * kr + kk);
                     d[0] = make_float4(f[0], f[1], f[2], f[3]);
@@ -158,32 +184,32 @@ __device__ __forceinline__ void stage_a(float *As, const GemvArgs &g, int k0, in
                 else { kk = i / MR; m = i - kk * MR; }
                 v[u] = 0u;
                 if (i < total && m < g.M && kk < klen)
-                    v[u] = __ldg(g.A + (long long)(k0 + kk) * g.lda + m);
+                    v[u] = __ldg(A + (long long)(k0 + kk) * g.lda + m);
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int i = i0 + u * GV_CONSUMERS;
-                if (i < total) As[i] = widen1<BF16>(v[u]);
+                if (i < total) As[i] = widen1<IK>(v[u]);
             }
         }
     }
 }
 
-
 // Shared memory of one CTA, from a 128-byte aligned base: the ring of boxes,
 // the op(A) slice (MR x kr FP32), this CTA's partial block (MR x CW FP32),
 // the per-warp sums of the K x N layout (8 x MR x 64 FP32), the stage
-// barriers full[ns] and empty[ns], and the abort flag.
+// barriers full[ns] and empty[ns], and the abort flag.  cw: output columns
+// per CTA (gemv_cols_per_block).
 struct GvLayout {
     int as, part, red, bars, abort_off, total;
 };
 
-__host__ __device__ inline GvLayout gv_layout(int mr, bool b_kn, int kr, int ns)
+__host__ __device__ inline GvLayout gv_layout(int mr, bool b_kn, int cw, int kr, int ns)
 {
     GvLayout L;
     L.as = ns * GV_STAGE_BYTES;
     L.part = L.as + 4 * mr * kr;
-    L.red = L.part + 4 * mr * (b_kn ? KN_CW : NK_CW);
+    L.red = L.part + 4 * mr * cw;
     L.bars = L.red + (b_kn ? 4 * GV_WARPS * mr * KN_CW : 0);
     L.abort_off = L.bars + 16 * ns;
     L.total = L.abort_off + 16 + 128;                  // + alignment slack
@@ -199,30 +225,35 @@ __device__ __forceinline__ bool stage_ready(const uint64_t *full, int s, int ns,
     return __all_sync(0xffffffffu, got);
 }
 
-// B stored N x K.  Box s of the range holds rows n0..n0+31, K elements
-// k0 + 256 s .. + 255 (row-major, 512 bytes a row).
-template <int MR, bool BF16>
-__device__ __forceinline__ void consume_nk(const GemvArgs &g, const uint16_t *ring,
+// B stored N x K.  Box s of the range holds rows n0 .. n0 + ROWS - 1 (32 for
+// 16-bit, 64 for 8-bit elements), K elements k0 + 256 s .. + 255, row-major.
+// Consumer warp w owns rows w * RPW .. + RPW - 1; lane l takes elements
+// 8l .. 8l + 7 of each.
+template <int MR, int IK>
+__device__ __forceinline__ void consume_nk(const GemvArgs &g, const uint8_t *ring,
                                            const uint64_t *full, uint64_t *empty,
                                            volatile int *abort_flag, float *As, float *part,
                                            int k0, int klen, int nst, int ct)
 {
-    stage_a<MR, BF16, true>(As, g, k0, klen, ct);
+    constexpr int ROWS = nk_rows(esize<IK>());
+    constexpr int RPW = ROWS / GV_WARPS;
+    stage_a<MR, IK, true>(As, g, k0, klen, ct);
     named_bar_sync(1, GV_CONSUMERS);
     const int cw = ct >> 5, lane = ct & 31;
-    float acc[MR][NK_RPW];
+    float acc[MR][RPW];
 #pragma unroll
     for (int m = 0; m < MR; ++m)
 #pragma unroll
-        for (int r = 0; r < NK_RPW; ++r) acc[m][r] = 0.0f;
+        for (int r = 0; r < RPW; ++r) acc[m][r] = 0.0f;
 
     for (int s = 0; s < nst; ++s) {
         if (!stage_ready(full, s, g.stages, abort_flag, g.err)) break;
         const int slot = s % g.stages;
-        const uint16_t *st = ring + slot * GV_STAGE_ELEMS + cw * NK_RPW * NK_KS + 8 * lane;
-        uint4 bv[NK_RPW];
+        const Elem<IK> *st = reinterpret_cast<const Elem<IK> *>(ring + slot * GV_STAGE_BYTES) +
+                             cw * RPW * NK_KS + 8 * lane;
+        Vec8<IK> bv[RPW];
 #pragma unroll
-        for (int r = 0; r < NK_RPW; ++r) bv[r] = *reinterpret_cast<const uint4 *>(st + r * NK_KS);
+        for (int r = 0; r < RPW; ++r) bv[r] = *reinterpret_cast<const Vec8<IK> *>(st + r * NK_KS);
         float a[MR][8];
 #pragma unroll
         for (int m = 0; m < MR; ++m) {
@@ -233,9 +264,9 @@ __device__ __forceinline__ void consume_nk(const GemvArgs &g, const uint16_t *ri
             a[m][4] = a1.x; a[m][5] = a1.y; a[m][6] = a1.z; a[m][7] = a1.w;
         }
 #pragma unroll
-        for (int r = 0; r < NK_RPW; ++r) {
+        for (int r = 0; r < RPW; ++r) {
             float b[8];
-            widen8<BF16>(bv[r], b);
+            widen8<IK>(bv[r], b);
 #pragma unroll
             for (int m = 0; m < MR; ++m)
 #pragma unroll
@@ -247,23 +278,24 @@ __device__ __forceinline__ void consume_nk(const GemvArgs &g, const uint16_t *ri
 #pragma unroll
     for (int m = 0; m < MR; ++m)
 #pragma unroll
-        for (int r = 0; r < NK_RPW; ++r) {
+        for (int r = 0; r < RPW; ++r) {
             float v = acc[m][r];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-            if (lane == 0) part[m * NK_CW + cw * NK_RPW + r] = v;
+            if (lane == 0) part[m * ROWS + cw * RPW + r] = v;
         }
 }
 
 // B stored K x N.  Box s of the range holds K rows k0 + 128 s .. + 127,
 // columns n0..n0+63 (row-major, 128 bytes a row).
-template <int MR, bool BF16>
-__device__ __forceinline__ void consume_kn(const GemvArgs &g, const uint16_t *ring,
+template <int MR, int IK>
+__device__ __forceinline__ void consume_kn(const GemvArgs &g, const uint8_t *ring,
                                            const uint64_t *full, uint64_t *empty,
                                            volatile int *abort_flag, float *As, float *red,
                                            float *part, int k0, int klen, int nst, int ct)
 {
-    stage_a<MR, BF16, false>(As, g, k0, klen, ct);
+    static_assert(IK != 2, "8-bit B is read N x K only");
+    stage_a<MR, IK, false>(As, g, k0, klen, ct);
     named_bar_sync(1, GV_CONSUMERS);
     const int cx = ct & 7, rl = ct >> 3;               // 8 column threads x 32 row lanes
     const int cw = ct >> 5, lane = ct & 31;
@@ -276,7 +308,7 @@ __device__ __forceinline__ void consume_kn(const GemvArgs &g, const uint16_t *ri
     for (int s = 0; s < nst; ++s) {
         if (!stage_ready(full, s, g.stages, abort_flag, g.err)) break;
         const int slot = s % g.stages;
-        const uint16_t *st = ring + slot * GV_STAGE_ELEMS + 8 * cx;
+        const uint16_t *st = reinterpret_cast<const uint16_t *>(ring + slot * GV_STAGE_BYTES) + 8 * cx;
         uint4 bv[KN_RPT];
 #pragma unroll
         for (int i = 0; i < KN_RPT; ++i)
@@ -292,7 +324,7 @@ __device__ __forceinline__ void consume_kn(const GemvArgs &g, const uint16_t *ri
                 a[0] = As[kk];
             }
             float b[8];
-            widen8<BF16>(bv[i], b);
+            widen8<IK>(bv[i], b);
 #pragma unroll
             for (int m = 0; m < MR; ++m)
 #pragma unroll
@@ -323,17 +355,17 @@ __device__ __forceinline__ void consume_kn(const GemvArgs &g, const uint16_t *ri
 
 // Grid: clusters of g.ranges CTAs, one cluster per block of output columns;
 // CTA rank r of a cluster covers K range [r kr, min(K, (r + 1) kr)).
-template <int MR, bool B_KN, bool BF16>
+template <int MR, bool B_KN, int IK>
 __global__ void __launch_bounds__(GV_THREADS, 1)
     gemv_kernel(const __grid_constant__ CUtensorMap tmB, const GemvArgs g)
 {
-    constexpr int CW = B_KN ? KN_CW : NK_CW;
+    constexpr int CW = B_KN ? KN_CW : nk_rows(esize<IK>());
     constexpr int KS = B_KN ? KN_KS : NK_KS;
     extern __shared__ uint8_t gv_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(gv_raw) + 127) & ~static_cast<uintptr_t>(127));
-    const GvLayout L = gv_layout(MR, B_KN, g.kr, g.stages);
-    const uint16_t *ring = reinterpret_cast<const uint16_t *>(base);
+    const GvLayout L = gv_layout(MR, B_KN, CW, g.kr, g.stages);
+    const uint8_t *ring = base;
     float *As = reinterpret_cast<float *>(base + L.as);
     float *part = reinterpret_cast<float *>(base + L.part);
     float *red = reinterpret_cast<float *>(base + L.red);
@@ -374,7 +406,7 @@ __global__ void __launch_bounds__(GV_THREADS, 1)
                     break;
                 const uint32_t fb = smem_u32(&full[slot]);
                 mbar_arrive_expect_tx(fb, GV_STAGE_BYTES);
-                const uint32_t dst = smem_u32(ring + slot * GV_STAGE_ELEMS);
+                const uint32_t dst = smem_u32(ring + slot * GV_STAGE_BYTES);
                 if (B_KN)
                     tma_load_2d(dst, &tmB, fb, n0, k0 + s * KS);
                 else
@@ -389,10 +421,10 @@ __global__ void __launch_bounds__(GV_THREADS, 1)
         }
     } else {
         const int ct = threadIdx.x - 32;
-        if (B_KN)
-            consume_kn<MR, BF16>(g, ring, full, empty, abort_flag, As, red, part, k0, klen, nst, ct);
+        if constexpr (B_KN)
+            consume_kn<MR, IK>(g, ring, full, empty, abort_flag, As, red, part, k0, klen, nst, ct);
         else
-            consume_nk<MR, BF16>(g, ring, full, empty, abort_flag, As, part, k0, klen, nst, ct);
+            consume_nk<MR, IK>(g, ring, full, empty, abort_flag, As, part, k0, klen, nst, ct);
     }
 
     cluster_sync_all();     // every partial block of the cluster is written
@@ -414,7 +446,7 @@ __global__ void __launch_bounds__(GV_THREADS, 1)
     cluster_sync_all();     // no CTA leaves while CTA 0 still reads its partials
 }
 
-template <int MR, bool B_KN, bool BF16>
+template <int MR, bool B_KN, int IK>
 cudaError_t launch_gemv_impl(const CUtensorMap &tmB, const GemvArgs &g, int col_blocks,
                              cudaStream_t s)
 {
@@ -423,17 +455,18 @@ cudaError_t launch_gemv_impl(const CUtensorMap &tmB, const GemvArgs &g, int col_
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
-    auto kernel = gemv_kernel<MR, B_KN, BF16>;
+    auto kernel = gemv_kernel<MR, B_KN, IK>;
     if (!(configured.load() & bit)) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  GV_MAX_SMEM);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
+    constexpr int CW = B_KN ? KN_CW : nk_rows(esize<IK>());
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(col_blocks * g.ranges));
     cfg.blockDim = dim3(GV_THREADS);
-    cfg.dynamicSmemBytes = (size_t)gv_layout(MR, B_KN, g.kr, g.stages).total;
+    cfg.dynamicSmemBytes = (size_t)gv_layout(MR, B_KN, CW, g.kr, g.stages).total;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -448,34 +481,39 @@ cudaError_t launch_gemv_impl(const CUtensorMap &tmB, const GemvArgs &g, int col_
 }
 
 template <int MR>
-cudaError_t launch_gemv_mr(const CUtensorMap &tmB, const GemvArgs &g, bool b_kn, bool bf16,
+cudaError_t launch_gemv_mr(const CUtensorMap &tmB, const GemvArgs &g, bool b_kn, int in_kind,
                            int col_blocks, cudaStream_t s)
 {
+    if (in_kind == 2)
+        return b_kn ? cudaErrorInvalidValue : launch_gemv_impl<MR, false, 2>(tmB, g, col_blocks, s);
     if (b_kn)
-        return bf16 ? launch_gemv_impl<MR, true, true>(tmB, g, col_blocks, s)
-                    : launch_gemv_impl<MR, true, false>(tmB, g, col_blocks, s);
-    return bf16 ? launch_gemv_impl<MR, false, true>(tmB, g, col_blocks, s)
-                : launch_gemv_impl<MR, false, false>(tmB, g, col_blocks, s);
+        return in_kind == 1 ? launch_gemv_impl<MR, true, 1>(tmB, g, col_blocks, s)
+                            : launch_gemv_impl<MR, true, 0>(tmB, g, col_blocks, s);
+    return in_kind == 1 ? launch_gemv_impl<MR, false, 1>(tmB, g, col_blocks, s)
+                        : launch_gemv_impl<MR, false, 0>(tmB, g, col_blocks, s);
 }
 
 }  // namespace
 
-int gemv_cols_per_block(bool b_kn) { return b_kn ? KN_CW : NK_CW; }
+int gemv_cols_per_block(bool b_kn, int in_kind)
+{
+    return b_kn ? KN_CW : nk_rows(in_kind == 2 ? 1 : 2);
+}
 int gemv_k_per_stage(bool b_kn) { return b_kn ? KN_KS : NK_KS; }
 int gemv_box_inner(bool b_kn) { return b_kn ? KN_CW : NK_KS; }
-int gemv_box_outer(bool b_kn) { return b_kn ? KN_KS : NK_CW; }
+int gemv_box_outer(bool b_kn, int in_kind) { return b_kn ? KN_KS : nk_rows(in_kind == 2 ? 1 : 2); }
 
-int gemv_smem_bytes(int mr, bool b_kn, int kr, int stages)
+int gemv_smem_bytes(int mr, bool b_kn, int in_kind, int kr, int stages)
 {
-    return gv_layout(mr, b_kn, kr, stages).total;
+    return gv_layout(mr, b_kn, gemv_cols_per_block(b_kn, in_kind), kr, stages).total;
 }
 
-cudaError_t launch_gemv(const CUtensorMap &tmB, const GemvArgs &g, int mr, bool b_kn, bool bf16,
+cudaError_t launch_gemv(const CUtensorMap &tmB, const GemvArgs &g, int mr, bool b_kn, int in_kind,
                         int col_blocks, cudaStream_t s)
 {
     switch (mr) {
-    case 1: return launch_gemv_mr<1>(tmB, g, b_kn, bf16, col_blocks, s);
-    case 2: return launch_gemv_mr<2>(tmB, g, b_kn, bf16, col_blocks, s);
+    case 1: return launch_gemv_mr<1>(tmB, g, b_kn, in_kind, col_blocks, s);
+    case 2: return launch_gemv_mr<2>(tmB, g, b_kn, in_kind, col_blocks, s);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -62,10 +62,11 @@ cudaError_t launch_splitk_reduce(const TileParams &p, int sms, cudaStream_t s);
 // boxes (tensor map tmB: B stored N x K read as {K, N} in boxes of
 // gemv_box_inner x gemv_box_outer, or B stored K x N read as {N, K}); the K
 // ranges of a block of output columns are reduced inside a cluster.
+// in_kind: 0 = binary16, 1 = bfloat16, 2 = e4m3 (B stored N x K only).
 struct GemvArgs {
-    const uint16_t *A;           // 16-bit op(A) storage
+    const void *A;               // op(A) storage (elements of in_kind)
     long long lda;
-    int a_t;                     // 1: A stored K x M (op T)
+    int a_t;                     // 1: A stored K x M (op T; 16-bit only)
     void *D;                     // output (also C when beta != 0)
     long long ldd;
     int M, N, K;
@@ -77,14 +78,14 @@ struct GemvArgs {
     int *err;                    // device error word
 };
 constexpr int GV_MAX_SMEM = 232448;          // 227 KB, the per-CTA maximum
-int gemv_cols_per_block(bool b_kn);          // output columns per cluster
-int gemv_k_per_stage(bool b_kn);             // K elements per box
-int gemv_box_inner(bool b_kn);               // box extent along the contiguous dimension
-int gemv_box_outer(bool b_kn);
-int gemv_smem_bytes(int mr, bool b_kn, int kr, int stages);
+int gemv_cols_per_block(bool b_kn, int in_kind);   // output columns per cluster
+int gemv_k_per_stage(bool b_kn);                   // K elements per box
+int gemv_box_inner(bool b_kn);                     // box extent along the contiguous dimension
+int gemv_box_outer(bool b_kn, int in_kind);
+int gemv_smem_bytes(int mr, bool b_kn, int in_kind, int kr, int stages);
 // mr: 1 or 2 (rows the kernel computes; M <= mr); b_kn: B stored K x N
-// (op N); col_blocks: cdiv(N, gemv_cols_per_block(b_kn)).
-cudaError_t launch_gemv(const CUtensorMap &tmB, const GemvArgs &g, int mr, bool b_kn, bool bf16,
+// (op N); col_blocks: cdiv(N, gemv_cols_per_block(b_kn, in_kind)).
+cudaError_t launch_gemv(const CUtensorMap &tmB, const GemvArgs &g, int mr, bool b_kn, int in_kind,
                         int col_blocks, cudaStream_t s);
 
 }  // namespace swg

@@ -2,10 +2,9 @@
 shared memory by TMA, the K ranges of a block of output columns reduced
 inside a thread-block cluster in rank order.
 
-gemm / gemm_ex with split_k = 0 take this path for 16-bit inputs when M <= 2
-and K fits in 8 ranges of the op(A) slice a CTA stages (8192 / rows elements);
-more rows, larger K, explicit split_k and e4m3 inputs keep the tensor-core
-path.  Every output is checked against the FP64 oracle ("GEMM o Coração
+gemm / gemm_ex with split_k = 0 take this path for 16-bit and e4m3 inputs when
+M <= 2 and K fits in 8 ranges of the op(A) slice a CTA stages (8192 / rows
+elements); more rows, larger K and explicit split_k keep the tensor-core path.  Every output is checked against the FP64 oracle ("GEMM o Coração
 Matemático", §1: D_ij = alpha sum_p op(A)_ip op(B)_pj + beta C_ij).  Storage
 padding carries a large fill value, so a read past a row shows in the result.
 """
@@ -198,3 +197,60 @@ def test_chained_calls_on_one_stream():
     check_half(to_f64(y1_host), oracle.gemm(0, 1, 1, N1, K1, 1.0, x, K1, W1, K1, 0.0), "y1")
     check_half(to_f64(y2.cpu()), oracle.gemm(0, 1, 1, N2, N1, 1.0, y1_host, N1, W2, N1, 0.0),
                "y2")
+
+
+def _e4m3_padded(rows, cols, ld, g, std=1.0, fill=256.0):
+    """rows x ld e4m3 storage (values exact in e4m3) holding N(0, std) values
+    rounded to e4m3 in its first cols columns and `fill` after them."""
+    t = torch.full((rows, ld), fill, dtype=torch.float32)
+    t[:, :cols] = (torch.randn(rows, cols, generator=g) * std).to(torch.float8_e4m3fn).float()
+    return t.to(torch.float8_e4m3fn)
+
+
+@pytest.mark.parametrize("M", [1, 2])
+@pytest.mark.parametrize("N,K", [(7, 16), (520, 1000), (600, 4100)])
+def test_e4m3_weights_ragged(M, N, K):
+    """8-bit operands (A stored M x K, B stored N x K, the e4m3 contract): the
+    same one-launch kernel with 64-row boxes; per-tensor scales folded into
+    alpha; ragged N and K, beta != 0 with a bf16 C."""
+    g = synth.generator(500 + M + N)
+    ld = round_up(K, 16)
+    A = _e4m3_padded(M, K, ld, g)
+    B = _e4m3_padded(N, K, ld, g, std=0.5)
+    ldc = round_up(N, 8)
+    C = padded(synth.normal((M, N), g), ldc, 3.0)
+    out, launches = _run(0, 1, M, N, K, 1.0 / 32, A, ld, B, ld, 0.5, C, ldc, swg.E4M3_BF16OUT)
+    assert launches == 1
+    assert torch.equal(out[:, N:], C[:, N:])
+    yhat = oracle.gemm(0, 1, M, N, K, 1.0 / 32, A, ld, B, ld, 0.5, C, ldc, in_type="e4m3")
+    check_half(to_f64(out[:, :N]), yhat, f"e4m3 gemv M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("M,K", [(1, 65536), (2, 32768)])
+def test_e4m3_longest_k(M, K):
+    N = 200
+    g = synth.generator(510 + M)
+    A = _e4m3_padded(M, K, K, g)
+    B = _e4m3_padded(N, K, K, g, std=0.25)
+    C = torch.zeros((M, N), dtype=torch.float32)
+    out, launches = _run(0, 1, M, N, K, 0.5, A, K, B, K, 0.0, C, N, swg.E4M3_F32OUT)
+    assert launches == 1
+    yhat = oracle.gemm(0, 1, M, N, K, 0.5, A, K, B, K, 0.0, in_type="e4m3", c_type="f32")
+    check_f32(to_f64(out), yhat, K, f"e4m3 gemv M={M} K={K}")
+
+
+def test_e4m3_switch_off_agrees(monkeypatch):
+    """The same e4m3 decode through the split-K tensor-core path
+    (SWG_GEMV=0): both within the FP32-output bound of the oracle."""
+    M, N, K = 1, 4096, 4096
+    g = synth.generator(520)
+    A = _e4m3_padded(M, K, K, g)
+    B = _e4m3_padded(N, K, K, g, std=0.5)
+    C = torch.zeros((M, N), dtype=torch.float32)
+    d_on, n_on = _run(0, 1, M, N, K, 0.25, A, K, B, K, 0.0, C, N, swg.E4M3_F32OUT)
+    monkeypatch.setenv("SWG_GEMV", "0")
+    d_off, n_off = _run(0, 1, M, N, K, 0.25, A, K, B, K, 0.0, C, N, swg.E4M3_F32OUT)
+    assert (n_on, n_off) == (1, 2)
+    yhat = oracle.gemm(0, 1, M, N, K, 0.25, A, K, B, K, 0.0, in_type="e4m3", c_type="f32")
+    check_f32(to_f64(d_on), yhat, K, "e4m3 gemv")
+    check_f32(to_f64(d_off), yhat, K, "e4m3 split-K")
