@@ -465,11 +465,12 @@ def time_reps(fn, reps, dev, stream, flush_buf):
 
 
 def component_cases():
-    """(name, kind, M, K, N) of the other workloads: fused SwiGLU, skinny split-K,
-    decode, the full MLP, the square bf16 GEMM at 4096 (all op combinations),
-    the 256^3 FP16-in / FP32-out GEMM with alpha = 1.5, beta = 0.5, and FP8."""
-    cases = [(f"swiglu_small_M{m}", "swiglu", m, 896, 4864) for m in (128, 512, 2048)]
-    cases += [(f"swiglu_8b_M{m}", "swiglu", m, 4096, 14336) for m in (512, 2048, 8192)]
+    """(name, kind, M, K, N) of the other workloads: fused SwiGLU (also at one
+    row, decode), skinny split-K, decode, the full MLP, the square bf16 GEMM at
+    4096 (all op combinations), the 256^3 FP16-in / FP32-out GEMM with
+    alpha = 1.5, beta = 0.5, and FP8."""
+    cases = [(f"swiglu_small_M{m}", "swiglu", m, 896, 4864) for m in (1, 128, 512, 2048)]
+    cases += [(f"swiglu_8b_M{m}", "swiglu", m, 4096, 14336) for m in (1, 512, 2048, 8192)]
     cases += [(f"skinny_splitk_M{m}", "skinny", m, 16384, 4096) for m in (16, 32, 64)]
     cases += [(f"decode_gemv_M{m}", "gemv", m, 4096, 4096) for m in (1, 8)]
     cases += [("mlp_small_M2048", "mlp", 2048, 896, 4864), ("mlp_8b_M2048", "mlp", 2048, 4096, 14336)]

@@ -506,7 +506,8 @@ int splitk_swapped(DeviceState *d, const TypeInfo &ti, int transA, int transB, i
 // op(A) slice a CTA stages within kGemvSlice / rows elements, each range a
 // whole number of boxes (256 or 128 K elements) except the last.  The ring
 // of 16 KB boxes is as deep as 227 KB of shared memory allows (12 at most),
-// or half that when the grid is larger than the GPU (two CTAs per SM).
+// or as a half or a third of it allows when the grid is larger than the GPU
+// (two or three CTAs per SM).
 // SWG_ERR_UNSUPPORTED, with nothing launched, when K needs more ranges, N
 // is beyond 2^30 or the tensor map cannot be encoded.
 constexpr int64_t kGemvMaxRows = 2;
@@ -540,9 +541,11 @@ bool make_tmap_plain(CUtensorMap *m, const void *ptr, int in_kind, int64_t inner
 }
 
 // in_kind: 0 binary16, 1 bfloat16, 2 e4m3 (A stored M x K, B stored N x K).
+// swiglu: B is the interleaved weight W_fused (K x N with N = 2 x the output
+// columns) and C is Y; the kernel's last step forms SiLU(Gate) * Up.
 int gemv_path(DeviceState *d, int in_kind, int out_kind, int transA, int transB, int64_t M,
               int64_t N, int64_t K, float alpha, const void *A, int64_t lda, const void *B,
-              int64_t ldb, float beta, void *C, int64_t ldc, cudaStream_t s)
+              int64_t ldb, float beta, void *C, int64_t ldc, cudaStream_t s, bool swiglu = false)
 {
     const int mr = M <= 1 ? 1 : 2;
     const bool b_kn = transB == SWG_OP_N;
@@ -556,7 +559,10 @@ int gemv_path(DeviceState *d, int in_kind, int out_kind, int transA, int transB,
     ranges = std::max<int64_t>(ranges, s_min);
     const int64_t kr = cdiv(cdiv(K, ranges), ks) * ks;
     ranges = cdiv(K, kr);
-    const int64_t budget = blocks * ranges > d->sms ? 115712 : swg::GV_MAX_SMEM;
+    // Up to three CTAs per SM when the grid is larger than the GPU (228 KB of
+    // shared memory per SM, 1 KB of it reserved per CTA).
+    const int64_t per_sm = std::min<int64_t>(3, cdiv(blocks * ranges, d->sms));
+    const int64_t budget = per_sm == 1 ? swg::GV_MAX_SMEM : 233472 / per_sm - 1024;
     const int64_t fixed = swg::gemv_smem_bytes(mr, b_kn, in_kind, (int)kr, 0);
     const int64_t per_stage = swg::gemv_smem_bytes(mr, b_kn, in_kind, (int)kr, 1) - fixed;
     const int64_t stages = std::min<int64_t>({12, cdiv(kr, ks), (budget - fixed) / per_stage});
@@ -585,6 +591,7 @@ int gemv_path(DeviceState *d, int in_kind, int out_kind, int transA, int transB,
     g.beta = beta;
     g.out_kind = out_kind;
     g.err = d->err;
+    g.swiglu = swiglu ? 1 : 0;
     if (swg::launch_gemv(tm, g, mr, b_kn, in_kind, (int)blocks, s) != cudaSuccess)
         return cuda_fail();
     g_launches++;
@@ -983,6 +990,13 @@ int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M, int64_t N
     }
 
     const int64_t N2 = 2 * N;
+    // One or two rows (decode): one launch of the FP32-pipe kernel, which
+    // streams W_fused once and forms SiLU(Gate) * Up in its final reduction.
+    if (M <= kGemvMaxRows && !gemv_disabled()) {
+        const int rc = gemv_path(d, 1, swg::OUT_BF16, SWG_OP_N, SWG_OP_N, M, N2, K, 1.0f, A, K,
+                                 W_fused, N2, 0.0f, Y, N, s, true);
+        if (rc != SWG_ERR_UNSUPPORTED) return rc;
+    }
     static const int cands[] = {256, 128, 64};
     const TileChoice tc = choose_tiles(d, 1, M, N2, cands, 3);
     const int bn = tc.bn;

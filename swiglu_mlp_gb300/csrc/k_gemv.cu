@@ -428,7 +428,24 @@ __global__ void __launch_bounds__(GV_THREADS, 1)
     }
 
     cluster_sync_all();     // every partial block of the cluster is written
-    if (rank == 0 && warp > 0) {
+    if (rank == 0 && warp > 0 && g.swiglu) {
+        // Column pairs (Gate, Up) of the interleaved weight -> one output
+        // column each, the SwiGLU page's pair-multiply epilogue.
+        const uint32_t part_s = smem_u32(part);
+        for (int t = threadIdx.x - 32; t < MR * (CW / 2); t += GV_CONSUMERS) {
+            const int m = t / (CW / 2), c = 2 * (t - m * (CW / 2)), n = n0 + c;
+            if (m < g.M && n < g.N) {
+                const uint32_t at = part_s + 4u * (uint32_t)(m * CW + c);
+                float gs = 0.0f, us = 0.0f;
+                for (int r = 0; r < g.ranges; ++r) {
+                    gs += ld_shared_cluster_f32(mapa_shared(at, (uint32_t)r));
+                    us += ld_shared_cluster_f32(mapa_shared(at + 4u, (uint32_t)r));
+                }
+                const float y = silu_f32(g.alpha * gs) * (g.alpha * us);
+                store_out(g.D, (long long)m * g.ldd + (n >> 1), y, g.out_kind);
+            }
+        }
+    } else if (rank == 0 && warp > 0) {
         const uint32_t part_s = smem_u32(part);
         for (int t = threadIdx.x - 32; t < MR * CW; t += GV_CONSUMERS) {
             const int m = t / CW, n = n0 + (t - m * CW);

@@ -76,6 +76,9 @@ struct GemvArgs {
     float alpha, beta;
     int out_kind;                // OutKind
     int *err;                    // device error word
+    // 1: B is an interleaved SwiGLU weight (columns 2j, 2j + 1 = Gate, Up of
+    // output j; N counts both) and D[m][j] = SiLU(alpha g) * (alpha u); no C.
+    int swiglu;
 };
 constexpr int GV_MAX_SMEM = 232448;          // 227 KB, the per-CTA maximum
 int gemv_cols_per_block(bool b_kn, int in_kind);   // output columns per cluster

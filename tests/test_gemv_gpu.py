@@ -254,3 +254,44 @@ def test_e4m3_switch_off_agrees(monkeypatch):
     yhat = oracle.gemm(0, 1, M, N, K, 0.25, A, K, B, K, 0.0, in_type="e4m3", c_type="f32")
     check_f32(to_f64(d_on), yhat, K, "e4m3 gemv")
     check_f32(to_f64(d_off), yhat, K, "e4m3 split-K")
+
+
+def _swiglu_fused(W1, W2, K, N):
+    """W_fused from the oracle's interleave (not from the CUDA path)."""
+    Wf = oracle.interleave(W1, W2, K, N)
+    return torch.from_numpy(Wf.view(np.int16)).view(torch.bfloat16)
+
+
+@pytest.mark.parametrize("M", [1, 2])
+@pytest.mark.parametrize("K,N", [(8, 8), (136, 520), (1000, 264), (896, 4864), (4096, 14336)])
+def test_swiglu_decode_rows(M, K, N):
+    """swiglu_mlp with one or two rows: one launch of the same kernel over the
+    interleaved W_fused, SiLU(Gate) * Up formed per column pair in its final
+    reduction ("Sobreposição de Ativação em Nível de Tile para Inferência
+    Eficiente de LLM", Metodologia); checked against the oracle from separate
+    W1 and W2, every output."""
+    A, W1, W2 = synth.swiglu(M, K, N, seed=600 + M + K, w_std=0.02 if K >= 896 else 0.1)
+    Wf = _swiglu_fused(W1, W2, K, N)
+    Y = torch.full((M, N), 9.0, dtype=torch.bfloat16, device="cuda")
+    before = swg.launch_count()
+    swg.swiglu_mlp(A.cuda(), Wf.cuda(), Y, M, N, K)
+    assert swg.launch_count() - before == 1
+    assert swg.get_device_error() == 0
+    yhat = oracle.swiglu(A, W1, W2, M, N, K)
+    check_half(to_f64(Y), yhat, f"swiglu decode M={M} K={K} N={N}")
+
+
+def test_swiglu_decode_agrees_with_tensor_path(monkeypatch):
+    M, K, N = 1, 896, 4864
+    A, W1, W2 = synth.swiglu(M, K, N, seed=610)
+    Wf = _swiglu_fused(W1, W2, K, N).cuda()
+    Ad = A.cuda()
+    Y1 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    Y2 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    swg.swiglu_mlp(Ad, Wf, Y1, M, N, K)
+    monkeypatch.setenv("SWG_GEMV", "0")
+    swg.swiglu_mlp(Ad, Wf, Y2, M, N, K)
+    assert swg.get_device_error() == 0
+    yhat = oracle.swiglu(A, W1, W2, M, N, K)
+    check_half(to_f64(Y1), yhat, "swiglu decode, one-launch kernel")
+    check_half(to_f64(Y2), yhat, "swiglu decode, tensor-core path")
