@@ -481,6 +481,7 @@ def component_cases():
     cases += [(f"gemm_4096_{t}", f"gemm_{t}", 4096, 4096, 4096) for t in ("nn", "nt", "tn", "tt")]
     cases += [("gemm_f16_f32out_256", "gemm_f16_small", 256, 256, 256)]
     cases += [("fp8_gemm_8192", "fp8gemm", 8192, 8192, 8192),
+              ("fp8_swiglu_8b_M1", "fp8swiglu", 1, 4096, 14336),
               ("fp8_swiglu_8b_M2048", "fp8swiglu", 2048, 4096, 14336),
               ("fp8_swiglu_8b_M8192", "fp8swiglu", 8192, 4096, 14336)]
     return cases

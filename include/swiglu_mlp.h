@@ -155,6 +155,11 @@ SWG_API int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,
  *   Alignment  all three pointers 16-byte aligned, K % 8 == 0 and
  *            N % 8 == 0; otherwise SWG_ERR_MISALIGNED.
  *   M == 0 or N == 0: nothing to do.  K == 0: Y = SiLU(0) * 0 = 0.
+ *   One or two rows (M <= 2, decode; K <= 8 * 8192 / M): one kernel on the
+ *            FP32 pipes streams W_fused once and forms SiLU(gate) * up per
+ *            column pair in its final, fixed-order reduction (the gemm
+ *            kernel for one or two rows); SWG_GEMV=0 keeps the tensor-core
+ *            tiles.
  */
 SWG_API int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M,
                int64_t N, int64_t K, void *stream);
@@ -172,6 +177,8 @@ SWG_API int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M,
  *   Y          bfloat16, M x N, row stride N (written).
  *   scale      s above; applied to Gate and Up before the SiLU.
  *   Alignment  pointers 16-byte aligned, K % 16 == 0, N % 8 == 0.
+ *   One or two rows (M <= 2): the same one-kernel path as swiglu_mlp, reading
+ *              W_fused_t in 256 x 64 byte boxes.
  */
 SWG_API int swiglu_mlp_fp8(const void *A, const void *W_fused_t, void *Y,
                            int64_t M, int64_t N, int64_t K, float scale,

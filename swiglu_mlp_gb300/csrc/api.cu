@@ -1068,6 +1068,14 @@ int swiglu_mlp_fp8(const void *A, const void *W_fused_t, void *Y, int64_t M, int
         return launch_status();
     }
     const int64_t N2 = 2 * N;
+    // One or two rows (decode): the FP32-pipe kernel over the transposed
+    // interleaved weight (its N x K layout), SiLU(Gate) * Up in its final
+    // reduction, the scale applied to Gate and Up first.
+    if (M <= kGemvMaxRows && !gemv_disabled()) {
+        const int rc = gemv_path(d, 2, swg::OUT_BF16, SWG_OP_N, SWG_OP_T, M, N2, K, scale, A, K,
+                                 W_fused_t, K, 0.0f, Y, N, s, true);
+        if (rc != SWG_ERR_UNSUPPORTED) return rc;
+    }
     static const int cands[] = {256, 128, 64};
     const TileChoice tc = choose_tiles(d, 5, M, N2, cands, 3);
     const int bn = tc.bn;

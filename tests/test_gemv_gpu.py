@@ -295,3 +295,21 @@ def test_swiglu_decode_agrees_with_tensor_path(monkeypatch):
     yhat = oracle.swiglu(A, W1, W2, M, N, K)
     check_half(to_f64(Y1), yhat, "swiglu decode, one-launch kernel")
     check_half(to_f64(Y2), yhat, "swiglu decode, tensor-core path")
+
+
+@pytest.mark.parametrize("M", [1, 2])
+@pytest.mark.parametrize("K,N", [(16, 8), (256, 520), (4096, 14336)])
+def test_fp8_swiglu_decode_rows(M, K, N):
+    """swiglu_mlp_fp8 with one or two rows: the e4m3 kernel over the
+    transposed interleaved weight [2N x K] (64-row boxes), the per-tensor
+    scale applied to Gate and Up before SiLU; every output against the
+    oracle on the same e4m3 values."""
+    A, W1, W2, sw = synth.swiglu_e4m3(M, K, N, seed=620 + M + K, w_std=0.05)
+    Wt = torch.from_numpy(oracle.interleave_t8(W1, W2, K, N)).view(torch.float8_e4m3fn)
+    Y = torch.full((M, N), 9.0, dtype=torch.bfloat16, device="cuda")
+    before = swg.launch_count()
+    swg.swiglu_mlp_fp8(A.cuda(), Wt.cuda(), Y, M, N, K, sw)
+    assert swg.launch_count() - before == 1
+    assert swg.get_device_error() == 0
+    yhat = oracle.swiglu_typed(A, W1, W2, M, N, K, in_type="e4m3", scale=sw)
+    check_half(to_f64(Y), yhat, f"fp8 swiglu decode M={M} K={K} N={N}")
