@@ -473,7 +473,8 @@ def component_cases():
     cases += [(f"swiglu_8b_M{m}", "swiglu", m, 4096, 14336) for m in (1, 512, 2048, 8192)]
     cases += [(f"skinny_splitk_M{m}", "skinny", m, 16384, 4096) for m in (16, 32, 64)]
     cases += [(f"decode_gemv_M{m}", "gemv", m, 4096, 4096) for m in (1, 8)]
-    cases += [("mlp_small_M2048", "mlp", 2048, 896, 4864), ("mlp_8b_M2048", "mlp", 2048, 4096, 14336)]
+    cases += [("mlp_small_M2048", "mlp", 2048, 896, 4864), ("mlp_8b_M2048", "mlp", 2048, 4096, 14336),
+              ("mlp_8b_M1", "mlp", 1, 4096, 14336)]
     cases += [("swiglu_dual_small_M2048", "dual", 2048, 896, 4864),
               ("swiglu_dual_8b_M2048", "dual", 2048, 4096, 14336)]
     cases += [("fp8_decode_gemv_M1", "fp8gemm", 1, 4096, 4096),

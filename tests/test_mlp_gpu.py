@@ -74,3 +74,23 @@ def test_mlp_rejects_before_launch():
         swg.swiglu_mlp_forward(Y, Y, Y, Y, Out, 8, 12, 8)     # N % 8 != 0
     assert e.value.status == 2
     assert swg.launch_count() == before
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 896, 4864), (2, 136, 520), (1, 4096, 14336)])
+def test_mlp_decode_rows(M, K, N):
+    """Decode: one or two rows through the whole MLP, two launches (the
+    one-or-two-rows kernel for the SwiGLU and again for the down projection,
+    beta = 1 residual), every output against the oracle."""
+    W1, W2, Wd, Wf = _weights(K, N, seed=40 + M + K, w_std=0.02)
+    A = synth.normal((M, K), synth.generator(41 + M))
+    R = synth.normal((M, K), synth.generator(42 + M))
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    Out = R.cuda()
+    before = swg.launch_count()
+    swg.swiglu_mlp_forward(A.cuda(), Wf.cuda(), Wd.cuda(), Y, Out, M, N, K, 1.0)
+    assert swg.launch_count() - before == 2
+    assert swg.get_device_error() == 0
+    check_half(to_f64(Y), oracle.swiglu(A, W1, W2, M, N, K), "Y")
+    yhat = oracle.mlp(A, W1, W2, Wd, M, N, K, beta=1.0, Out_old=R)
+    check_two_stage(to_f64(Out), yhat, _prop_bound(A, W1, W2, Wd, M, N, K, None),
+                    f"mlp decode {M}x{K}x{N}")
