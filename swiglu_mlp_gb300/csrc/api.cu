@@ -496,20 +496,20 @@ int splitk_swapped(DeviceState *d, const TypeInfo &ti, int transA, int transB, i
     return SWG_OK;
 }
 
-// One or two rows of 16-bit inputs: one launch of the cluster kernel of
-// k_gemv.cu on the FP32 pipes (the product streams op(B) once; tensor-core
+// One or two rows (16-bit or e4m3 inputs): one launch of the cluster kernel
+// of k_gemv.cu on the FP32 pipes (the product streams op(B) once; tensor-core
 // tiles would be almost all padding).  Measured on GB300 at 4096 x 4096: one
 // row 8.3 us back to back against 9.5-10.0 us for the split-K tensor-core
-// path; three or four rows were slower here (10.9-13.6 us) than there.  Blocks of 32 (B stored N x K) or 64
-// (B stored K x N) output columns.  K is cut into up to 8 ranges: as many as
-// bring the grid to about one CTA per SM, at least as many as keep the FP32
-// op(A) slice a CTA stages within kGemvSlice / rows elements, each range a
-// whole number of boxes (256 or 128 K elements) except the last.  The ring
-// of 16 KB boxes is as deep as 227 KB of shared memory allows (12 at most),
-// or as a half or a third of it allows when the grid is larger than the GPU
-// (two or three CTAs per SM).
-// SWG_ERR_UNSUPPORTED, with nothing launched, when K needs more ranges, N
-// is beyond 2^30 or the tensor map cannot be encoded.
+// path; three or four rows were slower there (10.9-13.6 us) than on the
+// tensor cores.  Blocks of 32 (B stored N x K; 64 for e4m3) or 128 (B stored
+// K x N) output columns.  K is cut into up to 8 ranges: as many as bring the
+// grid to about one CTA per SM, at least as many as keep the FP32 op(A) slice
+// a CTA stages within kGemvSlice / rows elements, each range a whole number
+// of boxes (256 or 64 K elements) except the last.  The ring of 16 KB boxes
+// is as deep as 227 KB of shared memory allows (12 at most), or as a half or
+// a third of it allows when the grid is larger than the GPU (two or three
+// CTAs per SM).  SWG_ERR_UNSUPPORTED, with nothing launched, when K needs
+// more ranges, N is beyond 2^30 or the tensor map cannot be encoded.
 constexpr int64_t kGemvMaxRows = 2;
 constexpr int64_t kGemvSlice = 8192;
 

@@ -26,10 +26,10 @@
 //     boxes of 256 K x 32 rows; each consumer warp owns 4 rows (output
 //     columns), lane l takes elements 8l..8l+7 of each row, and a shuffle
 //     butterfly sums the 32 lanes at the end;
-//   op(B) = B (B stored K x N, N contiguous): boxes of 64 columns x 128 K
-//     rows; 8 threads cover the 64 columns (8 each) and 32 row lanes take
-//     every 32nd row; the 4 row lanes of a warp are summed by shuffles, the 8
-//     warps in shared memory.
+//   op(B) = B (B stored K x N, N contiguous): boxes of 128 columns x 64 K
+//     rows; 16 threads cover the 128 columns (8 each) and 16 row lanes take
+//     every 16th row; the 2 row lanes of a warp are summed by a shuffle, the
+//     8 warps in shared memory.
 // Every sum runs in a fixed order.  The output is D = alpha * sum + beta * C
 // with C read only when beta != 0.  Each wait on a stage barrier is bounded:
 // past the limit the CTA records ERR_TIMEOUT in the error word, the producer
@@ -51,9 +51,9 @@ constexpr int GV_WARPS = GV_CONSUMERS / 32;
 constexpr int GV_THREADS = GV_CONSUMERS + 32;       // + the producer warp
 constexpr int GV_STAGE_BYTES = 16384;
 constexpr int NK_KS = 256;                          // B stored N x K: K elements per box
-constexpr int KN_CW = 64;                           // B stored K x N: columns per box
-constexpr int KN_KS = 128;                          //   K rows per box
-constexpr int KN_RPT = KN_KS / 32;                  //   rows per thread and box (4)
+constexpr int KN_CW = 128;                          // B stored K x N: columns per box
+constexpr int KN_KS = 64;                           //   K rows per box
+constexpr int KN_RPT = KN_KS / 16;                  //   rows per thread and box (4)
 
 // Input kinds: IK 0 = binary16, 1 = bfloat16, 2 = e4m3 (8-bit).
 template <int IK> using Elem = std::conditional_t<IK == 2, uint8_t, uint16_t>;
@@ -197,7 +197,7 @@ __device__ __forceinline__ void stage_a(float *As, const GemvArgs &g, int k0, in
 
 // Shared memory of one CTA, from a 128-byte aligned base: the ring of boxes,
 // the op(A) slice (MR x kr FP32), this CTA's partial block (MR x CW FP32),
-// the per-warp sums of the K x N layout (8 x MR x 64 FP32), the stage
+// the per-warp sums of the K x N layout (8 x MR x 128 FP32), the stage
 // barriers full[ns] and empty[ns], and the abort flag.  cw: output columns
 // per CTA (gemv_cols_per_block).
 struct GvLayout {
@@ -286,8 +286,8 @@ __device__ __forceinline__ void consume_nk(const GemvArgs &g, const uint8_t *rin
         }
 }
 
-// B stored K x N.  Box s of the range holds K rows k0 + 128 s .. + 127,
-// columns n0..n0+63 (row-major, 128 bytes a row).
+// B stored K x N.  Box s of the range holds K rows k0 + 64 s .. + 63,
+// columns n0..n0+127 (row-major, 256 bytes a row).
 template <int MR, int IK>
 __device__ __forceinline__ void consume_kn(const GemvArgs &g, const uint8_t *ring,
                                            const uint64_t *full, uint64_t *empty,
@@ -297,7 +297,7 @@ __device__ __forceinline__ void consume_kn(const GemvArgs &g, const uint8_t *rin
     static_assert(IK != 2, "8-bit B is read N x K only");
     stage_a<MR, IK, false>(As, g, k0, klen, ct);
     named_bar_sync(1, GV_CONSUMERS);
-    const int cx = ct & 7, rl = ct >> 3;               // 8 column threads x 32 row lanes
+    const int cx = ct & 15, rl = ct >> 4;              // 16 column threads x 16 row lanes
     const int cw = ct >> 5, lane = ct & 31;
     float acc[MR][8];
 #pragma unroll
@@ -312,10 +312,10 @@ __device__ __forceinline__ void consume_kn(const GemvArgs &g, const uint8_t *rin
         uint4 bv[KN_RPT];
 #pragma unroll
         for (int i = 0; i < KN_RPT; ++i)
-            bv[i] = *reinterpret_cast<const uint4 *>(st + (rl + 32 * i) * KN_CW);
+            bv[i] = *reinterpret_cast<const uint4 *>(st + (rl + 16 * i) * KN_CW);
 #pragma unroll
         for (int i = 0; i < KN_RPT; ++i) {
-            const int kk = s * KN_KS + rl + 32 * i;
+            const int kk = s * KN_KS + rl + 16 * i;
             float a[MR];
             if constexpr (MR == 2) {
                 const float2 t = *reinterpret_cast<const float2 *>(As + kk * 2);
@@ -333,15 +333,14 @@ __device__ __forceinline__ void consume_kn(const GemvArgs &g, const uint8_t *rin
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
     }
-    // The 4 row lanes of this warp (lanes cx, cx + 8, cx + 16, cx + 24).
+    // The 2 row lanes of this warp (lanes cx and cx + 16).
 #pragma unroll
     for (int m = 0; m < MR; ++m)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             float v = acc[m][e];
-            v += __shfl_xor_sync(0xffffffffu, v, 8);
             v += __shfl_xor_sync(0xffffffffu, v, 16);
-            if (lane < 8) red[(cw * MR + m) * KN_CW + 8 * lane + e] = v;
+            if (lane < 16) red[(cw * MR + m) * KN_CW + 8 * lane + e] = v;
         }
     named_bar_sync(1, GV_CONSUMERS);
     for (int t = ct; t < MR * KN_CW; t += GV_CONSUMERS) {
