@@ -476,7 +476,8 @@ def component_cases():
     cases += [("mlp_small_M2048", "mlp", 2048, 896, 4864), ("mlp_8b_M2048", "mlp", 2048, 4096, 14336),
               ("mlp_8b_M1", "mlp", 1, 4096, 14336)]
     cases += [("swiglu_dual_small_M2048", "dual", 2048, 896, 4864),
-              ("swiglu_dual_8b_M2048", "dual", 2048, 4096, 14336)]
+              ("swiglu_dual_8b_M2048", "dual", 2048, 4096, 14336),
+              ("swiglu_dual_8b_M1", "dual", 1, 4096, 14336)]
     cases += [("fp8_decode_gemv_M1", "fp8gemm", 1, 4096, 4096),
               ("fp8_skinny_splitk_M16", "fp8gemm", 16, 16384, 4096)]
     cases += [(f"gemm_4096_{t}", f"gemm_{t}", 4096, 4096, 4096) for t in ("nn", "nt", "tn", "tt")]

@@ -199,6 +199,8 @@ SWG_API int swiglu_mlp_fp8(const void *A, const void *W_fused_t, void *Y,
  *   W1, W2  bfloat16, each K x N, row stride N.
  *   Y       bfloat16, M x N, row stride N (written).
  *   Alignment, sizes and the K == 0 case as for swiglu_mlp.
+ *   One or two rows (M <= 2): the one-kernel path of swiglu_mlp, reading 64
+ *           columns of W1 beside the same 64 columns of W2 per stage.
  */
 SWG_API int swiglu_mlp_dual(const void *A, const void *W1, const void *W2,
                             void *Y, int64_t M, int64_t N, int64_t K,

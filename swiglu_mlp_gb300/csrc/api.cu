@@ -542,15 +542,20 @@ bool make_tmap_plain(CUtensorMap *m, const void *ptr, int in_kind, int64_t inner
 
 // in_kind: 0 binary16, 1 bfloat16, 2 e4m3 (A stored M x K, B stored N x K).
 // swiglu: B is the interleaved weight W_fused (K x N with N = 2 x the output
-// columns) and C is Y; the kernel's last step forms SiLU(Gate) * Up.
+// columns) and C is Y; the kernel's last step forms SiLU(Gate) * Up.  B2
+// non-null: SwiGLU from separate bf16 W1 = B and W2 = B2, both K x N with
+// row stride ldb, N the output width (64 output columns per block).
 int gemv_path(DeviceState *d, int in_kind, int out_kind, int transA, int transB, int64_t M,
               int64_t N, int64_t K, float alpha, const void *A, int64_t lda, const void *B,
-              int64_t ldb, float beta, void *C, int64_t ldc, cudaStream_t s, bool swiglu = false)
+              int64_t ldb, float beta, void *C, int64_t ldc, cudaStream_t s, bool swiglu = false,
+              const void *B2 = nullptr)
 {
     const int mr = M <= 1 ? 1 : 2;
     const bool b_kn = transB == SWG_OP_N;
+    const bool dual = B2 != nullptr;
+    if (dual && (!b_kn || in_kind != 1)) return SWG_ERR_UNSUPPORTED;
     const int64_t ks = swg::gemv_k_per_stage(b_kn);
-    const int64_t blocks = cdiv(N, swg::gemv_cols_per_block(b_kn, in_kind));
+    const int64_t blocks = cdiv(N, swg::gemv_cols_per_block(b_kn, in_kind) / (dual ? 2 : 1));
     const int64_t kr_max = kGemvSlice / mr;          // a multiple of both box lengths
     const int64_t s_min = cdiv(K, kr_max);
     if (s_min > 8 || N > (int64_t(1) << 30)) return SWG_ERR_UNSUPPORTED;
@@ -568,11 +573,18 @@ int gemv_path(DeviceState *d, int in_kind, int out_kind, int transA, int transB,
     const int64_t stages = std::min<int64_t>({12, cdiv(kr, ks), (budget - fixed) / per_stage});
     if (stages < 1) return SWG_ERR_UNSUPPORTED;
 
-    CUtensorMap tm;
-    const bool ok = b_kn ? make_tmap_plain(&tm, B, in_kind, N, K, ldb, swg::gemv_box_inner(true),
-                                           swg::gemv_box_outer(true, in_kind))
-                         : make_tmap_plain(&tm, B, in_kind, K, N, ldb, swg::gemv_box_inner(false),
-                                           swg::gemv_box_outer(false, in_kind));
+    CUtensorMap tm, tm2;
+    bool ok;
+    if (dual) {
+        const int bi = swg::gemv_box_inner(true) / 2, bo = swg::gemv_box_outer(true, in_kind);
+        ok = make_tmap_plain(&tm, B, in_kind, N, K, ldb, bi, bo) &&
+             make_tmap_plain(&tm2, B2, in_kind, N, K, ldb, bi, bo);
+    } else {
+        ok = b_kn ? make_tmap_plain(&tm, B, in_kind, N, K, ldb, swg::gemv_box_inner(true),
+                                    swg::gemv_box_outer(true, in_kind))
+                  : make_tmap_plain(&tm, B, in_kind, K, N, ldb, swg::gemv_box_inner(false),
+                                    swg::gemv_box_outer(false, in_kind));
+    }
     if (!ok) return SWG_ERR_UNSUPPORTED;
 
     swg::GemvArgs g{};
@@ -591,8 +603,9 @@ int gemv_path(DeviceState *d, int in_kind, int out_kind, int transA, int transB,
     g.beta = beta;
     g.out_kind = out_kind;
     g.err = d->err;
-    g.swiglu = swiglu ? 1 : 0;
-    if (swg::launch_gemv(tm, g, mr, b_kn, in_kind, (int)blocks, s) != cudaSuccess)
+    g.swiglu = swiglu || dual ? 1 : 0;
+    if (swg::launch_gemv(tm, dual ? &tm2 : nullptr, g, mr, b_kn, in_kind, (int)blocks, s) !=
+        cudaSuccess)
         return cuda_fail();
     g_launches++;
     return SWG_OK;
@@ -1138,6 +1151,13 @@ int swiglu_mlp_dual(const void *A, const void *W1, const void *W2, void *Y, int6
         return launch_status();
     }
 
+    // One or two rows (decode): the FP32-pipe kernel reading W1 and W2 in
+    // 64-column boxes side by side, SiLU(Gate) * Up in its final reduction.
+    if (M <= kGemvMaxRows && !gemv_disabled()) {
+        const int rc = gemv_path(d, 1, swg::OUT_BF16, SWG_OP_N, SWG_OP_N, M, N, K, 1.0f, A, K, W1,
+                                 N, 0.0f, Y, N, s, true, W2);
+        if (rc != SWG_ERR_UNSUPPORTED) return rc;
+    }
     // Tiles are chosen in the 2N-wide Gate|Up column space, as for swiglu_mlp.
     static const int cands[] = {256, 128};
     const TileChoice tc = choose_tiles(d, 3, M, 2 * N, cands, 2);

@@ -288,7 +288,7 @@ __device__ __forceinline__ void consume_nk(const GemvArgs &g, const uint8_t *rin
 
 // B stored K x N.  Box s of the range holds K rows k0 + 64 s .. + 63,
 // columns n0..n0+127 (row-major, 256 bytes a row).
-template <int MR, int IK>
+template <int MR, int IK, bool DUAL>
 __device__ __forceinline__ void consume_kn(const GemvArgs &g, const uint8_t *ring,
                                            const uint64_t *full, uint64_t *empty,
                                            volatile int *abort_flag, float *As, float *red,
@@ -308,11 +308,15 @@ __device__ __forceinline__ void consume_kn(const GemvArgs &g, const uint8_t *rin
     for (int s = 0; s < nst; ++s) {
         if (!stage_ready(full, s, g.stages, abort_flag, g.err)) break;
         const int slot = s % g.stages;
-        const uint16_t *st = reinterpret_cast<const uint16_t *>(ring + slot * GV_STAGE_BYTES) + 8 * cx;
+        // One box of 128 columns, or (DUAL) two boxes of 64 columns, W1's
+        // then W2's, each 64 rows of 128 bytes.
+        constexpr int ROW = DUAL ? KN_CW / 2 : KN_CW;
+        const uint16_t *st = reinterpret_cast<const uint16_t *>(ring + slot * GV_STAGE_BYTES) +
+                             (DUAL ? (cx >> 3) * (KN_KS * ROW) + 8 * (cx & 7) : 8 * cx);
         uint4 bv[KN_RPT];
 #pragma unroll
         for (int i = 0; i < KN_RPT; ++i)
-            bv[i] = *reinterpret_cast<const uint4 *>(st + (rl + 16 * i) * KN_CW);
+            bv[i] = *reinterpret_cast<const uint4 *>(st + (rl + 16 * i) * ROW);
 #pragma unroll
         for (int i = 0; i < KN_RPT; ++i) {
             const int kk = s * KN_KS + rl + 16 * i;
@@ -354,10 +358,12 @@ __device__ __forceinline__ void consume_kn(const GemvArgs &g, const uint8_t *rin
 
 // Grid: clusters of g.ranges CTAs, one cluster per block of output columns;
 // CTA rank r of a cluster covers K range [r kr, min(K, (r + 1) kr)).
-template <int MR, bool B_KN, int IK>
+template <int MR, bool B_KN, int IK, bool DUAL>
 __global__ void __launch_bounds__(GV_THREADS, 1)
-    gemv_kernel(const __grid_constant__ CUtensorMap tmB, const GemvArgs g)
+    gemv_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
+                const GemvArgs g)
 {
+    static_assert(!DUAL || (B_KN && IK == 1), "two weights: bf16 B stored K x N");
     constexpr int CW = B_KN ? KN_CW : nk_rows(esize<IK>());
     constexpr int KS = B_KN ? KN_KS : NK_KS;
     extern __shared__ uint8_t gv_raw[];
@@ -388,6 +394,7 @@ __global__ void __launch_bounds__(GV_THREADS, 1)
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tmB);
+        if (DUAL) tma_prefetch_desc(&tmB2);
     }
     __syncthreads();
     // B and op(A) may come from the kernel before this one on the stream.
@@ -406,10 +413,14 @@ __global__ void __launch_bounds__(GV_THREADS, 1)
                 const uint32_t fb = smem_u32(&full[slot]);
                 mbar_arrive_expect_tx(fb, GV_STAGE_BYTES);
                 const uint32_t dst = smem_u32(ring + slot * GV_STAGE_BYTES);
-                if (B_KN)
+                if (DUAL) {               // 64 Gate columns, then the same 64 Up columns
+                    tma_load_2d(dst, &tmB, fb, n0 / 2, k0 + s * KS);
+                    tma_load_2d(dst + GV_STAGE_BYTES / 2, &tmB2, fb, n0 / 2, k0 + s * KS);
+                } else if (B_KN) {
                     tma_load_2d(dst, &tmB, fb, n0, k0 + s * KS);
-                else
+                } else {
                     tma_load_2d(dst, &tmB, fb, k0 + s * KS, n0);
+                }
                 issued = s + 1;
             }
             // Boxes still in flight (only after an abort) land before the CTA
@@ -421,13 +432,30 @@ __global__ void __launch_bounds__(GV_THREADS, 1)
     } else {
         const int ct = threadIdx.x - 32;
         if constexpr (B_KN)
-            consume_kn<MR, IK>(g, ring, full, empty, abort_flag, As, red, part, k0, klen, nst, ct);
+            consume_kn<MR, IK, DUAL>(g, ring, full, empty, abort_flag, As, red, part, k0, klen, nst,
+                                     ct);
         else
             consume_nk<MR, IK>(g, ring, full, empty, abort_flag, As, part, k0, klen, nst, ct);
     }
 
     cluster_sync_all();     // every partial block of the cluster is written
-    if (rank == 0 && warp > 0 && g.swiglu) {
+    if (DUAL && rank == 0 && warp > 0) {
+        // Column j of the block is Gate j (from W1), column 64 + j Up j (W2).
+        const uint32_t part_s = smem_u32(part);
+        for (int t = threadIdx.x - 32; t < MR * (CW / 2); t += GV_CONSUMERS) {
+            const int m = t / (CW / 2), j = t - m * (CW / 2), n = n0 / 2 + j;
+            if (m < g.M && n < g.N) {
+                const uint32_t at = part_s + 4u * (uint32_t)(m * CW + j);
+                float gs = 0.0f, us = 0.0f;
+                for (int r = 0; r < g.ranges; ++r) {
+                    gs += ld_shared_cluster_f32(mapa_shared(at, (uint32_t)r));
+                    us += ld_shared_cluster_f32(mapa_shared(at + 4u * (CW / 2), (uint32_t)r));
+                }
+                const float y = silu_f32(g.alpha * gs) * (g.alpha * us);
+                store_out(g.D, (long long)m * g.ldd + n, y, g.out_kind);
+            }
+        }
+    } else if (rank == 0 && warp > 0 && g.swiglu) {
         // Column pairs (Gate, Up) of the interleaved weight -> one output
         // column each, the SwiGLU page's pair-multiply epilogue.
         const uint32_t part_s = smem_u32(part);
@@ -462,16 +490,16 @@ __global__ void __launch_bounds__(GV_THREADS, 1)
     cluster_sync_all();     // no CTA leaves while CTA 0 still reads its partials
 }
 
-template <int MR, bool B_KN, int IK>
-cudaError_t launch_gemv_impl(const CUtensorMap &tmB, const GemvArgs &g, int col_blocks,
-                             cudaStream_t s)
+template <int MR, bool B_KN, int IK, bool DUAL = false>
+cudaError_t launch_gemv_impl(const CUtensorMap &tmB, const CUtensorMap &tmB2, const GemvArgs &g,
+                             int col_blocks, cudaStream_t s)
 {
     static std::atomic<unsigned long long> configured{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
-    auto kernel = gemv_kernel<MR, B_KN, IK>;
+    auto kernel = gemv_kernel<MR, B_KN, IK, DUAL>;
     if (!(configured.load() & bit)) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  GV_MAX_SMEM);
@@ -493,20 +521,24 @@ cudaError_t launch_gemv_impl(const CUtensorMap &tmB, const GemvArgs &g, int col_
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kernel, tmB, g);
+    return cudaLaunchKernelEx(&cfg, kernel, tmB, tmB2, g);
 }
 
 template <int MR>
-cudaError_t launch_gemv_mr(const CUtensorMap &tmB, const GemvArgs &g, bool b_kn, int in_kind,
-                           int col_blocks, cudaStream_t s)
+cudaError_t launch_gemv_mr(const CUtensorMap &tmB, const CUtensorMap *tmB2, const GemvArgs &g,
+                           bool b_kn, int in_kind, int col_blocks, cudaStream_t s)
 {
+    if (tmB2)
+        return b_kn && in_kind == 1 ? launch_gemv_impl<MR, true, 1, true>(tmB, *tmB2, g, col_blocks, s)
+                                    : cudaErrorInvalidValue;
     if (in_kind == 2)
-        return b_kn ? cudaErrorInvalidValue : launch_gemv_impl<MR, false, 2>(tmB, g, col_blocks, s);
+        return b_kn ? cudaErrorInvalidValue
+                    : launch_gemv_impl<MR, false, 2>(tmB, tmB, g, col_blocks, s);
     if (b_kn)
-        return in_kind == 1 ? launch_gemv_impl<MR, true, 1>(tmB, g, col_blocks, s)
-                            : launch_gemv_impl<MR, true, 0>(tmB, g, col_blocks, s);
-    return in_kind == 1 ? launch_gemv_impl<MR, false, 1>(tmB, g, col_blocks, s)
-                        : launch_gemv_impl<MR, false, 0>(tmB, g, col_blocks, s);
+        return in_kind == 1 ? launch_gemv_impl<MR, true, 1>(tmB, tmB, g, col_blocks, s)
+                            : launch_gemv_impl<MR, true, 0>(tmB, tmB, g, col_blocks, s);
+    return in_kind == 1 ? launch_gemv_impl<MR, false, 1>(tmB, tmB, g, col_blocks, s)
+                        : launch_gemv_impl<MR, false, 0>(tmB, tmB, g, col_blocks, s);
 }
 
 }  // namespace
@@ -524,12 +556,12 @@ int gemv_smem_bytes(int mr, bool b_kn, int in_kind, int kr, int stages)
     return gv_layout(mr, b_kn, gemv_cols_per_block(b_kn, in_kind), kr, stages).total;
 }
 
-cudaError_t launch_gemv(const CUtensorMap &tmB, const GemvArgs &g, int mr, bool b_kn, int in_kind,
-                        int col_blocks, cudaStream_t s)
+cudaError_t launch_gemv(const CUtensorMap &tmB, const CUtensorMap *tmB2, const GemvArgs &g, int mr,
+                        bool b_kn, int in_kind, int col_blocks, cudaStream_t s)
 {
     switch (mr) {
-    case 1: return launch_gemv_mr<1>(tmB, g, b_kn, in_kind, col_blocks, s);
-    case 2: return launch_gemv_mr<2>(tmB, g, b_kn, in_kind, col_blocks, s);
+    case 1: return launch_gemv_mr<1>(tmB, tmB2, g, b_kn, in_kind, col_blocks, s);
+    case 2: return launch_gemv_mr<2>(tmB, tmB2, g, b_kn, in_kind, col_blocks, s);
     default: return cudaErrorInvalidValue;
     }
 }

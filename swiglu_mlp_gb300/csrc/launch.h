@@ -88,7 +88,10 @@ int gemv_box_outer(bool b_kn, int in_kind);
 int gemv_smem_bytes(int mr, bool b_kn, int in_kind, int kr, int stages);
 // mr: 1 or 2 (rows the kernel computes; M <= mr); b_kn: B stored K x N
 // (op N); col_blocks: cdiv(N, gemv_cols_per_block(b_kn, in_kind)).
-cudaError_t launch_gemv(const CUtensorMap &tmB, const GemvArgs &g, int mr, bool b_kn, int in_kind,
-                        int col_blocks, cudaStream_t s);
+// tmB2 non-null: SwiGLU from two bf16 weights stored K x N, tmB = W1 (Gate)
+// and tmB2 = W2 (Up), each read in boxes of 64 columns x 64 K rows; g.N is
+// the output width and col_blocks = cdiv(N, 64).
+cudaError_t launch_gemv(const CUtensorMap &tmB, const CUtensorMap *tmB2, const GemvArgs &g, int mr,
+                        bool b_kn, int in_kind, int col_blocks, cudaStream_t s);
 
 }  // namespace swg

@@ -313,3 +313,20 @@ def test_fp8_swiglu_decode_rows(M, K, N):
     assert swg.get_device_error() == 0
     yhat = oracle.swiglu_typed(A, W1, W2, M, N, K, in_type="e4m3", scale=sw)
     check_half(to_f64(Y), yhat, f"fp8 swiglu decode M={M} K={K} N={N}")
+
+
+@pytest.mark.parametrize("M", [1, 2])
+@pytest.mark.parametrize("K,N", [(8, 8), (136, 520), (1000, 200), (4096, 14336)])
+def test_swiglu_dual_decode_rows(M, K, N):
+    """swiglu_mlp_dual (separate W1, W2, no interleaved copy) with one or two
+    rows: one launch; each stage holds a 64-column box of W1 beside the same
+    columns of W2, and column j pairs with column 64 + j in the final
+    reduction.  Every output against the oracle."""
+    A, W1, W2 = synth.swiglu(M, K, N, seed=630 + M + K, w_std=0.02 if K >= 896 else 0.1)
+    Y = torch.full((M, N), 9.0, dtype=torch.bfloat16, device="cuda")
+    before = swg.launch_count()
+    swg.swiglu_mlp_dual(A.cuda(), W1.cuda(), W2.cuda(), Y, M, N, K)
+    assert swg.launch_count() - before == 1
+    assert swg.get_device_error() == 0
+    yhat = oracle.swiglu(A, W1, W2, M, N, K)
+    check_half(to_f64(Y), yhat, f"swiglu dual decode M={M} K={K} N={N}")
