@@ -1,17 +1,20 @@
 // k_gemv.cu — the few-rows product (one or two rows of op(A): decode of one
-// or two tokens) on the FP32 pipes, in one launch per call.
+// or two tokens) on the FP32 pipes, in one launch per call: GEMM (16-bit or
+// e4m3 operands) and the SwiGLU MLP's gate/up product (interleaved W_fused,
+// its transposed e4m3 form, or separate W1 and W2) with the pair-multiply
+// SiLU(Gate) * Up in the final reduction.
 //
 // With M <= 2 every weight element is used at most twice, so the call costs
 // the time to stream op(B) from HBM once ("GEMM o Coração Matemático", §14:
 // about one FLOP per byte at M = 1), and a 128-row tensor-core tile would be
 // at least 98% padding.  (With three or four rows the FP32 work per byte no
-// longer hides under the stream; those calls stay on the tensor cores.)  The K loop is split across CTAs when the output has
-// too few columns to fill the GPU ("为什么 GEMM 是 CUDA 的必修课", 关键技术
-// item 5); here the S K ranges of one block of output columns run as ONE
-// thread-block cluster, and CTA 0 of the cluster sums the S partial blocks,
-// read from the other CTAs' shared memory in rank order.  The result is
-// bit-identical from run to run, and there is no workspace and no second
-// kernel.
+// longer hides under the stream; those calls stay on the tensor cores.)  The
+// K loop is split across CTAs when the output has too few columns to fill the
+// GPU ("为什么 GEMM 是 CUDA 的必修课", 关键技术 item 5); here the S K ranges
+// of one block of output columns run as ONE thread-block cluster, and CTA 0
+// of the cluster sums the S partial blocks, read from the other CTAs' shared
+// memory in rank order.  The result is bit-identical from run to run, and
+// there is no workspace and no second kernel.
 //
 // Streaming at HBM speed needs about 150-250 KB in flight per SM (the loaded
 // DRAM latency is several microseconds), more than registers can hold, so B
@@ -27,9 +30,11 @@
 //     columns), lane l takes elements 8l..8l+7 of each row, and a shuffle
 //     butterfly sums the 32 lanes at the end;
 //   op(B) = B (B stored K x N, N contiguous): boxes of 128 columns x 64 K
-//     rows; 16 threads cover the 128 columns (8 each) and 16 row lanes take
-//     every 16th row; the 2 row lanes of a warp are summed by a shuffle, the
-//     8 warps in shared memory.
+//     rows (or, from separate W1 and W2, 64 columns of each side by side);
+//     16 threads cover the 128 columns (8 each) and 16 row lanes take every
+//     16th row; the 2 row lanes of a warp are summed by a shuffle, the 8 warps
+//     in shared memory.
+//   e4m3 B is read N x K only, in boxes of 256 K x 64 rows (8 rows a warp).
 // Every sum runs in a fixed order.  The output is D = alpha * sum + beta * C
 // with C read only when beta != 0.  Each wait on a stage barrier is bounded:
 // past the limit the CTA records ERR_TIMEOUT in the error word, the producer
