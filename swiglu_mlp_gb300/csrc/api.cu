@@ -565,7 +565,8 @@ int gemv_path(DeviceState *d, int in_kind, int out_kind, int transA, int transB,
     const int64_t kr = cdiv(cdiv(K, ranges), ks) * ks;
     ranges = cdiv(K, kr);
     // Up to three CTAs per SM when the grid is larger than the GPU (228 KB of
-    // shared memory per SM, 1 KB of it reserved per CTA).
+    // shared memory per SM, 1 KB of it reserved per CTA; every instantiation
+    // of the kernel uses at most 72 registers, so three 288-thread CTAs fit).
     const int64_t per_sm = std::min<int64_t>(3, cdiv(blocks * ranges, d->sms));
     const int64_t budget = per_sm == 1 ? swg::GV_MAX_SMEM : 233472 / per_sm - 1024;
     const int64_t fixed = swg::gemv_smem_bytes(mr, b_kn, in_kind, (int)kr, 0);

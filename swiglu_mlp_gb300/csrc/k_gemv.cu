@@ -245,11 +245,15 @@ __device__ __forceinline__ void consume_nk(const GemvArgs &g, const uint8_t *rin
     stage_a<MR, IK, true>(As, g, k0, klen, ct);
     named_bar_sync(1, GV_CONSUMERS);
     const int cw = ct >> 5, lane = ct & 31;
-    float acc[MR][RPW];
+    // Two partial sums per output, over the even and the odd elements of each
+    // 8-element chunk, advanced together by one packed FP32 FMA (16-bit B;
+    // e4m3 B keeps one scalar sum).
+    using Acc = std::conditional_t<IK != 2, float2, float>;
+    Acc acc[MR][RPW];
 #pragma unroll
     for (int m = 0; m < MR; ++m)
 #pragma unroll
-        for (int r = 0; r < RPW; ++r) acc[m][r] = 0.0f;
+        for (int r = 0; r < RPW; ++r) acc[m][r] = Acc{};
 
     for (int s = 0; s < nst; ++s) {
         if (!stage_ready(full, s, g.stages, abort_flag, g.err)) break;
@@ -273,9 +277,17 @@ __device__ __forceinline__ void consume_nk(const GemvArgs &g, const uint8_t *rin
             float b[8];
             widen8<IK>(bv[r], b);
 #pragma unroll
-            for (int m = 0; m < MR; ++m)
+            for (int m = 0; m < MR; ++m) {
+                if constexpr (IK != 2) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[m][r] = fmaf(a[m][e], b[e], acc[m][r]);
+                    for (int e = 0; e < 8; e += 2)
+                        acc[m][r] = __ffma2_rn(make_float2(a[m][e], a[m][e + 1]),
+                                               make_float2(b[e], b[e + 1]), acc[m][r]);
+                } else {   // 8 rows a warp: scalar FMAs keep the registers for 3 CTAs per SM
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[m][r] = fmaf(a[m][e], b[e], acc[m][r]);
+                }
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
@@ -284,7 +296,9 @@ __device__ __forceinline__ void consume_nk(const GemvArgs &g, const uint8_t *rin
     for (int m = 0; m < MR; ++m)
 #pragma unroll
         for (int r = 0; r < RPW; ++r) {
-            float v = acc[m][r];
+            float v;
+            if constexpr (IK != 2) v = acc[m][r].x + acc[m][r].y;
+            else v = acc[m][r];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
             if (lane == 0) part[m * ROWS + cw * RPW + r] = v;
@@ -335,9 +349,16 @@ __device__ __forceinline__ void consume_kn(const GemvArgs &g, const uint8_t *rin
             float b[8];
             widen8<IK>(bv[i], b);
 #pragma unroll
-            for (int m = 0; m < MR; ++m)
+            for (int m = 0; m < MR; ++m) {
+                const float2 am = make_float2(a[m], a[m]);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[m][e] = fmaf(a[m], b[e], acc[m][e]);
+                for (int e = 0; e < 8; e += 2) {   // two adjacent columns per packed FMA
+                    const float2 t = __ffma2_rn(am, make_float2(b[e], b[e + 1]),
+                                                make_float2(acc[m][e], acc[m][e + 1]));
+                    acc[m][e] = t.x;
+                    acc[m][e + 1] = t.y;
+                }
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
