@@ -390,6 +390,7 @@ __global__ void __launch_bounds__(GV_THREADS, 1)
                 const GemvArgs g)
 {
     static_assert(!DUAL || (B_KN && IK == 1), "two weights: bf16 B stored K x N");
+    static_assert(MR == 1 || MR == 2, "the op(A) loads are written for one or two rows");
     constexpr int CW = B_KN ? KN_CW : nk_rows(esize<IK>());
     constexpr int KS = B_KN ? KN_KS : NK_KS;
     extern __shared__ uint8_t gv_raw[];
