@@ -133,7 +133,10 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr)
 }
 
 // op(A)[m][k0 + kk] for m < MR, kk < kr, widened to FP32 into As, zero where
-// m >= M or kk >= klen.  M_MAJOR: As[m * kr + kk]; else As[kk * MR + m].
+// m >= M or kk >= klen.  M_MAJOR (the N x K consumer): row m at As + m * kr,
+// each 8-element chunk c split in halves, elements 8c..8c+3 at 4c and
+// 8c+4..8c+7 at kr/2 + 4c, so that lanes reading consecutive chunks touch
+// consecutive 16-byte words (no bank conflicts); else As[kk * MR + m].
 // A stored M x K (a_t = 0) is read 8 elements per load; A stored K x M
 // (a_t = 1, 16-bit inputs only) one element at a time.  Runs on the 256
 // consumer threads (ct = 0..255).
@@ -166,8 +169,13 @@ __device__ __forceinline__ void stage_a(float *As, const GemvArgs &g, int k0, in
                 const int m = q / per_row, kk = (q - m * per_row) * 8;
                 float f[8];
                 widen8<IK>(v[u], f);
-                if (M_MAJOR || MR == 1) {             // one row: the two layouts agree
-                    float4 *d = reinterpret_cast<float4 *>(As + m * kr + kk);
+                if (M_MAJOR) {
+                    float *row = As + m * kr + (kk >> 1);
+                    *reinterpret_cast<float4 *>(row) = make_float4(f[0], f[1], f[2], f[3]);
+                    *reinterpret_cast<float4 *>(row + (kr >> 1)) =
+                        make_float4(f[4], f[5], f[6], f[7]);
+                } else if (MR == 1) {                  // one row: As[kk]
+                    float4 *d = reinterpret_cast<float4 *>(As + kk);
                     d[0] = make_float4(f[0], f[1], f[2], f[3]);
                     d[1] = make_float4(f[4], f[5], f[6], f[7]);
                 } else {
@@ -194,7 +202,13 @@ __device__ __forceinline__ void stage_a(float *As, const GemvArgs &g, int k0, in
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int i = i0 + u * GV_CONSUMERS;
-                if (i < total) As[i] = widen1<IK>(v[u]);
+                if (i >= total) continue;
+                int dst = i;
+                if (M_MAJOR) {
+                    const int m = i / kr, kk = i - m * kr;
+                    dst = m * kr + ((kk & 4) ? (kr >> 1) : 0) + ((kk >> 3) << 2) + (kk & 3);
+                }
+                As[dst] = widen1<IK>(v[u]);
             }
         }
     }
@@ -266,9 +280,9 @@ __device__ __forceinline__ void consume_nk(const GemvArgs &g, const uint8_t *rin
         float a[MR][8];
 #pragma unroll
         for (int m = 0; m < MR; ++m) {
-            const float *ap = As + m * g.kr + s * NK_KS + 8 * lane;
+            const float *ap = As + m * g.kr + ((s * NK_KS + 8 * lane) >> 1);   // chunk halves
             const float4 a0 = *reinterpret_cast<const float4 *>(ap);
-            const float4 a1 = *reinterpret_cast<const float4 *>(ap + 4);
+            const float4 a1 = *reinterpret_cast<const float4 *>(ap + (g.kr >> 1));
             a[m][0] = a0.x; a[m][1] = a0.y; a[m][2] = a0.z; a[m][3] = a0.w;
             a[m][4] = a1.x; a[m][5] = a1.y; a[m][6] = a1.z; a[m][7] = a1.w;
         }
