@@ -52,10 +52,12 @@ typedef enum {
 typedef enum { SWG_OP_N = 0, SWG_OP_T = 1 } swg_op;
 
 /* Storage types.  A and B share one input type; C and D share one output type.
- * The e4m3 types (8-bit floating point: 1 sign, 4 exponent bits with bias 7,
- * 3 fraction bits; largest finite value 448) quantise A and B ("GEMM o
- * Coração Matemático", §12.4); per-tensor dequantisation scales are applied by
- * folding them into alpha (alpha * scale_A * scale_B).  They require
+ * The e4m3 types quantise A and B to 8 bits, with per-tensor dequantisation
+ * scales ("GEMM o Coração Matemático", §12.4: quantised operands with a
+ * scale); the scales are applied by folding them into alpha
+ * (alpha * scale_A * scale_B).  The 8-bit layout is E4M3 of the OCP 8-bit
+ * floating-point format (as torch's float8_e4m3fn): 1 sign, 4 exponent bits
+ * with bias 7, 3 fraction bits, no infinities, largest finite value 448.  They require
  * op(A) = A and op(B) = B^T, i.e. A stored M x K and B stored N x K (both
  * K-contiguous), and lda and ldb multiples of 16.  Split-K exists for them
  * only with M <= 64 (few rows, e.g. decode): such calls run the transposed
@@ -168,7 +170,9 @@ SWG_API int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M,
  * swiglu_mlp_fp8 — Y = SiLU(s * A W1) (.) (s * A W2) with e4m3 A and weights,
  * s = scale_A * scale_W (per-tensor dequantisation scales), FP32
  * accumulation, bfloat16 Y.  Same operation and sources as swiglu_mlp; the
- * 8-bit form follows "GEMM o Coração Matemático", §12.4 (quantised operands).
+ * 8-bit form follows "GEMM o Coração Matemático", §12.4 (quantised operands
+ * with a scale); the 8-bit layout is the OCP E4M3 format described at
+ * swg_dtype.
  *
  *   A          e4m3, M x K, row stride K.
  *   W_fused_t  e4m3, 2N x K, row stride K: the TRANSPOSED interleaved weight,
@@ -242,32 +246,43 @@ SWG_API int swiglu_interleave(const void *W1, const void *W2, void *W_fused,
                       int64_t K, int64_t N, void *stream);
 
 /*
- * gemm_splitk_noalloc — the split-K form of gemm that allocates no device
- * memory.  The pages have no counterpart to this call; it exists for callers
- * that cannot call cudaMalloc once they are running, for example a host
- * framework that already holds nearly all device memory in its own pool, or a
- * serving loop that forbids cudaMalloc/cudaFree because they can synchronise
- * the whole device.
+ * gemm_splitk_noalloc — gemm_ex without any device allocation.  The pages
+ * have no counterpart to this call.  It is for callers that cannot call
+ * cudaMalloc once they are running: a host framework that has already
+ * reserved nearly all device memory in its own pool (where a cudaMalloc
+ * would fail, or fragment that pool), or a serving loop that forbids
+ * cudaMalloc/cudaFree because either can synchronise the whole device.
  *
- * It computes exactly what gemm_ex computes (same arguments, same rules, same
- * fixed-order reduction, split_k with the same meaning, but always through
- * the split-K kernels) and launches the same two kernels.  The FP32 partial
- * sums go to a fixed array of SWG_NOALLOC_SCRATCH_BYTES that is part of the
- * library's device image: every GPU that loads the library holds it until the
- * process exits.  The caller still passes A, B and C.
+ * Same arguments, rules and results as gemm_ex: for every input it launches
+ * the kernels gemm_ex would launch, with the same tiles, split count and
+ * fixed-order reduction, so the two give bit-identical D.  The one
+ * difference: a split-K call keeps its FP32 partial sums in a fixed array of
+ * SWG_NOALLOC_SCRATCH_BYTES (plus two 64 KiB guard bands) that is part of the
+ * library's device image, instead of a workspace from cudaMalloc.  The
+ * caller still passes A, B and C.
  *
- *   Limit        the partials need splits * M * round_up(N, 4) * 4 bytes; a
- *                call that would need more than SWG_NOALLOC_SCRATCH_BYTES
- *                returns SWG_ERR_UNSUPPORTED and launches nothing (pick a
- *                smaller split_k, or use gemm / gemm_ex).
+ *   Limit        a split needs splits * M * round_up(N, 4) * 4 bytes of
+ *                partials; a call that would need more than
+ *                SWG_NOALLOC_SCRATCH_BYTES returns SWG_ERR_UNSUPPORTED and
+ *                launches nothing (pass a smaller split_k, or use gemm_ex).
  *   Allocation   none: no cudaMalloc, cudaFree or allocating library call.
+ *   Residency    the array is device memory of the library's module.  With
+ *                CUDA's default lazy module loading it is committed on a
+ *                device the first time this library runs there (the first
+ *                call of any of its entry points), and with
+ *                CUDA_MODULE_LOADING=EAGER when the library is loaded; it
+ *                stays until the process exits.  A caller about to reserve
+ *                nearly all device memory should make one call on each
+ *                device first.
  *   First call   on each device looks up the array's device address
  *                (cudaGetSymbolAddress) with that device current; make that
  *                first call before any stream capture.
- *   Sharing      all calls, on every stream, use the one array and it keeps
+ *   Sharing      all calls, on every stream, use the one array, and it keeps
  *                the last call's contents (each call writes every partial it
  *                reads, so nothing needs clearing).  Calls that overlap on the
  *                GPU race with each other: order them, e.g. on one stream.
+ *   Reset        call swg_shutdown() before cudaDeviceReset(): it makes the
+ *                next call look the address up again.
  */
 #define SWG_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 SWG_API int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N,
@@ -275,6 +290,19 @@ SWG_API int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N,
                                 int64_t lda, const void *B, int64_t ldb,
                                 float beta, void *C, int64_t ldc, int dtype,
                                 int split_k, void *stream);
+
+/*
+ * swg_debug_workspace_guards — diagnostic for tests (no counterpart on the
+ * pages).  With the environment variable SWG_TEST_WS_GUARD=1 set before a
+ * workspace is created, every split-K workspace and the fixed array of
+ * gemm_splitk_noalloc sit between 64 KiB guard bands of the byte 0xA5.  This
+ * call synchronises `stream` and the current device, then stores in
+ * *bad_bytes how many guard bytes of the current device's workspaces have
+ * changed (0 when no kernel wrote outside its partials; workspaces made
+ * without the variable are skipped).  SWG_ERR_INVALID_ARG for a null
+ * bad_bytes, SWG_ERR_CUDA if a copy fails.
+ */
+SWG_API int swg_debug_workspace_guards(void *stream, int64_t *bad_bytes);
 
 /* Human-readable name of a swg_status value (static string, never NULL). */
 SWG_API const char *swg_status_string(int status);
@@ -312,9 +340,11 @@ SWG_API const char *swg_cuda_error_name(int code);
 SWG_API uint64_t swg_launch_count(void);
 
 /* Frees every library-owned workspace on every device, including replaced
- * ones.  Safe to call twice; later calls allocate afresh.  Call only when no
- * library work is in flight and no captured graph that used them will be
- * replayed. */
+ * ones, and forgets every cached per-device lookup (device addresses,
+ * occupancy, kernel attributes), so it is also the call to make before
+ * cudaDeviceReset().  Safe to call twice; later calls allocate and look up
+ * afresh.  Call only when no library work is in flight and no captured graph
+ * that used the workspaces will be replayed. */
 SWG_API void swg_shutdown(void);
 
 #ifdef __cplusplus

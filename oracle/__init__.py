@@ -21,9 +21,12 @@ computes, with the passage it follows:
   ("GEMM o Coração Matemático", §13.3, with the gated activation above).
 * :func:`swiglu_typed`, :func:`interleave_t8` — the same SwiGLU on 8-bit
   (e4m3) operands with a per-tensor scale, and the transposed interleave the
-  8-bit kernel reads ("GEMM o Coração Matemático", §12.4).
-* :func:`silu`, :func:`f16_to_f64`, :func:`bf16_to_f64`, :func:`e4m3_to_f64`
-  — the scalar pieces.
+  8-bit kernel reads ("GEMM o Coração Matemático", §12.4 on quantised operands
+  with a scale; the e4m3 field layout is the OCP 8-bit floating-point E4M3
+  format, which the pages do not define, pinned against torch's
+  float8_e4m3fn).
+* :func:`silu`, :func:`f16_to_f64`, :func:`bf16_to_f64`, :func:`e4m3_to_f64`,
+  :func:`round_bf16` — the scalar pieces.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` against values and
 properties fixed outside the oracle (the page's worked example, exact integer
@@ -75,7 +78,8 @@ def _load():
             lib.orc_swiglu.argtypes = [vp, i64, vp, vp, i64, i64, i64, i64, vp, i64, vp, i64,
                                        vp, i32]
             lib.orc_swiglu.restype = i32
-            lib.orc_mlp.argtypes = [vp, vp, vp, vp, vp, f64, i64, i64, i64, vp, i64, vp, i32]
+            lib.orc_mlp.argtypes = [vp, vp, vp, vp, vp, f64, i64, i64, i64, vp, i64, vp, i32,
+                                    i32]
             lib.orc_mlp.restype = i32
             lib.orc_swiglu_typed.argtypes = [vp, vp, vp, i32, f64, i64, i64, i64, vp, i64, vp,
                                              i64, vp, i32]
@@ -86,6 +90,8 @@ def _load():
             lib.orc_e4m3_to_f64.restype = f64
             lib.orc_interleave.argtypes = [vp, vp, vp, i64, i64]
             lib.orc_interleave.restype = None
+            lib.orc_round_bf16.argtypes = [f64]
+            lib.orc_round_bf16.restype = f64
             lib.orc_silu.argtypes = [f64]
             lib.orc_silu.restype = f64
             lib.orc_f16_to_f64.argtypes = [ctypes.c_uint16]
@@ -186,17 +192,19 @@ def swiglu(A, W1, W2, M: int, N: int, K: int, rows=None, threads: int = 0,
 
 
 def mlp(A, W1, W2, Wd, M: int, N: int, K: int, beta: float = 0.0, Out_old=None, rows=None,
-        threads: int = 0) -> np.ndarray:
+        threads: int = 0, round_y: bool = False) -> np.ndarray:
     """Out = (SiLU(A W1) (.) (A W2)) W_down + beta * Out_old in double: A is
     M x K, W1 and W2 K x N, W_down N x K, Out_old M x K, all bf16 (Out_old read
-    only when beta != 0).  The gated activation is not rounded."""
+    only when beta != 0).  The gated activation Y stays in double, or with
+    round_y is rounded to bf16 (round-to-nearest-even, :func:`round_bf16`)
+    before the down projection, as the product stores it."""
     lib = _load()
     a, w1, w2, wd = (_as_buffer(x, "bf16") for x in (A, W1, W2, Wd))
     o = _as_buffer(Out_old, "bf16") if beta != 0.0 else None
     r, n_rows = _rows(rows, M)
     out = np.empty((n_rows, K), dtype=np.float64)
     rc = lib.orc_mlp(_ptr(a), _ptr(w1), _ptr(w2), _ptr(wd), _ptr(o), float(beta), M, N, K,
-                     _ptr(r), n_rows, out.ctypes.data, int(threads))
+                     _ptr(r), n_rows, out.ctypes.data, int(threads), 1 if round_y else 0)
     if rc != 0:
         raise ValueError("oracle mlp rejected its arguments")
     return out
@@ -241,6 +249,11 @@ def interleave(W1, W2, K: int, N: int) -> np.ndarray:
     out = np.empty((K, 2 * N), dtype=np.uint16)
     lib.orc_interleave(_ptr(w1), _ptr(w2), out.ctypes.data, K, N)
     return out
+
+
+def round_bf16(x: float) -> float:
+    """x rounded once to the nearest bfloat16 value, ties to even."""
+    return _load().orc_round_bf16(float(x))
 
 
 def silu(x: float) -> float:

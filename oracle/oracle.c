@@ -82,7 +82,11 @@ double orc_bf16_to_f64(uint16_t b)
 
 /* e4m3: 1 sign, 4 exponent bits (bias 7), 3 fraction bits; no infinities,
  * exponent and fraction all ones is NaN, so the largest value is
- * 1.75 * 2^8 = 448 ("GEMM o Coração Matemático", §12.4 on 8-bit formats). */
+ * 1.75 * 2^8 = 448.  The field layout is the E4M3 encoding of the OCP 8-bit
+ * floating-point format (the one torch's float8_e4m3fn implements, against
+ * which this decoder is pinned on all 256 patterns); the pages define no
+ * 8-bit layout -- "GEMM o Coração Matemático", §12.4 covers only quantised
+ * operands with a scale. */
 double orc_e4m3_to_f64(uint8_t b)
 {
     int sign = (b >> 7) & 1;
@@ -286,24 +290,51 @@ int orc_num_cores(void)
     return c > 0 ? (int)c : 1;
 }
 
+/* ---- rounding to bfloat16 -------------------------------------------- */
+
+/* x rounded to the nearest bfloat16 value, ties to the one whose last
+ * fraction bit is 0 (IEEE round-to-nearest-even), directly from the double
+ * (one rounding).  bfloat16 keeps 8 significant bits (1 implicit + 7 stored)
+ * over binary32's exponent range: normal values from 2^-126, subnormals in
+ * steps of 2^-133, largest finite (2 - 2^-7) * 2^127; larger magnitudes after
+ * rounding become infinities.  Used where the product stores an intermediate
+ * in bfloat16 (the gated activation between the MLP's two GEMMs). */
+double orc_round_bf16(double x)
+{
+    if (isnan(x) || isinf(x) || x == 0.0) return x;
+    int e;
+    (void)frexp(x, &e);                  /* |x| = m * 2^e, 0.5 <= m < 1 */
+    int q = e - 8;                       /* 8 significant bits: step 2^(e-8) */
+    if (q < -133) q = -133;              /* subnormal range: fixed step 2^-133 */
+    double r = ldexp(nearbyint(ldexp(x, -q)), q);   /* default mode: ties to even */
+    if (fabs(r) >= ldexp(1.0, 128)) r = x > 0 ? INFINITY : -INFINITY;
+    return r;
+}
+
 /* ---- full gated MLP -------------------------------------------------- */
 
-/* Out = Y * W_down + beta * Out_old with Y = SiLU(A W1) (.) (A W2) kept in
- * double (not rounded).  The FFN of "GEMM o Coração Matemático", §13.3 (two
- * GEMMs around an activation), with the gated activation of "Sobreposição de
- * Ativação em Nível de Tile ...", Definição do Problema.  A: M x K bf16,
- * W1/W2: K x N bf16, W_down: N x K bf16, Out_old: M x K bf16 (read only when
- * beta != 0).  Out: n_rows x K doubles for rows[] (all when rows == NULL). */
+/* Out = Y * W_down + beta * Out_old with Y = SiLU(A W1) (.) (A W2).  The FFN
+ * of "GEMM o Coração Matemático", §13.3 (two GEMMs around an activation),
+ * with the gated activation of "Sobreposição de Ativação em Nível de Tile
+ * ...", Definição do Problema.  A: M x K bf16, W1/W2: K x N bf16, W_down:
+ * N x K bf16, Out_old: M x K bf16 (read only when beta != 0).  Out: n_rows x K
+ * doubles for rows[] (all when rows == NULL).  round_y == 0 keeps Y in
+ * double; round_y == 1 rounds each exact Y to bfloat16 (orc_round_bf16)
+ * before the down projection, as a product that stores Y in bfloat16 between
+ * the two GEMMs does. */
 int orc_mlp(const uint16_t *A, const uint16_t *W1, const uint16_t *W2,
             const uint16_t *Wd, const uint16_t *Out_old, double beta, int64_t M,
             int64_t N, int64_t K, const int64_t *rows, int64_t n_rows,
-            double *Out, int n_threads)
+            double *Out, int n_threads, int round_y)
 {
     if (!rows && n_rows != M) return -1;
     if (n_rows == 0 || K == 0) return 0;
     double *Y = (double *)malloc(sizeof(double) * (size_t)(n_rows * (N > 0 ? N : 1)));
     if (!Y) return -1;
     int rc = orc_swiglu(A, K, W1, W2, N, M, N, K, rows, n_rows, NULL, N, Y, n_threads);
+    if (rc == 0 && round_y)
+        for (int64_t e = 0; e < n_rows * N; ++e)
+            Y[e] = orc_round_bf16(Y[e]);
     if (rc == 0) {
         for (int64_t r = 0; r < n_rows; ++r) {
             const int64_t i = rows ? rows[r] : r;

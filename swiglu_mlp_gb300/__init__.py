@@ -20,7 +20,7 @@ __all__ = [
     "SwgError", "OP_N", "OP_T", "F16_F32OUT", "BF16", "F16", "BF16_F32OUT", "E4M3_BF16OUT",
     "E4M3_F32OUT", "swiglu_mlp_fp8",
     "gemm", "gemm_ex", "gemm_splitk_noalloc", "swiglu_mlp", "swiglu_mlp_dual", "swiglu_mlp_forward", "swiglu_interleave", "status_string",
-    "get_device_error", "launch_count", "shutdown", "gemm_into", "selftest_wait_timeout",
+    "get_device_error", "debug_workspace_guards", "launch_count", "shutdown", "gemm_into", "selftest_wait_timeout",
     "swiglu_mlp_into", "interleave_weights", "library_path", "load",
 ]
 
@@ -97,6 +97,8 @@ def load():
         lib.swg_last_cuda_error.restype = i32
         lib.swg_cuda_error_name.argtypes = [i32]
         lib.swg_cuda_error_name.restype = ctypes.c_char_p
+        lib.swg_debug_workspace_guards.argtypes = [vp, ctypes.POINTER(i64)]
+        lib.swg_debug_workspace_guards.restype = i32
         _lib = lib
         return lib
 
@@ -216,6 +218,15 @@ def selftest_wait_timeout(limit_ns: int, stream=None) -> int:
     """Runs a kernel whose bounded wait is made to run out (see the C header)."""
     return _check(load().swg_selftest_wait_timeout(int(limit_ns), _stream(stream)),
                   "swg_selftest_wait_timeout")
+
+
+def debug_workspace_guards(stream=None) -> int:
+    """Changed guard bytes around the current device's split-K workspaces
+    (only those created under SWG_TEST_WS_GUARD=1; see the C header)."""
+    bad = ctypes.c_int64(0)
+    _check(load().swg_debug_workspace_guards(_stream(stream), ctypes.byref(bad)),
+           "swg_debug_workspace_guards")
+    return int(bad.value)
 
 
 def launch_count() -> int:

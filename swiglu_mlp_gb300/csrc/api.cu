@@ -64,6 +64,16 @@ int launch_status()
 std::atomic<uint64_t> g_launches{0};
 std::mutex g_mu;
 
+}  // namespace
+
+namespace swg {
+std::atomic<unsigned> g_setup_epoch{0};
+}
+
+void noalloc_forget();
+
+namespace {
+
 // Device error word: written by kernels whose bounded waits ran out.
 __device__ int g_err_word;
 
@@ -95,11 +105,25 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct Workspace {
     void *base = nullptr;   // split-K FP32 partials
     size_t bytes = 0;
-    // Smaller workspaces this one replaced.  Work already queued, or a CUDA
-    // graph captured earlier, may still address them, so they are freed only
-    // by swg_shutdown.
+    void *raw = nullptr;    // the allocation: base, or base - kGuardBytes with guards
+    // Smaller workspaces this one replaced (their raw allocations).  Work
+    // already queued, or a CUDA graph captured earlier, may still address
+    // them, so they are freed only by swg_shutdown.
     std::vector<void *> retired;
 };
+
+// Test switch SWG_TEST_WS_GUARD=1: every split-K workspace (and the fixed
+// array of gemm_splitk_noalloc) gets kGuardBytes of kGuardByte before and
+// after it, which swg_debug_workspace_guards checks.  A kernel that wrote
+// past either end of its partials would change them.
+constexpr size_t kGuardBytes = 64 * 1024;
+constexpr unsigned char kGuardByte = 0xA5;
+
+bool ws_guards_enabled()
+{
+    const char *v = std::getenv("SWG_TEST_WS_GUARD");
+    return v && v[0] == '1';
+}
 
 struct DeviceState {
     bool ready = false;
@@ -142,18 +166,56 @@ int workspace(DeviceState *d, cudaStream_t s, size_t bytes, Workspace *&out)
         cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
         if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return cuda_fail();
         if (cs != cudaStreamCaptureStatusNone) return SWG_ERR_UNSUPPORTED;
+        const bool guards = ws_guards_enabled();
+        const size_t extra = guards ? 2 * kGuardBytes : 0;
         void *p = nullptr;
-        if (cudaMalloc(&p, bytes) != cudaSuccess) {
+        if (cudaMalloc(&p, bytes + extra) != cudaSuccess) {
             cudaGetLastError();
             return SWG_ERR_NO_MEMORY;
         }
-        if (w.base) w.retired.push_back(w.base);
-        w.base = p;
+        if (guards) {
+            uint8_t *b = static_cast<uint8_t *>(p);
+            if (cudaMemsetAsync(b, kGuardByte, kGuardBytes, s) != cudaSuccess ||
+                cudaMemsetAsync(b + kGuardBytes + bytes, kGuardByte, kGuardBytes, s) !=
+                    cudaSuccess) {
+                cudaFree(p);
+                return cuda_fail();
+            }
+        }
+        if (w.raw) w.retired.push_back(w.raw);
+        w.raw = p;
+        w.base = static_cast<uint8_t *>(p) + (guards ? kGuardBytes : 0);
         w.bytes = bytes;
     }
     out = &w;
     return SWG_OK;
 }
+
+// Where a split-K call's FP32 partials go: the (device, stream) workspace
+// above, or -- for gemm_splitk_noalloc -- a fixed array of `bytes` bytes at
+// `base` that belongs to the library's device image.
+struct FixedScratch {
+    float *base;
+    size_t bytes;
+};
+
+int split_workspace(DeviceState *d, cudaStream_t s, size_t bytes, const FixedScratch *fx,
+                    float *&out)
+{
+    if (fx) {
+        if (bytes > fx->bytes) return SWG_ERR_UNSUPPORTED;   // partials would not fit
+        out = fx->base;
+        return SWG_OK;
+    }
+    Workspace *w = nullptr;
+    if (int rc = workspace(d, s, bytes, w)) return rc;
+    out = static_cast<float *>(w->base);
+    return SWG_OK;
+}
+
+// The fixed array of gemm_splitk_noalloc on the current device (defined at
+// the end of this file); called after argument validation.
+int noalloc_scratch(cudaStream_t s, FixedScratch &out);
 
 // Tuning and testing: SWG_MN_3D=0 keeps two 2-D boxes per MN-major operand
 // and stage instead of one 3-D box.
@@ -410,7 +472,7 @@ TileChoice choose_tiles(DeviceState *d, int kind, int64_t M, int64_t N, const in
 int splitk_swapped(DeviceState *d, const TypeInfo &ti, int transA, int transB, int64_t M,
                    int64_t N, int64_t K, float alpha, const void *A, int64_t lda, const void *B,
                    int64_t ldb, float beta, void *C, int64_t ldc, int split_k, cudaStream_t s,
-                   bool fp8 = false)
+                   bool fp8, const FixedScratch *fx)
 {
     const int bk = fp8 ? 128 : swg::BK;
     const int64_t kb = cdiv(K, bk);
@@ -449,8 +511,9 @@ int splitk_swapped(DeviceState *d, const TypeInfo &ti, int transA, int transB, i
     if (b3) tb = t3;
 
     const int64_t ld_ws = cdiv(N, 4) * 4;
-    Workspace *w = nullptr;
-    if (int rc = workspace(d, s, sizeof(float) * (size_t)splits * (size_t)M * (size_t)ld_ws, w))
+    float *ws = nullptr;
+    if (int rc = split_workspace(d, s, sizeof(float) * (size_t)splits * (size_t)M * (size_t)ld_ws,
+                                 fx, ws))
         return rc;
 
     TileParams p{};           // in the kernel's (transposed) frame
@@ -471,7 +534,7 @@ int splitk_swapped(DeviceState *d, const TypeInfo &ti, int transA, int transB, i
     p.idesc = make_idesc(fp8 ? false : ti.in_bf16, aT_mn, bT_mn, swg::BM, bn);
     p.a_mn_major = aT_mn;
     p.b_mn_major = bT_mn;
-    p.ws = static_cast<float *>(w->base);
+    p.ws = ws;
     p.ld_ws = ld_ws;
     p.err = d->err;
     const int grid = (int)std::min<int64_t>(p.units, d->sms);
@@ -722,7 +785,8 @@ int swg_selftest_wait_timeout(int64_t limit_ns, void *stream)
 // both K-major; per-tensor dequantisation scales are folded into alpha.
 static int gemm_fp8(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
                     const void *A, int64_t lda, const void *B, int64_t ldb, float beta, void *C,
-                    int64_t ldc, int out_kind, int out_bytes, int split_k, void *stream)
+                    int64_t ldc, int out_kind, int out_bytes, int split_k, void *stream,
+                    bool noalloc)
 {
     if ((transA != SWG_OP_N && transA != SWG_OP_T) || (transB != SWG_OP_N && transB != SWG_OP_T))
         return SWG_ERR_INVALID_ARG;
@@ -739,9 +803,15 @@ static int gemm_fp8(int transA, int transB, int64_t M, int64_t N, int64_t K, flo
     if (K > 0 && (!aligned16(A) || !aligned16(B) || lda % 16 != 0 || ldb % 16 != 0))
         return SWG_ERR_MISALIGNED;
 
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    FixedScratch fxs{};
+    const FixedScratch *fx = nullptr;
+    if (noalloc) {
+        if (int rc = noalloc_scratch(s, fxs)) return rc;
+        fx = &fxs;
+    }
     DeviceState *d = nullptr;
     if (int rc = device_state(d)) return rc;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0) {
         scale_kernel<<<grid_for(M * N, d->sms), 256, 0, s>>>(C, ldc, (int)M, (int)N, beta, out_kind);
         g_launches++;
@@ -762,7 +832,7 @@ static int gemm_fp8(int transA, int transB, int64_t M, int64_t N, int64_t K, flo
         if (split_k > 1 || (kb >= 8 && swapped_tiles * 2 <= d->sms)) {
             TypeInfo ti{false, out_kind, out_bytes};
             return splitk_swapped(d, ti, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta,
-                                  C, ldc, split_k, s, true);
+                                  C, ldc, split_k, s, true, fx);
         }
     }
     static const int cands[] = {256, 128};
@@ -806,14 +876,16 @@ static int gemm_fp8(int transA, int transB, int64_t M, int64_t N, int64_t K, flo
     return SWG_OK;
 }
 
-int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha, const void *A,
-            int64_t lda, const void *B, int64_t ldb, float beta, void *C, int64_t ldc, int dtype,
-            int split_k, void *stream)
+// gemm_ex and gemm_splitk_noalloc: one plan (kernels, tiles, split) for
+// both; they differ only in where split-K partials go (fx).
+static int gemm_impl(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
+                     const void *A, int64_t lda, const void *B, int64_t ldb, float beta, void *C,
+                     int64_t ldc, int dtype, int split_k, void *stream, bool noalloc)
 {
     if (dtype == SWG_E4M3_BF16OUT || dtype == SWG_E4M3_F32OUT)
         return gemm_fp8(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
                         dtype == SWG_E4M3_BF16OUT ? swg::OUT_BF16 : swg::OUT_F32,
-                        dtype == SWG_E4M3_BF16OUT ? 2 : 4, split_k, stream);
+                        dtype == SWG_E4M3_BF16OUT ? 2 : 4, split_k, stream, noalloc);
     TypeInfo ti;
     if (!type_info(dtype, ti)) return SWG_ERR_UNSUPPORTED;
     if ((transA != SWG_OP_N && transA != SWG_OP_T) || (transB != SWG_OP_N && transB != SWG_OP_T))
@@ -831,9 +903,15 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
     if (K > 0 && (!aligned16(A) || !aligned16(B) || (lda * 2) % 16 != 0 || (ldb * 2) % 16 != 0))
         return SWG_ERR_MISALIGNED;
 
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    FixedScratch fxs{};
+    const FixedScratch *fx = nullptr;
+    if (noalloc) {
+        if (int rc = noalloc_scratch(s, fxs)) return rc;
+        fx = &fxs;
+    }
     DeviceState *d = nullptr;
     if (int rc = device_state(d)) return rc;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     if (K == 0) {
         scale_kernel<<<grid_for(M * N, d->sms), 256, 0, s>>>(C, ldc, (int)M, (int)N, beta,
@@ -888,7 +966,7 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
     // become its N (smaller stages, deeper pipeline, fewer partials).
     if (splits > 1 && M <= 64)
         return splitk_swapped(d, ti, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C,
-                              ldc, split_k, static_cast<cudaStream_t>(stream));
+                              ldc, split_k, static_cast<cudaStream_t>(stream), false, fx);
     int kbps = (int)kb;
     if (splits > 1) {
         kbps = (int)cdiv(kb, splits);
@@ -941,11 +1019,12 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
     if (splits > 1) {
         const int units = (int)std::min<int64_t>(p.units, slots);
         const int64_t ld_ws = cdiv(N, 4) * 4;
-        Workspace *w = nullptr;
-        if (int rc = workspace(d, s, sizeof(float) * (size_t)splits * (size_t)M * (size_t)ld_ws,
-                               w))
+        float *ws = nullptr;
+        if (int rc = split_workspace(d, s,
+                                     sizeof(float) * (size_t)splits * (size_t)M * (size_t)ld_ws,
+                                     fx, ws))
             return rc;
-        p.ws = static_cast<float *>(w->base);
+        p.ws = ws;
         p.ld_ws = ld_ws;
         // Each CTA's last partial tile leaves through shared memory and TMA
         // stores into ws viewed as [splits][M][ld_ws].
@@ -971,6 +1050,14 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha
     if (e != cudaSuccess) return cuda_fail();
     g_launches++;
     return SWG_OK;
+}
+
+int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha, const void *A,
+            int64_t lda, const void *B, int64_t ldb, float beta, void *C, int64_t ldc, int dtype,
+            int split_k, void *stream)
+{
+    return gemm_impl(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtype, split_k,
+                     stream, false);
 }
 
 int gemm(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha, const void *A,
@@ -1271,70 +1358,108 @@ const char *swg_cuda_error_name(int code)
 
 void swg_shutdown(void)
 {
-    std::lock_guard<std::mutex> lk(g_mu);
-    int cur = 0;
-    const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
-    for (auto &dv : g_dev) {
-        bool any = false;
-        for (auto &kv : dv.second.ws) any = any || kv.second.base != nullptr;
-        if (!any) continue;
-        if (cudaSetDevice(dv.first) != cudaSuccess) continue;
-        for (auto &kv : dv.second.ws) {
-            if (kv.second.base) cudaFree(kv.second.base);
-            for (void *r : kv.second.retired) cudaFree(r);
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        int cur = 0;
+        const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+        for (auto &dv : g_dev) {
+            bool any = false;
+            for (auto &kv : dv.second.ws) any = any || kv.second.raw != nullptr;
+            if (any && cudaSetDevice(dv.first) == cudaSuccess) {
+                for (auto &kv : dv.second.ws) {
+                    if (kv.second.raw) cudaFree(kv.second.raw);
+                    for (void *r : kv.second.retired) cudaFree(r);
+                }
+            }
+            dv.second.ws.clear();
+            // Device addresses, occupancy figures and kernel attributes are
+            // looked up again by the next call: after a cudaDeviceReset the
+            // cached ones would be stale.
+            dv.second.ready = false;
+            dv.second.max_pairs.clear();
         }
-        dv.second.ws.clear();
+        if (have_cur) cudaSetDevice(cur);
+        swg::g_setup_epoch.fetch_add(1);
     }
-    if (have_cur) cudaSetDevice(cur);
+    noalloc_forget();
 }
 
 }  // extern "C"
 
-// =================================================================== no-allocation split-K
+// =================================================================== no-allocation GEMM
 //
-// gemm_splitk_noalloc runs the same split-K kernels as gemm_ex, but its FP32
-// partial sums live in a fixed array that is part of the library's device
-// image instead of in a workspace obtained with cudaMalloc.  It is for callers
-// that must not allocate device memory once they are running: for example a
-// host framework that has already reserved nearly all device memory in its
-// own pool (so a cudaMalloc would fail or fragment it), or a serving loop
-// that forbids cudaMalloc/cudaFree because they can synchronise the device.
+// gemm_splitk_noalloc runs exactly what gemm_ex plans for the same arguments
+// (the same kernels, tile shapes, split count and fixed-order reduction), but
+// a split-K call keeps its FP32 partial sums in a fixed array that is part of
+// the library's device image instead of a workspace from cudaMalloc.  It is
+// for callers that must not allocate device memory once they are running:
+// for example a host framework that has already reserved nearly all device
+// memory in its own pool (a cudaMalloc would fail, or fragment that pool), or
+// a serving loop that forbids cudaMalloc/cudaFree because they can
+// synchronise the whole device.
 
 namespace {
 
+constexpr size_t kNoallocGuardFloats = kGuardBytes / sizeof(float);
 constexpr size_t kNoallocScratchFloats = SWG_NOALLOC_SCRATCH_BYTES / sizeof(float);
 
-// The partials.  Every GPU that loads this library holds these bytes until
-// the process exits.  All calls share them; a call overwrites every element it
-// later reads, so nothing here needs to start at zero.
-static __device__ __align__(256) float g_noalloc_scratch[kNoallocScratchFloats];
+// The partials, between two guard bands of kGuardBytes that no kernel writes
+// (filled and checked only under SWG_TEST_WS_GUARD=1).  Every GPU on which
+// the library's kernels are loaded holds these bytes until the process exits.
+// All calls share them; a call writes every partial it later reads, so
+// nothing here has to start at zero.
+static __device__ __align__(256) float
+    g_noalloc_scratch[kNoallocGuardFloats + kNoallocScratchFloats + kNoallocGuardFloats];
 
 constexpr int kNoallocMaxDevices = 64;
 std::mutex g_noalloc_mu;
 bool g_noalloc_ready[kNoallocMaxDevices];
+bool g_noalloc_guarded[kNoallocMaxDevices];
 float *g_noalloc_ptr[kNoallocMaxDevices];   // device address of g_noalloc_scratch
-int *g_noalloc_err[kNoallocMaxDevices];     // device address of g_err_word
-int g_noalloc_sms[kNoallocMaxDevices];
 
-// Once per device, with that device current: the device addresses of the
-// scratch array and of the error word.  In host code the symbols themselves
-// are host-side stand-ins, so kernels must be given these addresses instead.
-int noalloc_setup(int &dev)
+// Once per device, with that device current: the array's device address.
+// In host code the symbol g_noalloc_scratch is a host-side stand-in, not a
+// device address, so kernels are given this address instead.  swg_shutdown
+// forgets it (a cudaDeviceReset invalidates it).
+int noalloc_setup(int &dev, cudaStream_t s)
 {
     if (int rc = current_device(dev)) return rc;
     if (dev < 0 || dev >= kNoallocMaxDevices) return SWG_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     if (g_noalloc_ready[dev]) return SWG_OK;
-    void *scratch = nullptr, *err = nullptr;
+    void *scratch = nullptr;
     if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess) return cuda_fail();
-    if (cudaGetSymbolAddress(&err, g_err_word) != cudaSuccess) return cuda_fail();
-    int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return cuda_fail();
     g_noalloc_ptr[dev] = static_cast<float *>(scratch);
-    g_noalloc_err[dev] = static_cast<int *>(err);
-    g_noalloc_sms[dev] = sms;
+    g_noalloc_guarded[dev] = false;
+    if (ws_guards_enabled()) {
+        uint8_t *b = static_cast<uint8_t *>(scratch);
+        if (cudaMemsetAsync(b, kGuardByte, kGuardBytes, s) != cudaSuccess ||
+            cudaMemsetAsync(b + kGuardBytes + SWG_NOALLOC_SCRATCH_BYTES, kGuardByte, kGuardBytes,
+                            s) != cudaSuccess)
+            return cuda_fail();
+        g_noalloc_guarded[dev] = true;
+    }
     g_noalloc_ready[dev] = true;
+    return SWG_OK;
+}
+
+// Number of bytes in [p, p + n) on the device that differ from kGuardByte
+// (-1 if they cannot be read).
+int64_t guard_damage(const void *p, size_t n)
+{
+    std::vector<unsigned char> h(n);
+    if (cudaMemcpy(h.data(), p, n, cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
+    int64_t bad = 0;
+    for (unsigned char c : h) bad += c != kGuardByte;
+    return bad;
+}
+
+int noalloc_scratch(cudaStream_t s, FixedScratch &out)
+{
+    int dev = 0;
+    if (int rc = noalloc_setup(dev, s)) return rc;
+    out.base = g_noalloc_ptr[dev] + kNoallocGuardFloats;
+    out.bytes = SWG_NOALLOC_SCRATCH_BYTES;
     return SWG_OK;
 }
 
@@ -1346,93 +1471,57 @@ int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N, int64_t K,
                         const void *A, int64_t lda, const void *B, int64_t ldb, float beta,
                         void *C, int64_t ldc, int dtype, int split_k, void *stream)
 {
-    TypeInfo ti;
-    if (!type_info(dtype, ti)) return SWG_ERR_UNSUPPORTED;
-    if ((transA != SWG_OP_N && transA != SWG_OP_T) || (transB != SWG_OP_N && transB != SWG_OP_T))
-        return SWG_ERR_INVALID_ARG;
-    if (M < 0 || N < 0 || K < 0 || split_k < 0) return SWG_ERR_INVALID_ARG;
-    if (M == 0 || N == 0) return SWG_OK;
-    const int64_t a_cols = transA ? M : K, b_cols = transB ? K : N;
-    if (C == nullptr || ldc < N) return SWG_ERR_INVALID_ARG;
-    if (K > 0 && (A == nullptr || B == nullptr || lda < a_cols || ldb < b_cols))
-        return SWG_ERR_INVALID_ARG;
-    if (M > kMaxDim || N > kMaxDim || K > kMaxDim || ldc > kMaxDim || lda > kMaxDim ||
-        ldb > kMaxDim)
-        return SWG_ERR_UNSUPPORTED;
-    if (!aligned16(C) || (ldc * ti.out_bytes) % 16 != 0) return SWG_ERR_MISALIGNED;
-    if (K > 0 && (!aligned16(A) || !aligned16(B) || (lda * 2) % 16 != 0 || (ldb * 2) % 16 != 0))
-        return SWG_ERR_MISALIGNED;
+    // Arguments are validated (before any CUDA call) and planned exactly as
+    // by gemm_ex; the array's set-up follows validation.
+    return gemm_impl(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtype, split_k,
+                     stream, true);
+}
 
-    // Split factor, as gemm_ex chooses it, but never below one range.
-    const int64_t kb = cdiv(K, swg::BK);
-    const int64_t tiles = cdiv(M, swg::BM) * cdiv(N, 256);
-    int splits = 1;
+int swg_debug_workspace_guards(void *stream, int64_t *bad_bytes)
+{
+    if (bad_bytes == nullptr) return SWG_ERR_INVALID_ARG;
+    *bad_bytes = 0;
     int dev = 0;
-    if (int rc = noalloc_setup(dev)) return rc;
-    const int sms = g_noalloc_sms[dev];
-    if (split_k == 0) {
-        if (tiles * 2 <= sms && kb >= 8) splits = (int)std::min<int64_t>(sms / tiles, kb / 4);
-    } else {
-        splits = (int)std::min<int64_t>(split_k, kb);
+    if (int rc = current_device(dev)) return rc;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess)
+        return cuda_fail();
+    int64_t bad = 0;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_dev.find(dev);
+        if (it != g_dev.end()) {
+            for (auto &kv : it->second.ws) {
+                const Workspace &w = kv.second;
+                if (!w.raw || w.raw == w.base) continue;          // allocated without guards
+                const uint8_t *lo = static_cast<const uint8_t *>(w.raw);
+                const int64_t a = guard_damage(lo, kGuardBytes);
+                const int64_t b = guard_damage(lo + kGuardBytes + w.bytes, kGuardBytes);
+                if (a < 0 || b < 0) return cuda_fail();
+                bad += a + b;
+            }
+        }
     }
-    splits = std::max(1, std::min(splits, swg::MAX_SPLITS));
-    int kbps = (int)std::max<int64_t>(kb, 1);
-    if (kb > 0) {
-        kbps = (int)cdiv(kb, splits);
-        splits = (int)cdiv(kb, kbps);
+    {
+        std::lock_guard<std::mutex> lk(g_noalloc_mu);
+        if (dev < kNoallocMaxDevices && g_noalloc_ready[dev] && g_noalloc_guarded[dev]) {
+            const uint8_t *lo = reinterpret_cast<const uint8_t *>(g_noalloc_ptr[dev]);
+            const int64_t a = guard_damage(lo, kGuardBytes);
+            const int64_t b = guard_damage(lo + kGuardBytes + SWG_NOALLOC_SCRATCH_BYTES,
+                                           kGuardBytes);
+            if (a < 0 || b < 0) return cuda_fail();
+            bad += a + b;
+        }
     }
-    const int64_t ld_ws = cdiv(N, 4) * 4;
-    if ((uint64_t)splits * (uint64_t)M * (uint64_t)ld_ws > kNoallocScratchFloats)
-        return SWG_ERR_UNSUPPORTED;   // partials would not fit in the fixed array
-
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (K == 0) {
-        scale_kernel<<<grid_for(M * N, sms), 256, 0, s>>>(C, ldc, (int)M, (int)N, beta,
-                                                           ti.out_kind);
-        g_launches++;
-        return launch_status();
-    }
-
-    const int bn = 256;
-    const bool a_mn = transA == SWG_OP_T;
-    const bool b_mn = transB == SWG_OP_N;
-    CUtensorMap ta, tb;
-    bool ok = a_mn ? make_tmap(&ta, A, ti.in_bf16, M, K, lda, 64)
-                   : make_tmap(&ta, A, ti.in_bf16, K, M, lda, swg::BM);
-    ok = ok && (b_mn ? make_tmap(&tb, B, ti.in_bf16, N, K, ldb, 64)
-                     : make_tmap(&tb, B, ti.in_bf16, K, N, ldb, bn));
-    if (!ok) return cuda_fail();
-
-    TileParams p{};
-    p.M = (int)M;
-    p.N = (int)N;
-    p.K = (int)K;
-    p.m_blocks = (int)cdiv(M, swg::BM);
-    p.n_blocks = (int)cdiv(N, bn);
-    p.k_blocks = (int)kb;
-    p.bk = swg::BK;
-    p.tiles = p.m_blocks * p.n_blocks;
-    p.splits = splits;
-    p.kb_per_split = kbps;
-    p.units = p.tiles * splits;
-    p.group_m = 16;
-    p.idesc = make_idesc(ti.in_bf16, a_mn, b_mn, swg::BM, bn);
-    p.a_mn_major = a_mn;
-    p.b_mn_major = b_mn;
-    p.alpha = alpha;
-    p.beta = beta;
-    p.D = C;
-    p.ldd = ldc;
-    p.out_kind = ti.out_kind;
-    p.ws = g_noalloc_ptr[dev];
-    p.ld_ws = ld_ws;
-    p.err = g_noalloc_err[dev];
-    const int grid = (int)std::min<int64_t>(p.units, sms);
-    if (swg::launch_tc_splitk(bn, false, ta, tb, p, grid, s) != cudaSuccess) return cuda_fail();
-    g_launches++;
-    if (swg::launch_splitk_reduce(p, sms, s) != cudaSuccess) return cuda_fail();
-    g_launches++;
+    *bad_bytes = bad;
     return SWG_OK;
 }
 
 }  // extern "C"
+
+// Forgets the device addresses cached by gemm_splitk_noalloc (swg_shutdown).
+void noalloc_forget()
+{
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    for (int i = 0; i < kNoallocMaxDevices; ++i) g_noalloc_ready[i] = false;
+}

@@ -2,7 +2,9 @@
 // and kind::f8f6f4 MMAs: the plain GEMM epilogue, the interleaved SwiGLU
 // epilogue, and the swapped-operand split-K partials for few rows (decode).
 // Per-tensor dequantisation scales arrive folded into alpha.
-// Quantised operands: "GEMM o Coração Matemático", §12.4; the SwiGLU page
+// Quantised operands with a scale: "GEMM o Coração Matemático", §12.4 (the
+// 8-bit layout itself is the OCP E4M3 format, which the pages do not
+// define); the SwiGLU page
 // ("Sobreposição de Ativação ...", Definição do Problema) notes that FP8 /
 // INT4 raise the relative cost of the memory-bound activation step.
 #include "launch_impl.cuh"

@@ -535,17 +535,16 @@ template <int MR, bool B_KN, int IK, bool DUAL = false>
 cudaError_t launch_gemv_impl(const CUtensorMap &tmB, const CUtensorMap &tmB2, const GemvArgs &g,
                              int col_blocks, cudaStream_t s)
 {
-    static std::atomic<unsigned long long> configured{0};
+    static DeviceOnce configured;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const unsigned long long bit = 1ull << (dev & 63);
     auto kernel = gemv_kernel<MR, B_KN, IK, DUAL>;
-    if (!(configured.load() & bit)) {
+    if (configured.needed(dev)) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  GV_MAX_SMEM);
         if (e != cudaSuccess) return e;
-        configured.fetch_or(bit);
+        configured.mark(dev);
     }
     constexpr int CW = B_KN ? KN_CW : nk_rows(esize<IK>());
     cudaLaunchConfig_t cfg = {};

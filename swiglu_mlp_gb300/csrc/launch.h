@@ -5,9 +5,30 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "tc_gemm.cuh"
 
 namespace swg {
+
+// Launch set-up done once per kernel and device (the dynamic shared-memory
+// opt-in).  swg_shutdown advances g_setup_epoch, so set-up cached before it is
+// done again on the next launch -- after a cudaDeviceReset, which clears
+// function attributes, it has to be.
+extern std::atomic<unsigned> g_setup_epoch;
+
+struct DeviceOnce {
+    static constexpr int kDevices = 64;
+    std::atomic<unsigned> done[kDevices] = {};      // epoch + 1 of the last set-up
+    bool needed(int dev) const
+    {
+        return dev < 0 || dev >= kDevices || done[dev].load() != g_setup_epoch.load() + 1u;
+    }
+    void mark(int dev)
+    {
+        if (dev >= 0 && dev < kDevices) done[dev].store(g_setup_epoch.load() + 1u);
+    }
+};
 
 // Launch the persistent tcgen05 kernel with the given epilogue.  `bn` is one
 // of the tile widths the TU instantiates (anything else returns

@@ -15,17 +15,16 @@ cudaError_t launch_tc_impl(const CUtensorMap &ta, const CUtensorMap &tb, const C
                            const TileParams &p, int units, cudaStream_t s)
 {
     using C = Cfg<BN, PAIR>;
-    static std::atomic<unsigned long long> configured{0};
+    static DeviceOnce configured;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const unsigned long long bit = 1ull << (dev & 63);
     auto kernel = tc_gemm_kernel<BN, EPI, PAIR, FP8>;
-    if (!(configured.load() & bit)) {
+    if (configured.needed(dev)) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        configured.fetch_or(bit);
+        configured.mark(dev);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(NUM_THREADS);

@@ -21,6 +21,66 @@ def round_up(x: int, m: int) -> int:
     return (x + m - 1) // m * m
 
 
+# Guard bands around outputs (a stand-in for a memory checker, which is not
+# available on the GPU pool): sentinel bit patterns -- NaNs with a payload no
+# kernel computes -- fill the rows above and below an output and the columns
+# right of it up to its row stride; after the call every sentinel must be
+# unchanged.  Tiled kernels go wrong at their edges ("GEMM o Coração
+# Matemático", §4.2), e.g. a staged TMA store built with a wrong extent.
+_SENTINEL = {torch.bfloat16: (torch.int16, 0x7FA5), torch.float16: (torch.int16, 0x7E5A),
+             torch.float32: (torch.int32, 0x7FA5A5A5)}
+GUARD_ROWS_ABOVE = 4
+GUARD_ROWS_BELOW = 130          # more than one 128-row tile
+GUARD_COLS_BYTES = 128          # one TMA store box
+
+
+class Guarded:
+    """A rows x cols output inside a larger device allocation of sentinels.
+
+    ``view`` is the output (row stride ``ld``) to pass to the library; it
+    holds ``init`` (a rows x cols tensor) or, without one, the value ``fill``.
+    ``ld`` defaults to cols + 128 bytes of guard columns, rounded to 16 bytes;
+    pass ``ld=cols`` where the callee fixes the row stride (then only the rows
+    above and below guard it).  ``check()`` asserts every sentinel unchanged;
+    ``cpu()`` checks and returns the output."""
+
+    def __init__(self, rows, cols, dtype, init=None, fill=None, ld=None,
+                 above=GUARD_ROWS_ABOVE, below=GUARD_ROWS_BELOW, device="cuda"):
+        ity, bits = _SENTINEL[dtype]
+        esz = torch.empty((), dtype=dtype).element_size()
+        if ld is None:
+            ld = round_up(cols + GUARD_COLS_BYTES // esz, 16 // esz)
+        assert ld >= cols and (ld * esz) % 16 == 0, (ld, cols, esz)
+        self.rows, self.cols, self.ld, self.above, self.below = rows, cols, ld, above, below
+        self.dtype, self.ity, self.bits = dtype, ity, bits
+        self.full = torch.full((above + rows + below, ld), bits, dtype=ity,
+                               device=device).view(dtype)
+        self.view = self.full[above:above + rows, :cols]
+        if init is not None:
+            self.view.copy_(init)
+        elif fill is not None:
+            self.view.fill_(fill)
+        # the library may be called on another stream than the one that
+        # filled the buffer
+        torch.cuda.current_stream(self.full.device).synchronize()
+
+    def check(self, what: str = "") -> None:
+        full = self.full.view(self.ity).cpu()
+        a, r = self.above, self.rows
+        regions = [("rows above", full[:a]), ("rows below", full[a + r:]),
+                   ("columns right", full[a:a + r, self.cols:])]
+        for name, reg in regions:
+            bad = reg != self.bits
+            if bool(bad.any()):
+                idx = bad.nonzero()[:5].tolist()
+                raise AssertionError(f"{what}: {int(bad.sum())} guard elements ({name}) "
+                                     f"overwritten, e.g. {idx}")
+
+    def cpu(self, what: str = "") -> torch.Tensor:
+        self.check(what)
+        return self.view.cpu()
+
+
 def padded(t: torch.Tensor, ld: int, fill: float = 0.0) -> torch.Tensor:
     """rows x ld storage holding t in its first columns; the padding carries
     `fill` so a kernel that reads past the row shows it."""
@@ -66,21 +126,3 @@ def report(y: np.ndarray, yhat: np.ndarray) -> dict:
     rel = err / np.maximum(np.abs(yhat), 1e-30)
     return {"max_abs": float(err.max()), "max_rel": float(rel.max()),
             "frac_rel_gt_1pct": float((rel > 1e-2).mean())}
-
-
-def check_two_stage(y, yhat, prop_bound, what=""):
-    """Output of a composition whose intermediate is stored in bf16 (the full
-    MLP: Y in bf16 between its two GEMMs).  The single-GEMM bound is widened by
-    the propagated rounding of the intermediate, prop_bound = 2^-8 * |Y| |W|
-    computed from the oracle's exact intermediate (2^-8 covers the bf16 store,
-    2^-9, plus the FP32 arithmetic before it)."""
-    assert y.shape == yhat.shape
-    assert np.isfinite(y).all(), f"{what}: non-finite outputs"
-    err = np.abs(y - yhat)
-    bound = ATOL + RTOL * np.abs(yhat) + prop_bound
-    bad = err > bound
-    if bad.any():
-        idx = np.argwhere(bad)[:5].tolist()
-        raise AssertionError(f"{what}: {int(bad.sum())} elements out of tolerance, e.g. {idx}; "
-                             f"{report(y, yhat)}")
-    return report(y, yhat)

@@ -147,3 +147,31 @@ def test_selftest_timeout_argument_checks(lib):
     assert lib.swg_selftest_wait_timeout(0, None) == INVALID
     assert lib.swg_selftest_wait_timeout(-5, None) == INVALID
     assert lib.swg_selftest_wait_timeout(2_000_000_000, None) == INVALID
+
+
+def test_noalloc_rejects_bad_arguments_before_any_cuda_call(lib):
+    """gemm_splitk_noalloc validates exactly as gemm_ex does, before its
+    once-per-device set-up, so argument errors are reported without a GPU."""
+    def n(**kw):
+        a = dict(tA=0, tB=0, M=64, N=4096, K=16384, A=P, lda=16384, B=P, ldb=4096, C=P,
+                 ldc=4096, dtype=1, split_k=0)
+        a.update(kw)
+        return lib.gemm_splitk_noalloc(a["tA"], a["tB"], a["M"], a["N"], a["K"],
+                                       ctypes.c_float(1.0), a["A"], a["lda"], a["B"], a["ldb"],
+                                       ctypes.c_float(1.0), a["C"], a["ldc"], a["dtype"],
+                                       a["split_k"], None)
+    assert n(M=-1) == INVALID
+    assert n(split_k=-2) == INVALID
+    assert n(tA=2) == INVALID
+    assert n(A=0) == INVALID
+    assert n(ldc=4000) == INVALID
+    assert n(dtype=9) == UNSUPPORTED
+    assert n(C=P + 8) == MISALIGNED
+    assert n(lda=16388) == MISALIGNED
+    assert n(M=0) == OK and n(N=0) == OK
+    # e4m3 rules are gemm_ex's too: op(A) = A and op(B) = B^T only
+    assert n(dtype=4, tB=0, ldb=16384) == UNSUPPORTED
+
+
+def test_debug_workspace_guards_needs_an_output(lib):
+    assert lib.swg_debug_workspace_guards(None, None) == INVALID

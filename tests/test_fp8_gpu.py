@@ -11,7 +11,7 @@ import torch
 import oracle
 import swiglu_mlp_gb300 as swg
 import synth
-from helpers import check_f32, check_half, to_f64
+from helpers import Guarded, check_f32, check_half, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -39,39 +39,42 @@ def test_fp8_gemm(monkeypatch, tile_mode, M, N, K):
     ldc = ((N + 7) // 8) * 8
     Cp = torch.zeros((M, ldc), dtype=torch.bfloat16)
     Cp[:, :N] = C
-    Cd = Cp.cuda()
-    swg.gemm(0, 1, M, N, K, 1.5 * sa * sb, Ap.cuda(), lda, Bp.cuda(), ldb, 0.5, Cd, ldc,
+    Cg = Guarded(M, N, torch.bfloat16, init=C, ld=ldc)
+    swg.gemm(0, 1, M, N, K, 1.5 * sa * sb, Ap.cuda(), lda, Bp.cuda(), ldb, 0.5, Cg.view, ldc,
              swg.E4M3_BF16OUT)
     assert swg.get_device_error() == 0
-    out = Cd.cpu()
-    assert torch.all(out[:, N:] == 0)
+    out = Cg.cpu(f"fp8 gemm {M}x{N}x{K}")
     yhat = oracle.gemm(0, 1, M, N, K, 1.5 * sa * sb, Ap, lda, Bp, ldb, 0.5, Cp, ldc,
                        in_type="e4m3", c_type="bf16")
-    check_half(to_f64(out[:, :N]), yhat, f"fp8 gemm {tile_mode} {M}x{N}x{K}")
+    check_half(to_f64(out), yhat, f"fp8 gemm {tile_mode} {M}x{N}x{K}")
 
 
 def test_fp8_gemm_f32_out():
     M, N, K = 256, 384, 512
     g = synth.generator(77)
     A, Bt = _e4m3((M, K), g), _e4m3((N, K), g)
-    D = torch.empty((M, N), dtype=torch.float32, device="cuda")
-    swg.gemm(0, 1, M, N, K, 0.25, A.cuda(), K, Bt.cuda(), K, 0.0, D, N, swg.E4M3_F32OUT)
+    D = Guarded(M, N, torch.float32)
+    swg.gemm(0, 1, M, N, K, 0.25, A.cuda(), K, Bt.cuda(), K, 0.0, D.view, D.ld, swg.E4M3_F32OUT)
     assert swg.get_device_error() == 0
     yhat = oracle.gemm(0, 1, M, N, K, 0.25, A, K, Bt, K, 0.0, in_type="e4m3")
-    check_f32(to_f64(D), yhat, K, "fp8 f32 out")
+    check_f32(to_f64(D.cpu("fp8 f32 out")), yhat, K, "fp8 f32 out")
 
 
 def test_fp8_square_8192_sampled():
     M = N = K = 8192
     g = synth.generator(1)
     A, Bt = _e4m3((M, K), g), _e4m3((N, K), g)
-    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    swg.gemm(0, 1, M, N, K, 1.0 / 64, A.cuda(), K, Bt.cuda(), K, 0.0, D, N, swg.E4M3_BF16OUT)
+    D = Guarded(M, N, torch.bfloat16, ld=N)
+    swg.gemm(0, 1, M, N, K, 1.0 / 64, A.cuda(), K, Bt.cuda(), K, 0.0, D.view, N,
+             swg.E4M3_BF16OUT)
     assert swg.get_device_error() == 0
-    assert bool(torch.isfinite(D).all())
-    rows = [0, 255, 256, 4097, M - 1]
+    out = D.cpu("fp8 8192^3")
+    assert bool(torch.isfinite(out).all())
+    rng = np.random.default_rng(8192)
+    rows = sorted({0, 127, 128, 255, 256, 4097, M - 257, M - 256, M - 1,
+                   *rng.integers(0, M, 4).tolist()})
     yhat = oracle.gemm(0, 1, M, N, K, 1.0 / 64, A, K, Bt, K, 0.0, in_type="e4m3", rows=rows)
-    check_half(to_f64(D)[rows], yhat, "fp8 8192^3")
+    check_half(to_f64(out)[rows], yhat, "fp8 8192^3")
 
 
 def test_fp8_layout_rules():
@@ -92,12 +95,13 @@ def test_fp8_swiglu(monkeypatch, tile_mode, M, K, N):
         monkeypatch.setenv("SWG_TILE_MODE", tile_mode)
     A, W1, W2, sw = synth.swiglu_e4m3(M, K, N, seed=M + K + N, w_std=0.05)
     Wt = torch.from_numpy(oracle.interleave_t8(W1, W2, K, N)).view(torch.float8_e4m3fn)
-    Y = torch.full((M, N), 9.0, dtype=torch.bfloat16, device="cuda")
-    swg.swiglu_mlp_fp8(A.cuda(), Wt.cuda(), Y, M, N, K, sw)
+    Y = Guarded(M, N, torch.bfloat16, fill=9.0, ld=N)
+    swg.swiglu_mlp_fp8(A.cuda(), Wt.cuda(), Y.view, M, N, K, sw)
     assert swg.get_device_error() == 0
-    rows = None if M <= 300 else [0, 127, 128, 255, 256, M - 1]
+    rows = None if M <= 300 else [0, 127, 128, 255, 256, 383, 384, 511, 512, M - 1]
     yhat = oracle.swiglu_typed(A, W1, W2, M, N, K, in_type="e4m3", scale=sw, rows=rows)
-    y = to_f64(Y) if rows is None else to_f64(Y)[rows]
+    out = to_f64(Y.cpu(f"fp8 swiglu {M}x{K}x{N}"))
+    y = out if rows is None else out[rows]
     check_half(y, yhat, f"fp8 swiglu {tile_mode} {M}x{K}x{N}")
 
 
@@ -105,12 +109,14 @@ def test_fp8_swiglu_8b_sampled():
     M, K, N = 2048, 4096, 14336
     A, W1, W2, sw = synth.swiglu_e4m3(M, K, N, seed=3)
     Wt = torch.from_numpy(oracle.interleave_t8(W1, W2, K, N)).view(torch.float8_e4m3fn)
-    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    swg.swiglu_mlp_fp8(A.cuda(), Wt.cuda(), Y, M, N, K, sw)
+    Y = Guarded(M, N, torch.bfloat16, ld=N)
+    swg.swiglu_mlp_fp8(A.cuda(), Wt.cuda(), Y.view, M, N, K, sw)
     assert swg.get_device_error() == 0
-    rows = [0, 255, 256, M - 1]
+    rng = np.random.default_rng(2049)
+    rows = sorted({0, 127, 128, 255, 256, M // 2, M - 257, M - 256, M - 1,
+                   *rng.integers(0, M, 4).tolist()})
     yhat = oracle.swiglu_typed(A, W1, W2, M, N, K, in_type="e4m3", scale=sw, rows=rows)
-    check_half(to_f64(Y)[rows], yhat, "fp8 swiglu 8B")
+    check_half(to_f64(Y.cpu("fp8 swiglu 8B"))[rows], yhat, "fp8 swiglu 8B")
 
 
 @pytest.mark.parametrize("M", [1, 7, 16, 33, 64])
@@ -124,16 +130,13 @@ def test_fp8_few_rows_split_k(M, split_k):
     Bt = _e4m3((N, K), g)
     C = synth.normal((M, N), g)
     ldc = 528
-    Cp = torch.zeros((M, ldc), dtype=torch.bfloat16)
-    Cp[:, :N] = C
-    Cd = Cp.cuda()
-    swg.gemm_ex(0, 1, M, N, K, 1.0 / 32, A.cuda(), K, Bt.cuda(), K, 0.5, Cd, ldc,
+    Cg = Guarded(M, N, torch.bfloat16, init=C, ld=ldc)
+    swg.gemm_ex(0, 1, M, N, K, 1.0 / 32, A.cuda(), K, Bt.cuda(), K, 0.5, Cg.view, ldc,
                 swg.E4M3_BF16OUT, split_k)
     assert swg.get_device_error() == 0
-    out = Cd.cpu()
-    assert torch.all(out[:, N:] == 0)
+    out = Cg.cpu(f"fp8 few rows M={M}")
     yhat = oracle.gemm(0, 1, M, N, K, 1.0 / 32, A, K, Bt, K, 0.5, C, N, in_type="e4m3")
-    check_half(to_f64(out[:, :N]), yhat, f"fp8 few rows M={M} split={split_k}")
+    check_half(to_f64(out), yhat, f"fp8 few rows M={M} split={split_k}")
 
 
 def test_fp8_decode_gemv_f32_out_deterministic():

@@ -13,7 +13,7 @@ import torch
 import oracle
 import swiglu_mlp_gb300 as swg
 import synth
-from helpers import check_f32, check_half, padded, round_up, to_f64
+from helpers import Guarded, check_f32, check_half, padded, round_up, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -41,18 +41,15 @@ def run_case(M, N, K, tA, tB, code, alpha, beta, seed, pad=(0, 0, 0), c_fill=Non
     Cp = padded(C, ldc, 5.0)
     if c_fill is not None:
         Cp.fill_(c_fill)
-    Cd = Cp.cuda()
+    # C inside guard bands: rows above and below, and its padding columns
+    Cg = Guarded(M, N, tout, init=Cp[:, :N], ld=ldc)
     Ad, Bd = Ap.cuda(), Bp.cuda()
     if split_k is None:
-        swg.gemm(tA, tB, M, N, K, alpha, Ad, lda, Bd, ldb, beta, Cd, ldc, code)
+        swg.gemm(tA, tB, M, N, K, alpha, Ad, lda, Bd, ldb, beta, Cg.view, ldc, code)
     else:
-        swg.gemm_ex(tA, tB, M, N, K, alpha, Ad, lda, Bd, ldb, beta, Cd, ldc, code, split_k)
+        swg.gemm_ex(tA, tB, M, N, K, alpha, Ad, lda, Bd, ldb, beta, Cg.view, ldc, code, split_k)
     assert swg.get_device_error() == 0
-    out = Cd.cpu()
-    # the padding columns of C must be untouched
-    if ldc > N:
-        assert torch.equal(out[:, N:], Cp[:, N:])
-    y = to_f64(out[:, :N])
+    y = to_f64(Cg.cpu(f"gemm {M}x{N}x{K} tA={tA} tB={tB} code={code}"))
     yhat = oracle.gemm(tA, tB, M, N, K, alpha, Ap, lda, Bp, ldb, beta, Cp, ldc,
                        in_type=oin, c_type=oout, rows=rows)
     if rows is not None:
@@ -70,11 +67,14 @@ def test_config_f16_256_cubed_full():
     """FP16 in, FP32 out: C = 1.5 A B + 0.5 C, 256^3, U(-1,1) inputs, seed 0."""
     M = N = K = 256
     A, B, C = synth.gemm_f16_small(seed=0)
-    Ad, Bd, Cd = A.cuda(), B.cuda(), C.cuda()
-    swg.gemm(0, 0, M, N, K, 1.5, Ad, K, Bd, N, 0.5, Cd, N, swg.F16_F32OUT)
-    assert swg.get_device_error() == 0
-    yhat = oracle.gemm(0, 0, M, N, K, 1.5, A, K, B, N, 0.5, C, N, in_type="f16", c_type="f32")
-    check_f32(to_f64(Cd), yhat, K, "f16 256^3")
+    Ad, Bd = A.cuda(), B.cuda()
+    for ld in (N, N + 32):                  # the benchmark's ldc = N, and a guarded pad
+        Cg = Guarded(M, N, torch.float32, init=C, ld=ld)
+        swg.gemm(0, 0, M, N, K, 1.5, Ad, K, Bd, N, 0.5, Cg.view, ld, swg.F16_F32OUT)
+        assert swg.get_device_error() == 0
+        yhat = oracle.gemm(0, 0, M, N, K, 1.5, A, K, B, N, 0.5, C, N, in_type="f16",
+                           c_type="f32")
+        check_f32(to_f64(Cg.cpu("f16 256^3")), yhat, K, f"f16 256^3 ldc={ld}")
 
 
 @pytest.mark.parametrize("tA", [0, 1])
@@ -131,10 +131,10 @@ def test_identity_product_exact():
     g = synth.generator(41)
     A = synth.normal((M, K), g).cuda()
     eye = torch.eye(K, dtype=torch.bfloat16, device="cuda")
-    D = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
-    swg.gemm(0, 0, M, K, K, 1.0, A, K, eye, K, 0.0, D, K, swg.BF16)
+    D = Guarded(M, K, torch.bfloat16)
+    swg.gemm(0, 0, M, K, K, 1.0, A, K, eye, K, 0.0, D.view, D.ld, swg.BF16)
     torch.cuda.synchronize()
-    assert torch.equal(D, A)
+    assert torch.equal(D.cpu("A I"), A.cpu())
 
 
 def test_transpose_identity_gpu():
@@ -143,26 +143,26 @@ def test_transpose_identity_gpu():
     M, N, K = 256, 384, 512
     A, B, _ = synth.gemm_bf16(M, N, K, seed=43)
     Ad, Bd = A.cuda(), B.cuda()
-    D = torch.empty((M, N), dtype=torch.float32, device="cuda")
-    Dt = torch.empty((N, M), dtype=torch.float32, device="cuda")
-    swg.gemm(0, 0, M, N, K, 1.0, Ad, K, Bd, N, 0.0, D, N, swg.BF16_F32OUT)
-    swg.gemm(1, 1, N, M, K, 1.0, Bd, N, Ad, K, 0.0, Dt, M, swg.BF16_F32OUT)
+    D = Guarded(M, N, torch.float32)
+    Dt = Guarded(N, M, torch.float32)
+    swg.gemm(0, 0, M, N, K, 1.0, Ad, K, Bd, N, 0.0, D.view, D.ld, swg.BF16_F32OUT)
+    swg.gemm(1, 1, N, M, K, 1.0, Bd, N, Ad, K, 0.0, Dt.view, Dt.ld, swg.BF16_F32OUT)
     torch.cuda.synchronize()
     yhat = oracle.gemm(0, 0, M, N, K, 1.0, A, K, B, N, 0.0)
-    check_f32(to_f64(D), yhat, K, "D")
-    check_f32(to_f64(Dt).T, yhat, K, "D^T")
+    check_f32(to_f64(D.cpu("D")), yhat, K, "D")
+    check_f32(to_f64(Dt.cpu("D^T")).T, yhat, K, "D^T")
 
 
 def test_alpha_linearity_power_of_two_exact():
     M, N, K = 256, 256, 192
     A, B, _ = synth.gemm_bf16(M, N, K, seed=47)
     Ad, Bd = A.cuda(), B.cuda()
-    D1 = torch.empty((M, N), dtype=torch.float32, device="cuda")
-    D4 = torch.empty((M, N), dtype=torch.float32, device="cuda")
-    swg.gemm(0, 0, M, N, K, 1.0, Ad, K, Bd, N, 0.0, D1, N, swg.BF16_F32OUT)
-    swg.gemm(0, 0, M, N, K, 4.0, Ad, K, Bd, N, 0.0, D4, N, swg.BF16_F32OUT)
+    D1 = Guarded(M, N, torch.float32)
+    D4 = Guarded(M, N, torch.float32)
+    swg.gemm(0, 0, M, N, K, 1.0, Ad, K, Bd, N, 0.0, D1.view, D1.ld, swg.BF16_F32OUT)
+    swg.gemm(0, 0, M, N, K, 4.0, Ad, K, Bd, N, 0.0, D4.view, D4.ld, swg.BF16_F32OUT)
     torch.cuda.synchronize()
-    assert torch.equal(D4, 4.0 * D1)
+    assert torch.equal(D4.cpu("alpha 4"), 4.0 * D1.cpu("alpha 1"))
 
 
 def test_beta_one_accumulates_twice():
@@ -170,32 +170,35 @@ def test_beta_one_accumulates_twice():
     M, N, K = 128, 256, 128
     A, B, _ = synth.gemm_bf16(M, N, K, seed=53, dist="ints")
     Ad, Bd = A.cuda(), B.cuda()
-    C = torch.zeros((M, N), dtype=torch.float32, device="cuda")
-    swg.gemm(0, 0, M, N, K, 1.0, Ad, K, Bd, N, 1.0, C, N, swg.BF16_F32OUT)
-    swg.gemm(0, 0, M, N, K, 1.0, Ad, K, Bd, N, 1.0, C, N, swg.BF16_F32OUT)
+    C = Guarded(M, N, torch.float32, fill=0.0)
+    swg.gemm(0, 0, M, N, K, 1.0, Ad, K, Bd, N, 1.0, C.view, C.ld, swg.BF16_F32OUT)
+    swg.gemm(0, 0, M, N, K, 1.0, Ad, K, Bd, N, 1.0, C.view, C.ld, swg.BF16_F32OUT)
     torch.cuda.synchronize()
     AB = oracle.gemm(0, 0, M, N, K, 1.0, A, K, B, N, 0.0)
-    assert np.array_equal(to_f64(C), 2 * AB)   # small integers: exact
+    assert np.array_equal(to_f64(C.cpu("beta 1")), 2 * AB)   # small integers: exact
 
 
 @pytest.mark.parametrize("size", [4096, 8192])
 @pytest.mark.parametrize("tA", [0, 1])
 @pytest.mark.parametrize("tB", [0, 1])
 def test_square_bf16_sampled(size, tA, tB):
-    """The benchmark's square bf16 cases, alpha = 1, beta = 0: every output
-    finite, sampled rows (first, last, tile edges, random) equal to the
-    oracle within tolerance."""
+    """The benchmark's square bf16 cases, alpha = 1, beta = 0 (ldc = N, as
+    the benchmark calls it): every output finite, sampled rows (first, last,
+    the 128-row tile and 256-row pair-tile edges, the middle, random) equal
+    to the oracle within tolerance, guard rows above and below untouched."""
     M = N = K = size
     A, B, _ = synth.gemm_bf16(M, N, K, tA, tB, seed=1)
     Ad, Bd = A.cuda(), B.cuda()
-    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    swg.gemm(tA, tB, M, N, K, 1.0, Ad, A.shape[1], Bd, B.shape[1], 0.0, D, N, swg.BF16)
+    D = Guarded(M, N, torch.bfloat16, ld=N)
+    swg.gemm(tA, tB, M, N, K, 1.0, Ad, A.shape[1], Bd, B.shape[1], 0.0, D.view, N, swg.BF16)
     assert swg.get_device_error() == 0
-    assert bool(torch.isfinite(D).all())
+    out = D.cpu(f"{size}^3")
+    assert bool(torch.isfinite(out).all())
     rng = np.random.default_rng(size + tA * 2 + tB)
-    rows = sorted({0, 127, 128, M - 1, *rng.integers(0, M, 4).tolist()})
+    rows = sorted({0, 127, 128, 255, 256, M // 2, M - 257, M - 256, M - 1,
+                   *rng.integers(0, M, 4).tolist()})
     yhat = oracle.gemm(tA, tB, M, N, K, 1.0, A, A.shape[1], B, B.shape[1], 0.0, rows=rows)
-    check_half(to_f64(D)[rows], yhat, f"{size}^3 tA={tA} tB={tB}")
+    check_half(to_f64(out)[rows], yhat, f"{size}^3 tA={tA} tB={tB}")
 
 
 def test_default_stream_is_torch_current_stream():
@@ -228,9 +231,9 @@ def test_mn_major_3d_boxes_match_2d(monkeypatch, tA, tB, shape):
     out = []
     for flag in ("1", "0"):
         monkeypatch.setenv("SWG_MN_3D", flag)
-        D = C.clone()
-        swg.gemm(tA, tB, M, N, K, 1.0, A, A.shape[1], B, B.shape[1], 0.5, D, N, swg.BF16)
-        out.append(D.cpu())
+        D = Guarded(M, N, torch.bfloat16, init=C)
+        swg.gemm(tA, tB, M, N, K, 1.0, A, A.shape[1], B, B.shape[1], 0.5, D.view, D.ld, swg.BF16)
+        out.append(D.cpu(f"3-D boxes={flag}"))
     assert swg.get_device_error() == 0
     assert torch.equal(out[0], out[1])
     yhat = oracle.gemm(tA, tB, M, N, K, 1.0, A.cpu(), A.shape[1], B.cpu(), B.shape[1], 0.5,
@@ -246,11 +249,14 @@ def test_swiglu_3d_weight_boxes_match_2d(monkeypatch, M, K, N):
     out = []
     for flag in ("1", "0"):
         monkeypatch.setenv("SWG_MN_3D", flag)
-        Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-        swg.swiglu_mlp(Ad, Wf, Y, M, N, K)
-        out.append(Y.cpu())
+        Y = Guarded(M, N, torch.bfloat16, ld=N)
+        swg.swiglu_mlp(Ad, Wf, Y.view, M, N, K)
+        out.append(Y.cpu(f"swiglu 3-D boxes={flag}"))
     assert swg.get_device_error() == 0
     assert torch.equal(out[0], out[1])
+    rows = sorted({0, 127, 128, 255, 256, M - 1})
+    yhat = oracle.swiglu(A, W1, W2, M, N, K, rows=rows)
+    check_half(to_f64(out[0])[rows], yhat, f"swiglu 3-D boxes M={M}")
 
 
 @pytest.mark.parametrize("M", [16, 64])
@@ -266,9 +272,9 @@ def test_few_rows_3d_boxes_match_2d(monkeypatch, M, tA, tB):
     out = []
     for flag in ("1", "0"):
         monkeypatch.setenv("SWG_MN_3D", flag)
-        D = C.clone()
-        swg.gemm(tA, tB, M, N, K, 1.0, A, A.shape[1], B, B.shape[1], 1.0, D, N, swg.BF16)
-        out.append(D.cpu())
+        D = Guarded(M, N, torch.bfloat16, init=C)
+        swg.gemm(tA, tB, M, N, K, 1.0, A, A.shape[1], B, B.shape[1], 1.0, D.view, D.ld, swg.BF16)
+        out.append(D.cpu(f"few rows 3-D boxes={flag}"))
     assert swg.get_device_error() == 0
     assert torch.equal(out[0], out[1])
     yhat = oracle.gemm(tA, tB, M, N, K, 1.0, A.cpu(), A.shape[1], B.cpu(), B.shape[1], 1.0,
@@ -284,9 +290,9 @@ def test_swiglu_dual_3d_boxes_match_2d(monkeypatch, M):
     out = []
     for flag in ("1", "0"):
         monkeypatch.setenv("SWG_MN_3D", flag)
-        Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-        swg.swiglu_mlp_dual(Ad, W1d, W2d, Y, M, N, K)
-        out.append(Y.cpu())
+        Y = Guarded(M, N, torch.bfloat16, ld=N)
+        swg.swiglu_mlp_dual(Ad, W1d, W2d, Y.view, M, N, K)
+        out.append(Y.cpu(f"dual 3-D boxes={flag}"))
     assert swg.get_device_error() == 0
     assert torch.equal(out[0], out[1])
     yhat = oracle.swiglu(A, W1, W2, M, N, K)

@@ -15,7 +15,7 @@ import torch
 import oracle
 import swiglu_mlp_gb300 as swg
 import synth
-from helpers import check_f32, check_half, padded, round_up, to_f64
+from helpers import Guarded, check_f32, check_half, padded, round_up, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -29,13 +29,20 @@ def _operands(seed, tA, tB, M, N, K, dtype=torch.bfloat16, fill=9.0):
 
 
 def _run(tA, tB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtype, split_k=0):
-    Cd = C.cuda()
+    """C (M x ldc on the host) goes to the device inside guard bands: rows
+    above and below, and its columns past N.  Returns C with the first N
+    columns replaced by the result (after checking every guard) and the
+    number of kernel launches."""
+    N_out = min(N, C.shape[1])
+    Cg = Guarded(M, N_out, C.dtype, init=C[:, :N_out], ld=ldc)
     before = swg.launch_count()
-    swg.gemm_ex(tA, tB, M, N, K, alpha, A.cuda(), lda, B.cuda(), ldb, beta, Cd, ldc, dtype,
+    swg.gemm_ex(tA, tB, M, N, K, alpha, A.cuda(), lda, B.cuda(), ldb, beta, Cg.view, ldc, dtype,
                 split_k)
     launches = swg.launch_count() - before
     assert swg.get_device_error() == 0
-    return Cd.cpu(), launches
+    out = C.clone()
+    out[:, :N_out] = Cg.cpu(f"gemv {M}x{N}x{K}")
+    return out, launches
 
 
 @pytest.mark.parametrize("M", [1, 2, 3, 4])
@@ -119,9 +126,9 @@ def test_bitwise_deterministic():
     Ad, Bd = A.cuda(), B.cuda()
     outs = []
     for _ in range(3):
-        D = torch.empty((M, N), dtype=torch.float32, device="cuda")
-        swg.gemm(0, 1, M, N, K, 1.0, Ad, lda, Bd, ldb, 0.0, D, N, swg.BF16_F32OUT)
-        outs.append(D.cpu())
+        D = Guarded(M, N, torch.float32)
+        swg.gemm(0, 1, M, N, K, 1.0, Ad, lda, Bd, ldb, 0.0, D.view, D.ld, swg.BF16_F32OUT)
+        outs.append(D.cpu("repeat"))
     assert swg.get_device_error() == 0
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
 
@@ -272,13 +279,13 @@ def test_swiglu_decode_rows(M, K, N):
     W1 and W2, every output."""
     A, W1, W2 = synth.swiglu(M, K, N, seed=600 + M + K, w_std=0.02 if K >= 896 else 0.1)
     Wf = _swiglu_fused(W1, W2, K, N)
-    Y = torch.full((M, N), 9.0, dtype=torch.bfloat16, device="cuda")
+    Y = Guarded(M, N, torch.bfloat16, fill=9.0, ld=N)
     before = swg.launch_count()
-    swg.swiglu_mlp(A.cuda(), Wf.cuda(), Y, M, N, K)
+    swg.swiglu_mlp(A.cuda(), Wf.cuda(), Y.view, M, N, K)
     assert swg.launch_count() - before == 1
     assert swg.get_device_error() == 0
     yhat = oracle.swiglu(A, W1, W2, M, N, K)
-    check_half(to_f64(Y), yhat, f"swiglu decode M={M} K={K} N={N}")
+    check_half(to_f64(Y.cpu("swiglu decode")), yhat, f"swiglu decode M={M} K={K} N={N}")
 
 
 def test_swiglu_decode_agrees_with_tensor_path(monkeypatch):
@@ -286,15 +293,15 @@ def test_swiglu_decode_agrees_with_tensor_path(monkeypatch):
     A, W1, W2 = synth.swiglu(M, K, N, seed=610)
     Wf = _swiglu_fused(W1, W2, K, N).cuda()
     Ad = A.cuda()
-    Y1 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    Y2 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    swg.swiglu_mlp(Ad, Wf, Y1, M, N, K)
+    Y1 = Guarded(M, N, torch.bfloat16, ld=N)
+    Y2 = Guarded(M, N, torch.bfloat16, ld=N)
+    swg.swiglu_mlp(Ad, Wf, Y1.view, M, N, K)
     monkeypatch.setenv("SWG_GEMV", "0")
-    swg.swiglu_mlp(Ad, Wf, Y2, M, N, K)
+    swg.swiglu_mlp(Ad, Wf, Y2.view, M, N, K)
     assert swg.get_device_error() == 0
     yhat = oracle.swiglu(A, W1, W2, M, N, K)
-    check_half(to_f64(Y1), yhat, "swiglu decode, one-launch kernel")
-    check_half(to_f64(Y2), yhat, "swiglu decode, tensor-core path")
+    check_half(to_f64(Y1.cpu("one-launch")), yhat, "swiglu decode, one-launch kernel")
+    check_half(to_f64(Y2.cpu("tensor path")), yhat, "swiglu decode, tensor-core path")
 
 
 @pytest.mark.parametrize("M", [1, 2])
@@ -306,13 +313,13 @@ def test_fp8_swiglu_decode_rows(M, K, N):
     oracle on the same e4m3 values."""
     A, W1, W2, sw = synth.swiglu_e4m3(M, K, N, seed=620 + M + K, w_std=0.05)
     Wt = torch.from_numpy(oracle.interleave_t8(W1, W2, K, N)).view(torch.float8_e4m3fn)
-    Y = torch.full((M, N), 9.0, dtype=torch.bfloat16, device="cuda")
+    Y = Guarded(M, N, torch.bfloat16, fill=9.0, ld=N)
     before = swg.launch_count()
-    swg.swiglu_mlp_fp8(A.cuda(), Wt.cuda(), Y, M, N, K, sw)
+    swg.swiglu_mlp_fp8(A.cuda(), Wt.cuda(), Y.view, M, N, K, sw)
     assert swg.launch_count() - before == 1
     assert swg.get_device_error() == 0
     yhat = oracle.swiglu_typed(A, W1, W2, M, N, K, in_type="e4m3", scale=sw)
-    check_half(to_f64(Y), yhat, f"fp8 swiglu decode M={M} K={K} N={N}")
+    check_half(to_f64(Y.cpu("fp8 decode")), yhat, f"fp8 swiglu decode M={M} K={K} N={N}")
 
 
 @pytest.mark.parametrize("M", [1, 2])
@@ -323,10 +330,10 @@ def test_swiglu_dual_decode_rows(M, K, N):
     columns of W2, and column j pairs with column 64 + j in the final
     reduction.  Every output against the oracle."""
     A, W1, W2 = synth.swiglu(M, K, N, seed=630 + M + K, w_std=0.02 if K >= 896 else 0.1)
-    Y = torch.full((M, N), 9.0, dtype=torch.bfloat16, device="cuda")
+    Y = Guarded(M, N, torch.bfloat16, fill=9.0, ld=N)
     before = swg.launch_count()
-    swg.swiglu_mlp_dual(A.cuda(), W1.cuda(), W2.cuda(), Y, M, N, K)
+    swg.swiglu_mlp_dual(A.cuda(), W1.cuda(), W2.cuda(), Y.view, M, N, K)
     assert swg.launch_count() - before == 1
     assert swg.get_device_error() == 0
     yhat = oracle.swiglu(A, W1, W2, M, N, K)
-    check_half(to_f64(Y), yhat, f"swiglu dual decode M={M} K={K} N={N}")
+    check_half(to_f64(Y.cpu("dual decode")), yhat, f"swiglu dual decode M={M} K={K} N={N}")

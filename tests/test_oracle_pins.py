@@ -338,6 +338,73 @@ def test_mlp_down_projection_bruteforce():
 
 
 
+def test_round_bf16_matches_torch_on_binary32_values():
+    """round_bf16 against torch's binary32 -> bfloat16 conversion (round to
+    nearest, ties to even), on values exactly representable in binary32, so
+    that conversion rounds them once: random bit patterns over the whole range
+    (normal, subnormal, near overflow) and patterns whose dropped half is
+    exactly a tie or one unit either side of it."""
+    rng = np.random.default_rng(5)
+    hi = rng.integers(0, 2 ** 16, 20000, dtype=np.uint64)
+    lows = [rng.integers(0, 2 ** 16, 20000, dtype=np.uint64)] + [
+        np.full(20000, v, dtype=np.uint64) for v in (0x8000, 0x7FFF, 0x8001, 0x0000)]
+    for lo in lows:
+        f = ((hi << 16) | lo).astype(np.uint32).view(np.float32)
+        f = f[np.isfinite(f)]
+        ref = torch.from_numpy(f.copy()).to(torch.bfloat16).to(torch.float64).numpy()
+        got = np.array([oracle.round_bf16(float(x)) for x in f])
+        assert np.array_equal(got, ref)
+
+
+def test_round_bf16_hand_cases():
+    """Ties go to the even neighbour; the exact value is rounded once (a value
+    just above a tie goes up, where rounding through binary32 first would
+    land on the tie and go down); every bfloat16 value is unchanged; the
+    overflow and subnormal ends."""
+    assert oracle.round_bf16(1 + 2 ** -8) == 1.0
+    assert oracle.round_bf16(1 + 3 * 2 ** -8) == 1 + 2 ** -6
+    assert oracle.round_bf16(-(1 + 2 ** -8)) == -1.0
+    assert oracle.round_bf16(1 + 2 ** -8 + 2 ** -40) == 1 + 2 ** -7
+    big = (2 - 2 ** -7) * 2.0 ** 127                   # largest finite bfloat16
+    assert oracle.round_bf16(big) == big
+    assert oracle.round_bf16((2 - 2 ** -8 - 2 ** -30) * 2.0 ** 127) == big
+    assert oracle.round_bf16((2 - 2 ** -8) * 2.0 ** 127) == float("inf")   # tie: even is 2^128
+    assert oracle.round_bf16(-1e39) == float("-inf")
+    assert oracle.round_bf16(2.0 ** -134) == 0.0                          # tie with 0
+    assert oracle.round_bf16(3 * 2.0 ** -134) == 2.0 ** -132              # tie, even side
+    assert oracle.round_bf16(2.0 ** -133) == 2.0 ** -133
+    assert np.isnan(oracle.round_bf16(float("nan")))
+    for b in range(0, 1 << 16, 7):
+        v = oracle.bf16_to_f64(b)
+        if np.isfinite(v):
+            assert oracle.round_bf16(v) == v
+
+
+def test_mlp_with_bf16_activation():
+    """round_y: W_down = I returns the gated activation rounded to bfloat16
+    element by element, and the down projection of a general W_down is the
+    in-order sum over the rounded activation."""
+    M, K = 5, 16
+    A, W1, W2 = synth.swiglu(M, K, K, seed=35, w_std=0.2)
+    eye = torch.eye(K, dtype=torch.bfloat16)
+    Y = oracle.swiglu(A, W1, W2, M, K, K)
+    Yr = np.vectorize(oracle.round_bf16)(Y)
+    assert not np.array_equal(Yr, Y)
+    assert np.array_equal(oracle.mlp(A, W1, W2, eye, M, K, K, round_y=True), Yr)
+    N = 10
+    A, W1, W2 = synth.swiglu(M, K, N, seed=36, w_std=0.3)
+    Wd = synth.small_ints((N, K), synth.generator(37), -2, 2)
+    Yr = np.vectorize(oracle.round_bf16)(oracle.swiglu(A, W1, W2, M, N, K))
+    Wdf = Wd.to(torch.float64).tolist()
+    out = oracle.mlp(A, W1, W2, Wd, M, N, K, round_y=True)
+    for i in range(M):
+        for k in range(K):
+            s = 0.0
+            for n in range(N):
+                s += Yr[i, n] * Wdf[n][k]
+            assert out[i, k] == s
+
+
 def test_e4m3_decoder_all_patterns():
     bits = torch.arange(256, dtype=torch.int32).to(torch.uint8)
     ref = bits.view(torch.float8_e4m3fn).to(torch.float64).numpy()

@@ -12,7 +12,7 @@ import torch
 import oracle
 import swiglu_mlp_gb300 as swg
 import synth
-from helpers import check_half, padded, round_up, to_f64
+from helpers import Guarded, check_f32, check_half, padded, round_up, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -37,13 +37,12 @@ def test_gemm_tile_modes(tile_mode, tA, tB, shape):
     C = synth.normal((M, N), g)
     lda, ldb, ldc = round_up(A.shape[1], 8), round_up(B.shape[1], 8), round_up(N, 8)
     Ap, Bp, Cp = padded(A, lda, 2.0), padded(B, ldb, 2.0), padded(C, ldc, 4.0)
-    Cd = Cp.cuda()
-    swg.gemm(tA, tB, M, N, K, 0.5, Ap.cuda(), lda, Bp.cuda(), ldb, 1.0, Cd, ldc, swg.BF16)
+    Cg = Guarded(M, N, torch.bfloat16, init=C, ld=ldc)
+    swg.gemm(tA, tB, M, N, K, 0.5, Ap.cuda(), lda, Bp.cuda(), ldb, 1.0, Cg.view, ldc, swg.BF16)
     assert swg.get_device_error() == 0
-    out = Cd.cpu()
-    assert torch.equal(out[:, N:], Cp[:, N:])
+    out = Cg.cpu(f"{tile_mode} {shape}")
     yhat = oracle.gemm(tA, tB, M, N, K, 0.5, Ap, lda, Bp, ldb, 1.0, Cp, ldc)
-    check_half(to_f64(out[:, :N]), yhat, f"{tile_mode} {shape} tA={tA} tB={tB}")
+    check_half(to_f64(out), yhat, f"{tile_mode} {shape} tA={tA} tB={tB}")
 
 
 @pytest.mark.parametrize("tile_mode", MODES, indirect=True)
@@ -51,22 +50,23 @@ def test_gemm_tile_modes(tile_mode, tA, tB, shape):
 def test_swiglu_tile_modes(tile_mode, M, K, N):
     A, W1, W2 = synth.swiglu(M, K, N, seed=M + K, w_std=0.08)
     Wf = torch.from_numpy(oracle.interleave(W1, W2, K, N).view(np.int16)).view(torch.bfloat16)
-    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    swg.swiglu_mlp(A.cuda(), Wf.cuda(), Y, M, N, K)
+    Y = Guarded(M, N, torch.bfloat16, ld=N)
+    swg.swiglu_mlp(A.cuda(), Wf.cuda(), Y.view, M, N, K)
     assert swg.get_device_error() == 0
-    check_half(to_f64(Y), oracle.swiglu(A, W1, W2, M, N, K), f"{tile_mode} swiglu {M}x{K}x{N}")
+    check_half(to_f64(Y.cpu(f"{tile_mode} swiglu")), oracle.swiglu(A, W1, W2, M, N, K),
+               f"{tile_mode} swiglu {M}x{K}x{N}")
 
 
 @pytest.mark.parametrize("tile_mode", ["1cta", "2cta256"], indirect=True)
 def test_square_4096_tile_modes(tile_mode):
     M = N = K = 4096
     A, B, _ = synth.gemm_bf16(M, N, K, 0, 0, seed=1)
-    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    swg.gemm(0, 0, M, N, K, 1.0, A.cuda(), K, B.cuda(), N, 0.0, D, N, swg.BF16)
+    D = Guarded(M, N, torch.bfloat16, ld=N)
+    swg.gemm(0, 0, M, N, K, 1.0, A.cuda(), K, B.cuda(), N, 0.0, D.view, N, swg.BF16)
     assert swg.get_device_error() == 0
-    rows = [0, 255, 256, 2049, M - 1]
+    rows = [0, 127, 128, 255, 256, 2049, M - 257, M - 256, M - 1]
     yhat = oracle.gemm(0, 0, M, N, K, 1.0, A, K, B, N, 0.0, rows=rows)
-    check_half(to_f64(D)[rows], yhat, f"{tile_mode} 4096^3")
+    check_half(to_f64(D.cpu(f"{tile_mode} 4096^3"))[rows], yhat, f"{tile_mode} 4096^3")
 
 
 @pytest.mark.parametrize("tile_mode", ["1cta", "2cta128", "2cta256"], indirect=True)
@@ -82,12 +82,13 @@ def test_split_k_both_tile_shapes(tile_mode, split_k, tA, tB):
     C = synth.normal((M, N), g)
     lda, ldb = round_up(A.shape[1], 8), round_up(B.shape[1], 8)
     Ap, Bp = padded(A, lda, 2.0), padded(B, ldb, 2.0)
-    Cd = C.cuda()
-    swg.gemm_ex(tA, tB, M, N, K, 0.75, Ap.cuda(), lda, Bp.cuda(), ldb, 0.5, Cd, N, swg.BF16,
-                split_k)
+    Cg = Guarded(M, N, torch.bfloat16, init=C)
+    swg.gemm_ex(tA, tB, M, N, K, 0.75, Ap.cuda(), lda, Bp.cuda(), ldb, 0.5, Cg.view, Cg.ld,
+                swg.BF16, split_k)
     assert swg.get_device_error() == 0
     yhat = oracle.gemm(tA, tB, M, N, K, 0.75, Ap, lda, Bp, ldb, 0.5, C, N)
-    check_half(to_f64(Cd), yhat, f"{tile_mode} split={split_k} tA={tA} tB={tB}")
+    check_half(to_f64(Cg.cpu(f"{tile_mode} split")), yhat,
+               f"{tile_mode} split={split_k} tA={tA} tB={tB}")
 
 
 @pytest.mark.parametrize("tile_mode", MODES, indirect=True)
@@ -109,15 +110,12 @@ def test_beta_zero_edges_and_padding(tile_mode, code, shape):
     ldb = round_up(N, 8)
     Bp = padded(B, ldb, 3.0)
     ldc = round_up(N + 24, 8)
-    D0 = torch.full((M, ldc), 7.0, dtype=out_t)
-    Dd = D0.cuda()
-    swg.gemm(0, 0, M, N, K, 1.0, A.cuda(), K, Bp.cuda(), ldb, 0.0, Dd, ldc, dt)
+    Dg = Guarded(M, N, out_t, fill=7.0, ld=ldc)
+    swg.gemm(0, 0, M, N, K, 1.0, A.cuda(), K, Bp.cuda(), ldb, 0.0, Dg.view, ldc, dt)
     assert swg.get_device_error() == 0
-    out = Dd.cpu()
-    assert torch.equal(out[:, N:], D0[:, N:])
+    out = Dg.cpu(f"{tile_mode} {shape} staged stores")
     yhat = oracle.gemm(0, 0, M, N, K, 1.0, A, K, Bp, ldb, 0.0)
     if dt == swg.BF16_F32OUT:
-        from helpers import check_f32
-        check_f32(to_f64(out[:, :N]), yhat, K, f"{tile_mode} {shape} f32 out")
+        check_f32(to_f64(out), yhat, K, f"{tile_mode} {shape} f32 out")
     else:
-        check_half(to_f64(out[:, :N]), yhat, f"{tile_mode} {shape} bf16 out")
+        check_half(to_f64(out), yhat, f"{tile_mode} {shape} bf16 out")
