@@ -254,7 +254,7 @@ def test_swiglu_3d_weight_boxes_match_2d(monkeypatch, M, K, N):
         out.append(Y.cpu(f"swiglu 3-D boxes={flag}"))
     assert swg.get_device_error() == 0
     assert torch.equal(out[0], out[1])
-    rows = sorted({0, 127, 128, 255, 256, M - 1})
+    rows = sorted(r for r in {0, 127, 128, 255, 256, M - 1} if r < M)
     yhat = oracle.swiglu(A, W1, W2, M, N, K, rows=rows)
     check_half(to_f64(out[0])[rows], yhat, f"swiglu 3-D boxes M={M}")
 
