@@ -462,6 +462,14 @@ TileChoice choose_tiles(DeviceState *d, int kind, int64_t M, int64_t N, const in
     return c;
 }
 
+// SWG_CLUSTER_SPLITK=0 keeps automatic few-rows splits on the workspace path
+// (tests compare the two reductions).
+bool cluster_splitk_disabled()
+{
+    const char *v = std::getenv("SWG_CLUSTER_SPLITK");
+    return v && v[0] == '0';
+}
+
 // Split-K GEMM with swapped operands for M <= 64: the kernel computes
 // D^T = op(B)^T op(A)^T with op(B)^T (N x K) as its 128-row operand and
 // op(A)^T as its BN-column operand, writes transposed FP32 partials
@@ -510,12 +518,6 @@ int splitk_swapped(DeviceState *d, const TypeInfo &ti, int transA, int transB, i
     const bool b3 = !fp8 && bT_mn && make_tmap_mn3(&t3, A, ti.in_bf16, M, K, lda, bn / 64);
     if (b3) tb = t3;
 
-    const int64_t ld_ws = cdiv(N, 4) * 4;
-    float *ws = nullptr;
-    if (int rc = split_workspace(d, s, sizeof(float) * (size_t)splits * (size_t)M * (size_t)ld_ws,
-                                 fx, ws))
-        return rc;
-
     TileParams p{};           // in the kernel's (transposed) frame
     p.a_mn3 = a3;
     p.b_mn3 = b3;
@@ -527,16 +529,53 @@ int splitk_swapped(DeviceState *d, const TypeInfo &ti, int transA, int transB, i
     p.k_blocks = (int)kb;
     p.bk = bk;
     p.tiles = p.m_blocks * p.n_blocks;
-    p.splits = splits;
-    p.kb_per_split = kbps;
-    p.units = p.tiles * splits;
     p.group_m = 16;
     p.idesc = make_idesc(fp8 ? false : ti.in_bf16, aT_mn, bT_mn, swg::BM, bn);
     p.a_mn_major = aT_mn;
     p.b_mn_major = bT_mn;
+    p.err = d->err;
+
+    // Automatic split: the K ranges of a tile run as one thread-block cluster
+    // whose CTAs sum their partials over distributed shared memory -- one
+    // launch, no workspace.  Cluster size: the largest of 4, 2, 1 that keeps
+    // the grid within the SMs and every range at least 4 K blocks.  Used when
+    // it gives as many ranges as the workspace path would, or at least half
+    // the SMs; otherwise (small N) the workspace path splits K further.
+    int cl = 0;
+    if (split_k == 0 && !cluster_splitk_disabled()) {
+        int S = 1;
+        while (S < swg::MAX_CLUSTER_SPLITS && tiles * 2 * S <= d->sms && kb >= 8 * S) S *= 2;
+        if (S == splits || tiles * S * 2 >= d->sms) cl = S;
+    }
+    if (cl > 0) {
+        p.splits = cl;
+        p.kb_per_split = (int)cdiv(kb, cl);
+        p.units = p.tiles * cl;
+        // every rank has at least one K block (S <= kb / 4 guarantees it)
+        if ((int64_t)(cl - 1) * p.kb_per_split >= kb) return SWG_ERR_UNSUPPORTED;
+        p.alpha = alpha;
+        p.beta = beta;
+        p.D = C;
+        p.ldd = ldc;
+        p.out_kind = ti.out_kind;
+        if ((fp8 ? swg::launch_tc_splitk_cl_fp8(bn, ta, tb, p, p.units, s)
+                 : swg::launch_tc_splitk_cl(bn, ta, tb, p, p.units, s)) != cudaSuccess)
+            return cuda_fail();
+        g_launches++;
+        return SWG_OK;
+    }
+
+    const int64_t ld_ws = cdiv(N, 4) * 4;
+    float *ws = nullptr;
+    if (int rc = split_workspace(d, s, sizeof(float) * (size_t)splits * (size_t)M * (size_t)ld_ws,
+                                 fx, ws))
+        return rc;
+
+    p.splits = splits;
+    p.kb_per_split = kbps;
+    p.units = p.tiles * splits;
     p.ws = ws;
     p.ld_ws = ld_ws;
-    p.err = d->err;
     const int grid = (int)std::min<int64_t>(p.units, d->sms);
     if ((fp8 ? swg::launch_tc_splitk_t_fp8(bn, ta, tb, p, grid, s)
              : swg::launch_tc_splitk_t(bn, ta, tb, p, grid, s)) != cudaSuccess)
@@ -1097,6 +1136,51 @@ int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M, int64_t N
         const int rc = gemv_path(d, 1, swg::OUT_BF16, SWG_OP_N, SWG_OP_N, M, N2, K, 1.0f, A, K,
                                  W_fused, N2, 0.0f, Y, N, s, true);
         if (rc != SWG_ERR_UNSUPPORTED) return rc;
+    }
+    // At most 128 rows: one 128 x 256 tile per 256 columns of the 2N-space,
+    // with its K range cut into S pieces that run as one thread-block cluster
+    // and are summed over distributed shared memory before the pair-multiply
+    // (one launch, no workspace).  S is the largest of 4, 2 that keeps the
+    // grid within the SMs and every piece non-empty; otherwise (S = 1, many
+    // tiles) the persistent kernel below.
+    if (M <= swg::BM && !cluster_splitk_disabled()) {
+        const int64_t kb = cdiv(K, swg::BK);
+        const int64_t tiles = cdiv(N2, 256);
+        int S = 1;
+        while (S < swg::MAX_CLUSTER_SPLITS && tiles * 2 * S <= d->sms &&
+               (2 * S - 1) * cdiv(kb, 2 * S) < kb)
+            S *= 2;
+        if (S > 1) {
+            CUtensorMap ta, tb, t3;
+            if (!make_tmap(&ta, A, true, K, M, K, swg::BM) ||
+                !make_tmap(&tb, W_fused, true, N2, K, N2, 64))
+                return cuda_fail();
+            TileParams p{};
+            p.b_mn3 = make_tmap_mn3(&t3, W_fused, true, N2, K, N2, 256 / 64);
+            if (p.b_mn3) tb = t3;
+            p.M = (int)M;
+            p.N = (int)N2;
+            p.K = (int)K;
+            p.m_blocks = 1;
+            p.n_blocks = (int)tiles;
+            p.k_blocks = (int)kb;
+            p.bk = swg::BK;
+            p.tiles = (int)tiles;
+            p.splits = S;
+            p.kb_per_split = (int)cdiv(kb, S);
+            p.units = p.tiles * S;
+            p.group_m = 16;
+            p.idesc = make_idesc(true, false, true, swg::BM, 256);
+            p.b_mn_major = 1;
+            p.alpha = 1.0f;
+            p.D = Y;
+            p.ldd = N;
+            p.out_kind = swg::OUT_BF16;
+            p.err = d->err;
+            if (swg::launch_tc_swiglu_cl(ta, tb, p, p.units, s) != cudaSuccess) return cuda_fail();
+            g_launches++;
+            return SWG_OK;
+        }
     }
     static const int cands[] = {256, 128, 64};
     const TileChoice tc = choose_tiles(d, 1, M, N2, cands, 3);

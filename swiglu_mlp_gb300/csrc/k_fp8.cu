@@ -56,6 +56,17 @@ cudaError_t launch_tc_splitk_t_fp8(int bn, const CUtensorMap &ta, const CUtensor
     }
 }
 
+cudaError_t launch_tc_splitk_cl_fp8(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
+                                    const TileParams &p, int ctas, cudaStream_t s)
+{
+    switch (bn) {
+    case 16: return launch_tc_impl<16, EPI_SPLITK_CL, false, true>(ta, tb, p, ctas, s);
+    case 32: return launch_tc_impl<32, EPI_SPLITK_CL, false, true>(ta, tb, p, ctas, s);
+    case 64: return launch_tc_impl<64, EPI_SPLITK_CL, false, true>(ta, tb, p, ctas, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
 int max_active_pairs_fp8(int kind, int bn, int sms)
 {
     if (bn != 256) return 0;

@@ -143,6 +143,17 @@ cudaError_t launch_tc_splitk_t(int bn, const CUtensorMap &ta, const CUtensorMap 
     }
 }
 
+cudaError_t launch_tc_splitk_cl(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
+                                const TileParams &p, int ctas, cudaStream_t s)
+{
+    switch (bn) {
+    case 16: return launch_tc_impl<16, EPI_SPLITK_CL, false>(ta, tb, p, ctas, s);
+    case 32: return launch_tc_impl<32, EPI_SPLITK_CL, false>(ta, tb, p, ctas, s);
+    case 64: return launch_tc_impl<64, EPI_SPLITK_CL, false>(ta, tb, p, ctas, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
 cudaError_t launch_splitk_reduce(const TileParams &p, int sms, cudaStream_t s)
 {
     const long long items = (long long)p.M * ((p.N + 3) / 4);

@@ -42,6 +42,12 @@ cudaError_t launch_tc_swiglu_dual(int bn, bool pair, const CUtensorMap &ta, cons
     }
 }
 
+cudaError_t launch_tc_swiglu_cl(const CUtensorMap &ta, const CUtensorMap &tb, const TileParams &p,
+                                int ctas, cudaStream_t s)
+{
+    return launch_tc_impl<256, EPI_SWIGLU_CL, false>(ta, tb, p, ctas, s);
+}
+
 int max_active_pairs_dual(int bn, int sms)
 {
     return bn == 256 ? max_active_pairs_impl<256, EPI_SWIGLU_DUAL>(sms) : 0;

@@ -50,6 +50,20 @@ cudaError_t launch_tc_splitk(int bn, bool pair, const CUtensorMap &ta, const CUt
 cudaError_t launch_tc_splitk_t(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
                                const TileParams &p, int units, cudaStream_t s);
 
+// The same product with the K ranges of a tile reduced inside a cluster of
+// p.splits CTAs (1, 2 or 4; EPI_SPLITK_CL): one launch of `ctas` = tiles x
+// splits CTAs, no workspace.  16-bit operands, and e4m3 (both K-major).
+cudaError_t launch_tc_splitk_cl(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
+                                const TileParams &p, int ctas, cudaStream_t s);
+cudaError_t launch_tc_splitk_cl_fp8(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
+                                    const TileParams &p, int ctas, cudaStream_t s);
+
+// Fused SwiGLU over W_fused for at most 128 rows with the K ranges of each
+// 128 x 256 tile reduced inside a cluster of p.splits CTAs (EPI_SWIGLU_CL);
+// `ctas` = tiles x splits.
+cudaError_t launch_tc_swiglu_cl(const CUtensorMap &ta, const CUtensorMap &tb, const TileParams &p,
+                                int ctas, cudaStream_t s);
+
 // SwiGLU from separate W1 (tw1) and W2 (tw2), each K x N; BN = 128 or 256
 // (single CTA) or 256 (pair).
 cudaError_t launch_tc_swiglu_dual(int bn, bool pair, const CUtensorMap &ta, const CUtensorMap &tw1,

@@ -45,6 +45,14 @@ cudaError_t launch_tc_impl(const CUtensorMap &ta, const CUtensorMap &tb, const C
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
         cfg.gridDim = dim3(2 * units);
+    } else if (ClusterK<EPI>::value && p.splits > 1) {
+        // one cluster of p.splits CTAs per tile; `units` = tiles x splits CTAs
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = p.splits;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+        cfg.gridDim = dim3(units);
     } else {
         cfg.gridDim = dim3(units);
     }

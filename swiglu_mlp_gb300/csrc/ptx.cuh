@@ -383,6 +383,18 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
                  : "memory");
 }
 
+// 16-byte load from the shared memory of a CTA of this cluster
+// (cluster_addr from mapa_shared).
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t cluster_addr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
+
 // Every thread of every CTA in the cluster arrives, then waits for all.
 __device__ __forceinline__ void cluster_sync_all()
 {

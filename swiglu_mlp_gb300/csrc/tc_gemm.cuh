@@ -69,12 +69,31 @@ namespace swg {
 // columns come from W1 (Gate) and the last BN/2 from W2 (Up) -- in a CTA pair
 // the even CTA loads its half of B from W1 and the odd CTA from W2 -- so the
 // accumulator row holds Gate in columns [0, BN/2) and Up in [BN/2, BN).
+// EPI_SPLITK_CL: swapped-operand split-K reduced inside a thread-block
+// cluster.  The p.splits CTAs of a cluster (at most 8) compute the K ranges of
+// one tile, one range per rank; each parks its FP32 partial in its own shared
+// memory, and after a cluster barrier rank r reads its share of the tile's
+// output rows from every rank's shared memory in rank order 0, 1, .., S-1,
+// applies alpha and beta * C and stores D.  One launch, no workspace.  Each
+// CTA runs exactly one unit, so the grid is tiles x S CTAs.
+// EPI_SWIGLU_CL: the same cluster reduction for the fused SwiGLU in the
+// output's own frame (rows = rows of A, columns = the 2N-space of W_fused):
+// rank r sums its share of the tile's column pairs over the S ranks and
+// stores SiLU(alpha * gate) * (alpha * up).
 enum EpiKind {
     EPI_STORE = 0,
     EPI_SWIGLU = 1,
     EPI_SPLITK = 2,
     EPI_SPLITK_T = 3,
-    EPI_SWIGLU_DUAL = 4
+    EPI_SWIGLU_DUAL = 4,
+    EPI_SPLITK_CL = 5,
+    EPI_SWIGLU_CL = 6
+};
+
+// The epilogues whose K ranges are reduced inside a cluster (one unit per CTA).
+template <int EPI>
+struct ClusterK {
+    static constexpr bool value = EPI == EPI_SPLITK_CL || EPI == EPI_SWIGLU_CL;
 };
 enum OutKind { OUT_BF16 = 0, OUT_F16 = 1, OUT_F32 = 2 };
 
@@ -87,6 +106,7 @@ constexpr int NUM_THREADS = 64 + NUM_EPI_THREADS;
 constexpr int EPI_WARP0 = 2;
 constexpr int ERR_TIMEOUT = 6;       // == SWG_ERR_DEVICE_TIMEOUT
 constexpr int MAX_SPLITS = 16;       // split-K ranges per tile (host enforces)
+constexpr int MAX_CLUSTER_SPLITS = 4; // K ranges of one tile reduced in a cluster
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // pipeline waits
 constexpr uint64_t DRAIN_LIMIT_NS = 1000000ull;      // teardown drains
 
@@ -447,6 +467,251 @@ __device__ __forceinline__ void store_staged(const TileParams &p, const CUtensor
     bulk_wait_all();
 }
 
+// ------------------------------------------------ cluster split-K epilogue
+// EPI_SPLITK_CL, run by the eight epilogue warps of each CTA of a cluster of
+// S = p.splits CTAs (kernel frame: TMEM lane = output column n of the tile,
+// TMEM column j = output row m).
+//   1. Before the accumulator is ready, each thread loads the C values of the
+//      outputs it will produce (beta != 0), so that DRAM read overlaps the
+//      main loop.
+//   2. The accumulator (128 lanes x BN columns, FP32) goes to this CTA's own
+//      shared memory as part[j][lane] (the consumed pipeline stages).
+//   3. Cluster barrier (every thread of every CTA arrives; release/acquire at
+//      cluster scope orders the parked partials before the remote reads).
+//   4. This rank owns output rows [r * BN / S, (r + 1) * BN / S) of the tile:
+//      for each group of four columns it reads the partials of ranks
+//      0, 1, .., S-1 over distributed shared memory, sums them in that
+//      order starting from 0, and stores alpha * sum + beta * C.
+// The teardown's cluster barrier keeps every CTA's shared memory alive until
+// all ranks have read it.
+template <int BN>
+__device__ __forceinline__ void splitk_cluster_epilogue(const TileParams &p, uint32_t tmem_base,
+                                                        uint8_t *smem, uint64_t *acc_full,
+                                                        volatile int *abort_flag, int unit,
+                                                        int krank)
+{
+    constexpr int ITEMS = BN / 8;              // float4 items per thread when S = 1
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int et = threadIdx.x - EPI_WARP0 * 32;     // 0 .. 255
+    const int S = p.splits;
+    int mb, nb, split, tile;
+    unit_coords(p, unit, mb, nb, split, tile);
+    const int rows = BN / S;                   // output rows this rank reduces
+    const int n_items = rows * (BM / 4);
+    const int Mo = p.N, No = p.M;              // output rows / columns
+    float c[ITEMS][4];
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        c[it][0] = c[it][1] = c[it][2] = c[it][3] = 0.0f;
+        const int idx = et + it * NUM_EPI_THREADS;
+        if (p.beta == 0.0f || idx >= n_items) continue;
+        const int m = nb * BN + krank * rows + idx / (BM / 4);
+        const int n = mb * BM + (idx % (BM / 4)) * 4;
+        if (m >= Mo || n >= No) continue;
+        const long long off = (long long)m * p.ldd + n;
+        if (No - n >= 4) {
+            if (p.out_kind == OUT_F32) {
+                const float4 v = *reinterpret_cast<const float4 *>(
+                    reinterpret_cast<const float *>(p.D) + off);
+                c[it][0] = v.x;
+                c[it][1] = v.y;
+                c[it][2] = v.z;
+                c[it][3] = v.w;
+            } else {
+                const uint2 w = *reinterpret_cast<const uint2 *>(
+                    reinterpret_cast<const uint16_t *>(p.D) + off);
+                const uint32_t ww[2] = {w.x, w.y};
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (p.out_kind == OUT_F16) {
+                        const __half2 c2 = *reinterpret_cast<const __half2 *>(&ww[h]);
+                        c[it][2 * h] = __low2float(c2);
+                        c[it][2 * h + 1] = __high2float(c2);
+                    } else {
+                        const __nv_bfloat162 c2 = *reinterpret_cast<const __nv_bfloat162 *>(&ww[h]);
+                        c[it][2 * h] = __low2float(c2);
+                        c[it][2 * h + 1] = __high2float(c2);
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (j < No - n) c[it][j] = load_out(p.D, off + j, p.out_kind);
+        }
+    }
+
+    // 2. park the partial: part[j][lane], j < BN, lane < 128
+    float *part = reinterpret_cast<float *>(smem);
+    constexpr int W = BN >= 32 ? 32 : 16;
+    const int q = warp & 3;
+    const int h = (warp - EPI_WARP0) / 4;
+    const bool active = (BN == 64) || h == 0;
+    const int j0 = BN == 64 ? h * 32 : 0;
+    bool ok = wait_bounded(smem_u32(&acc_full[0]), 0, abort_flag, p.err);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+        tc_fence_after();
+        if (active) {
+            uint32_t r[W];
+            tmem_ld_cols(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + j0, r);
+            tmem_ld_wait(r);
+#pragma unroll
+            for (int j = 0; j < W; ++j) part[(j0 + j) * BM + q * 32 + lane] = __uint_as_float(r[j]);
+        }
+    }
+    tc_fence_before();
+    // 3. every rank's partial is parked
+    cluster_sync_all();
+    // 4. reduce this rank's rows in rank order and store D
+    const uint32_t part_addr = smem_u32(part);
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const int idx = et + it * NUM_EPI_THREADS;
+        if (idx >= n_items) continue;
+        const int ml = krank * rows + idx / (BM / 4);
+        const int nl = (idx % (BM / 4)) * 4;
+        const int m = nb * BN + ml;
+        const int n = mb * BM + nl;
+        if (m >= Mo || n >= No) continue;
+        const uint32_t a = part_addr + (uint32_t)((ml * BM + nl) * 4);
+        float4 v[MAX_CLUSTER_SPLITS];
+#pragma unroll
+        for (int r = 0; r < MAX_CLUSTER_SPLITS; ++r)
+            if (r < S) v[r] = ld_dsmem_f4(mapa_shared(a, (uint32_t)r));
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int r = 0; r < MAX_CLUSTER_SPLITS; ++r) {
+            if (r < S) {
+                acc[0] += v[r].x;
+                acc[1] += v[r].y;
+                acc[2] += v[r].z;
+                acc[3] += v[r].w;
+            }
+        }
+        float out[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            out[j] = p.beta != 0.0f ? __fmaf_rn(p.beta, c[it][j], p.alpha * acc[j])
+                                    : p.alpha * acc[j];
+        const long long off = (long long)m * p.ldd + n;
+        if (No - n >= 4) {
+            if (p.out_kind == OUT_F32)
+                *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.D) + off) =
+                    make_float4(out[0], out[1], out[2], out[3]);
+            else
+                *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(p.D) + off) =
+                    make_uint2(pack2(out[0], out[1], p.out_kind), pack2(out[2], out[3], p.out_kind));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (j < No - n) store_out(p.D, off + j, out[j], p.out_kind);
+        }
+    }
+}
+
+// EPI_SWIGLU_CL, run by the eight epilogue warps of each CTA of a cluster of
+// S = p.splits CTAs, one K range each (output frame: TMEM lane = row of the
+// tile, TMEM column = 2N-space column, Gate at even and Up at odd columns).
+//   1. The accumulator goes to this CTA's own shared memory, row-major with
+//      a row stride of BN + 4 floats (16-byte stores without bank conflicts).
+//   2. Cluster barrier, as in splitk_cluster_epilogue.
+//   3. Rank r owns the tile's 2N-space columns [r * BN / S, (r + 1) * BN / S):
+//      for each row and group of 16 columns (8 outputs) it reads ranks
+//      0, 1, .., S-1 over distributed shared memory, sums in that order from
+//      0, forms y = SiLU(alpha * gate) * (alpha * up) per pair, rounds once to
+//      bf16 and stores 16 bytes of Y.
+template <int BN>
+__device__ __forceinline__ void swiglu_cluster_epilogue(const TileParams &p, uint32_t tmem_base,
+                                                        uint8_t *smem, uint64_t *acc_full,
+                                                        volatile int *abort_flag, int unit,
+                                                        int krank)
+{
+    constexpr int LD = BN + 4;
+    constexpr int NC = BN / 32;                // 32-column chunks per tile row
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int et = threadIdx.x - EPI_WARP0 * 32;
+    const int S = p.splits;
+    int mb, nb, split, tile;
+    unit_coords(p, unit, mb, nb, split, tile);
+    float *part = reinterpret_cast<float *>(smem);
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int c_begin = ((warp - EPI_WARP0) / 4) * (NC / 2);
+    bool ok = wait_bounded(smem_u32(&acc_full[0]), 0, abort_flag, p.err);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+        tc_fence_after();
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+        for (int c = c_begin; c < c_begin + NC / 2; ++c) {
+            uint32_t r[32];
+            tmem_ld_32cols(t_row + c * 32, r);
+            tmem_ld_wait(r);
+            float4 *dst = reinterpret_cast<float4 *>(part + row * LD + c * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                     __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+    }
+    tc_fence_before();
+    cluster_sync_all();
+    const uint32_t part_addr = smem_u32(part);
+    const int cols = BN / S;                   // this rank's 2N-space columns
+    const int n_items = BM * (cols / 16);
+    const int n_out = p.N / 2;                 // output columns (p.N is the 2N-space width)
+#pragma unroll 1
+    for (int idx = et; idx < n_items; idx += NUM_EPI_THREADS) {
+        const int rr = idx % BM;
+        const int c0 = krank * cols + (idx / BM) * 16;
+        const int m = mb * BM + rr;
+        const int n = (nb * BN + c0) / 2;      // first output column of the item
+        if (m >= p.M || n >= n_out) continue;
+        const uint32_t a = part_addr + (uint32_t)((rr * LD + c0) * 4);
+        float4 v[MAX_CLUSTER_SPLITS][4];
+#pragma unroll
+        for (int r = 0; r < MAX_CLUSTER_SPLITS; ++r) {
+            if (r < S) {
+                const uint32_t ra = mapa_shared(a, (uint32_t)r);
+#pragma unroll
+                for (int w = 0; w < 4; ++w) v[r][w] = ld_dsmem_f4(ra + 16 * w);
+            }
+        }
+        float acc[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+#pragma unroll
+        for (int r = 0; r < MAX_CLUSTER_SPLITS; ++r) {
+            if (r < S) {
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    acc[4 * w] += v[r][w].x;
+                    acc[4 * w + 1] += v[r][w].y;
+                    acc[4 * w + 2] += v[r][w].z;
+                    acc[4 * w + 3] += v[r][w].w;
+                }
+            }
+        }
+        float y[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            y[j] = silu_f32(p.alpha * acc[2 * j]) * (p.alpha * acc[2 * j + 1]);
+        __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.D) + (long long)m * p.ldd + n;
+        if (n_out - n >= 8) {
+            *reinterpret_cast<uint4 *>(dst) =
+                make_uint4(pack2(y[0], y[1], OUT_BF16), pack2(y[2], y[3], OUT_BF16),
+                           pack2(y[4], y[5], OUT_BF16), pack2(y[6], y[7], OUT_BF16));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (j < n_out - n) dst[j] = __float2bfloat16_rn(y[j]);
+        }
+    }
+}
+
 // FP8: operands are 8-bit (e4m3/e5m2) and the MMA is kind::f8f6f4.  In bytes
 // nothing else changes: a 128-byte swizzled stage row holds 128 elements and
 // each MMA (K = 32) consumes 32 bytes of it, as a kind::f16 MMA (K = 16) does.
@@ -479,8 +744,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // cluster, and this CTA owns rows [128*rank, 128*rank + 128) of the tile.
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
     const bool leader = rank == 0;
-    const int first_unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-    const int unit_step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    // Cluster-reduced K: cluster c is tile c, rank r its K range r (unit r * tiles + c).
+    constexpr bool CLK = ClusterK<EPI>::value;
+    const int krank = CLK ? (int)cluster_ctarank() : 0;
+    const int first_unit = PAIR  ? (int)(blockIdx.x >> 1)
+                           : CLK ? krank * p.tiles + (int)blockIdx.x / p.splits
+                                 : (int)blockIdx.x;
+    const int unit_step = PAIR ? (int)(gridDim.x >> 1) : CLK ? p.units : (int)gridDim.x;
 
     // Programmatic dependent launch: the kernel queued behind this one on the
     // stream (the split-K reduction, or the next GEMM of a chain) may be
@@ -490,6 +760,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (threadIdx.x == 0) {
+        // Tensor maps are fetched from memory on first use: start that now.
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
@@ -503,8 +776,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_init(smem_u32(staged), NUM_EPI_WARPS);
         *abort_flag = 0;
         fence_barrier_init();
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
         if (EPI == EPI_SWIGLU_DUAL || p.tma_store) tma_prefetch_desc(&tmX);
     }
     if (warp == 1) {
@@ -641,6 +912,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
         __syncwarp();
+        if (CLK) cluster_sync_all();   // partials parked (see the epilogue)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && leader) {
@@ -713,6 +985,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             wait_bounded(smem_u32(mma_done), 0, abort_flag, p.err, false, DRAIN_LIMIT_NS);
         }
         __syncwarp();
+        if (CLK) cluster_sync_all();   // partials parked (see the epilogue)
+    } else if (EPI == EPI_SPLITK_CL) {
+        splitk_cluster_epilogue<BN>(p, tmem_base, smem, acc_full, abort_flag, first_unit, krank);
+    } else if (EPI == EPI_SWIGLU_CL) {
+        swiglu_cluster_epilogue<BN>(p, tmem_base, smem, acc_full, abort_flag, first_unit, krank);
     } else if (EPI == EPI_SWIGLU_DUAL) {
         // ------------------------------------------ epilogue (separate W1, W2)
         // Output column j of the tile = SiLU(acc[j]) * acc[BN/2 + j]; warps
@@ -892,8 +1169,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
     // Pair mode: neither CTA may free its tensor memory or exit while the
-    // leader's MMAs or the peer's arrivals can still reach it.
-    if (PAIR)
+    // leader's MMAs or the peer's arrivals can still reach it.  Cluster
+    // split-K: nor while another rank still reads its parked partial.
+    if (PAIR || CLK)
         cluster_sync_all();
     else
         __syncthreads();

@@ -108,8 +108,8 @@ def test_capture_and_replay_bitwise():
 
 @pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")
 def test_allocation_while_capturing_is_refused():
-    """A split-K call on a stream that has no workspace yet would have to
-    allocate one: while that stream is capturing, the call returns
+    """A split-K call with nine explicit K ranges (the workspace path) on a
+    stream that has no workspace yet would have to allocate one: while that stream is capturing, the call returns
     SWG_ERR_UNSUPPORTED and launches nothing."""
     s = torch.cuda.Stream()
     P, O = _problem(702), _outputs()
@@ -118,14 +118,15 @@ def test_allocation_while_capturing_is_refused():
     before = swg.launch_count()
     rc = None
     with torch.cuda.graph(g, stream=s):
-        rc = swg.load().gemm(0, 0, 32, 2048, 8192, ctypes.c_float(1.0), P["As"].data_ptr(), 8192,
-                             P["Bs"].data_ptr(), 2048, ctypes.c_float(0.0), O["Ds"].data_ptr(),
-                             2048, swg.BF16, ctypes.c_void_p(s.cuda_stream))
+        rc = swg.load().gemm_ex(0, 0, 32, 2048, 8192, ctypes.c_float(1.0), P["As"].data_ptr(),
+                                8192, P["Bs"].data_ptr(), 2048, ctypes.c_float(0.0),
+                                O["Ds"].data_ptr(), 2048, swg.BF16, 9,
+                                ctypes.c_void_p(s.cuda_stream))
     assert rc == 3                                # SWG_ERR_UNSUPPORTED
     assert swg.launch_count() == before
     # Outside the capture the same call allocates and runs.
     with torch.cuda.stream(s):
-        swg.gemm(0, 0, 32, 2048, 8192, 1.0, P["As"], 8192, P["Bs"], 2048, 0.0, O["Ds"], 2048,
-                 swg.BF16)
+        swg.gemm_ex(0, 0, 32, 2048, 8192, 1.0, P["As"], 8192, P["Bs"], 2048, 0.0, O["Ds"], 2048,
+                    swg.BF16, 9)
     torch.cuda.synchronize()
     assert swg.get_device_error() == 0

@@ -1,0 +1,70 @@
+"""Fused SwiGLU for at most 128 rows with the K range of each 128 x 256 tile
+split over a thread-block cluster: the CTAs sum Gate and Up partials over
+distributed shared memory, in rank order, before the pair-multiply
+("Sobreposição de Ativação em Nível de Tile para Inferência Eficiente de LLM",
+Metodologia, Kernel-2's pair-multiply; "为什么 GEMM 是 CUDA 的必修课", 关键技术
+item 5 for the split).  Checked against the oracle from separate W1 and W2,
+every output, on ragged shapes and on the small-model shape; against the
+persistent kernel (SWG_CLUSTER_SPLITK=0) within the same tolerance; repeated
+calls bit-identical.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import swiglu_mlp_gb300 as swg
+import synth
+from helpers import Guarded, check_half, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(M, K, N, seed, w_std=0.02, A=None):
+    A_, W1, W2 = synth.swiglu(M, K, N, seed=seed, w_std=w_std)
+    A = A_ if A is None else A
+    Wf = torch.from_numpy(oracle.interleave(W1, W2, K, N).view(np.int16)).view(torch.bfloat16)
+    Y = Guarded(M, N, torch.bfloat16, fill=9.0, ld=N)
+    swg.swiglu_mlp(A.cuda(), Wf.cuda(), Y.view, M, N, K)
+    assert swg.get_device_error() == 0
+    return to_f64(Y.cpu(f"swiglu cluster {M}x{K}x{N}")), A, W1, W2
+
+
+@pytest.mark.parametrize("M,K,N", [(3, 904, 1000),      # ragged 2N tile and K, 4 ranges
+                                   (64, 896, 4864),     # small model, 38 tiles x 4
+                                   (128, 4096, 1024),   # 8 tiles x 4, long K
+                                   (33, 1024, 8),       # one partial tile
+                                   (128, 136, 520)])    # 3 K blocks: 2 ranges
+def test_every_output(M, K, N):
+    y, A, W1, W2 = _run(M, K, N, seed=M + K + N, w_std=0.05)
+    check_half(y, oracle.swiglu(A, W1, W2, M, N, K), f"swiglu cluster {M}x{K}x{N}")
+
+
+def test_tails_keep_relative_accuracy():
+    """Gates of standard deviation 8 (K = 256 in four single-block ranges):
+    SiLU's negative tail keeps its relative accuracy through the cluster
+    reduction -- no output differs from the oracle by more than 1%
+    relative."""
+    M, K, N = 128, 256, 256
+    y, A, W1, W2 = _run(M, K, N, seed=91, w_std=0.5)
+    stats = check_half(y, oracle.swiglu(A, W1, W2, M, N, K), "swiglu cluster tails")
+    assert stats["frac_rel_gt_1pct"] == 0.0, stats
+    assert stats["max_rel"] < 1e-2, stats
+
+
+def test_matches_persistent_kernel_and_repeats(monkeypatch):
+    M, K, N = 128, 896, 4864
+    A, W1, W2 = synth.swiglu(M, K, N, seed=8)
+    Ad = A.cuda()
+    Wf = swg.interleave_weights(W1.cuda(), W2.cuda())
+    outs = []
+    for flag in ("1", "1", "0"):
+        monkeypatch.setenv("SWG_CLUSTER_SPLITK", flag)
+        Y = Guarded(M, N, torch.bfloat16, ld=N)
+        swg.swiglu_mlp(Ad, Wf, Y.view, M, N, K)
+        outs.append(Y.cpu(f"cluster={flag}"))
+    assert swg.get_device_error() == 0
+    assert torch.equal(outs[0], outs[1])
+    yhat = oracle.swiglu(A, W1, W2, M, N, K)
+    check_half(to_f64(outs[0]), yhat, "cluster")
+    check_half(to_f64(outs[2]), yhat, "persistent")

@@ -85,15 +85,15 @@ def _both(tA, tB, M, N, K, alpha, beta, code, split_k, seed):
 
 
 def test_two_calls_match_existing_entry_point():
-    # call 1: the skinny split-K shape, automatic split (few rows: the
-    # transposed product), beta = 1, bf16 out
-    ref, new, yhat = _both(0, 0, 64, 4096, 16384, 1.0, 1.0, swg.BF16, 0, seed=101)
+    # call 1: the skinny split-K shape with four K ranges (few rows: the
+    # transposed product, partials in the fixed array), beta = 1, bf16 out
+    ref, new, yhat = _both(0, 0, 64, 4096, 16384, 1.0, 1.0, swg.BF16, 4, seed=101)
     assert torch.equal(new, ref)
     check_half(to_f64(new), yhat, "noalloc call 1")
     # call 2: right after it, another shape and kernel (M > 64: 128- or
     # 256-row tiles whose last partial tile is a TMA store into the array),
     # three forced splits, beta = 0, FP32 out
-    ref, new, yhat = _both(1, 1, 300, 520, 1000, 0.5, 0.0, swg.BF16_F32OUT, 3, seed=102)
+    ref, new, yhat = _both(1, 1, 296, 520, 1000, 0.5, 0.0, swg.BF16_F32OUT, 3, seed=102)
     assert torch.equal(new, ref)
     check_f32(to_f64(new), yhat, 1000, "noalloc call 2")
     assert swg.debug_workspace_guards() == 0
