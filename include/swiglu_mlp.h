@@ -100,7 +100,15 @@ typedef enum {
  *   Split-K         chosen automatically when the output has too few tiles to
  *                   fill the GPU ("为什么 GEMM 是 CUDA 的必修课", 关键技术 item 5);
  *                   the partial sums are reduced in a fixed order, so repeated
- *                   calls give bit-identical results.  The FP32 partials live
+ *                   calls give bit-identical results.
+ *                   Few rows (M <= 64) with an automatic split: the K ranges
+ *                   of each output tile run as one thread-block cluster of up
+ *                   to 4 CTAs that sum their FP32 partials through shared
+ *                   memory, in range order -- one kernel, no workspace --
+ *                   when that occupies at least half of the SMs or splits K
+ *                   as often as the workspace path would (SWG_CLUSTER_SPLITK=0
+ *                   turns it off).
+ *                   Otherwise the FP32 partials live
  *                   in a library-owned workspace, allocated (cudaMalloc) on
  *                   first use per (device, stream) and replaced by a larger
  *                   one when a larger split needs it; replaced workspaces stay
@@ -119,7 +127,8 @@ typedef enum {
  *                   workspace) has run on that stream; a call that would have
  *                   to allocate while its stream is capturing returns
  *                   SWG_ERR_UNSUPPORTED and launches nothing.  Calls of the
- *                   one-or-two-rows kernel need no earlier run.
+ *                   one-or-two-rows kernel and of the cluster-reduced split
+ *                   need no earlier run.
  */
 SWG_API int gemm(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
          const void *A, int64_t lda, const void *B, int64_t ldb, float beta,
@@ -162,6 +171,14 @@ SWG_API int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,
  *            column pair in its final, fixed-order reduction (the gemm
  *            kernel for one or two rows); SWG_GEMV=0 keeps the tensor-core
  *            tiles.
+ *   At most 64 rows (decode of a few sequences): one 128 x 128 tile per
+ *            128 columns of the 2N-space, its K range split over a
+ *            thread-block cluster of up to 4 CTAs whose Gate and Up partials
+ *            (first M rows) are summed through shared memory, in range
+ *            order, before the pair-multiply (one kernel, no workspace), when
+ *            the tiles leave at least half of the SMs free
+ *            ("为什么 GEMM 是 CUDA 的必修课", 关键技术 item 5); otherwise, and
+ *            with SWG_CLUSTER_SPLITK=0, the persistent tiles.
  */
 SWG_API int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M,
                int64_t N, int64_t K, void *stream);

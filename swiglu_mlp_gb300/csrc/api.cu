@@ -399,6 +399,25 @@ int max_pairs(DeviceState *d, int kind, int bn)
     return n;
 }
 
+// Resident clusters of `csize` CTAs of a cluster-reduced split kernel
+// (kind 0 = few-rows GEMM, 1 = the same with e4m3, 2 = SwiGLU), cached per
+// device like max_pairs.
+int max_clusters(DeviceState *d, int kind, int bn, int csize)
+{
+    const int key = (16 + kind) * 65536 + bn * 16 + csize;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = d->max_pairs.find(key);
+        if (it != d->max_pairs.end()) return it->second;
+    }
+    const int n = kind == 0   ? swg::max_active_clusters_splitk_cl(bn, csize, d->sms)
+                  : kind == 1 ? swg::max_active_clusters_splitk_cl_fp8(bn, csize, d->sms)
+                              : swg::max_active_clusters_swiglu_cl(bn, csize, d->sms);
+    std::lock_guard<std::mutex> lk(g_mu);
+    d->max_pairs[key] = n;
+    return n;
+}
+
 // Tile mode override for tests and tuning: SWG_TILE_MODE=1cta forces
 // single-CTA 128-row tiles, =2cta forces CTA-pair 256-row tiles, =2cta128
 // and =2cta256 also fix the pair tile's width.
@@ -536,16 +555,20 @@ int splitk_swapped(DeviceState *d, const TypeInfo &ti, int transA, int transB, i
     p.err = d->err;
 
     // Automatic split: the K ranges of a tile run as one thread-block cluster
-    // whose CTAs sum their partials over distributed shared memory -- one
-    // launch, no workspace.  Cluster size: the largest of 4, 2, 1 that keeps
-    // the grid within the SMs and every range at least 4 K blocks.  Used when
-    // it gives as many ranges as the workspace path would, or at least half
-    // the SMs; otherwise (small N) the workspace path splits K further.
+    // whose CTAs sum their partials through shared memory -- one launch, no
+    // workspace.  Cluster size: the largest of 4, 2, 1 whose clusters are all
+    // resident at once (one per tile) and whose ranges are at least 4 K
+    // blocks.  Used when it gives as many ranges as the workspace path would,
+    // or at least half the SMs; otherwise (small N) the workspace path
+    // splits K further.
     int cl = 0;
     if (split_k == 0 && !cluster_splitk_disabled()) {
         int S = 1;
-        while (S < swg::MAX_CLUSTER_SPLITS && tiles * 2 * S <= d->sms && kb >= 8 * S) S *= 2;
-        if (S == splits || tiles * S * 2 >= d->sms) cl = S;
+        while (S < swg::MAX_CLUSTER_SPLITS && tiles * 2 * S <= d->sms && kb >= 8 * S &&
+               tiles <= max_clusters(d, fp8 ? 1 : 0, bn, 2 * S))
+            S *= 2;
+        // (64-row tiles keep at most 16 rows of the reduction per rank)
+        if ((S == splits || tiles * S * 2 >= d->sms) && S * 32 >= bn) cl = S;
     }
     if (cl > 0) {
         p.splits = cl;
@@ -1137,26 +1160,34 @@ int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M, int64_t N
                                  W_fused, N2, 0.0f, Y, N, s, true);
         if (rc != SWG_ERR_UNSUPPORTED) return rc;
     }
-    // At most 128 rows: one 128 x 256 tile per 256 columns of the 2N-space,
-    // with its K range cut into S pieces that run as one thread-block cluster
-    // and are summed over distributed shared memory before the pair-multiply
-    // (one launch, no workspace).  S is the largest of 4, 2 that keeps the
-    // grid within the SMs and every piece non-empty; otherwise (S = 1, many
-    // tiles) the persistent kernel below.
-    if (M <= swg::BM && !cluster_splitk_disabled()) {
+    // At most 64 rows (decode of a few sequences): one 128 x 128 tile per
+    // block of the 2N-space, only its first M rows used and exchanged, with
+    // its K range cut into S pieces that run as one
+    // thread-block cluster and are summed through shared memory before the
+    // pair-multiply (one launch, no workspace).  Otherwise (many tiles, or
+    // no cluster configuration that is resident at once) the persistent
+    // kernel below.
+    if (M <= 64 && !cluster_splitk_disabled()) {
         const int64_t kb = cdiv(K, swg::BK);
-        const int64_t tiles = cdiv(N2, 256);
-        int S = 1;
-        while (S < swg::MAX_CLUSTER_SPLITS && tiles * 2 * S <= d->sms &&
-               (2 * S - 1) * cdiv(kb, 2 * S) < kb)
-            S *= 2;
-        if (S > 1) {
+        // The cluster size using the most CTAs with every cluster resident at
+        // once.  Tiles are 128 x 128: the receive buffer of a 256-column tile
+        // would leave room for a single pipeline stage.
+        const int bn = 128;
+        const int64_t tiles = cdiv(N2, bn);
+        int S = 0;
+        for (int s_c = 2; s_c <= swg::MAX_CLUSTER_SPLITS; s_c *= 2) {
+            if (tiles * s_c > d->sms || (s_c - 1) * cdiv(kb, s_c) >= kb) continue;
+            if (tiles > max_clusters(d, 2, bn, s_c)) continue;
+            S = s_c;
+        }
+        // worth it when the tiles alone would leave half of the SMs idle
+        if (S > 0 && tiles * 2 <= d->sms) {
             CUtensorMap ta, tb, t3;
             if (!make_tmap(&ta, A, true, K, M, K, swg::BM) ||
                 !make_tmap(&tb, W_fused, true, N2, K, N2, 64))
                 return cuda_fail();
             TileParams p{};
-            p.b_mn3 = make_tmap_mn3(&t3, W_fused, true, N2, K, N2, 256 / 64);
+            p.b_mn3 = make_tmap_mn3(&t3, W_fused, true, N2, K, N2, bn / 64);
             if (p.b_mn3) tb = t3;
             p.M = (int)M;
             p.N = (int)N2;
@@ -1170,14 +1201,15 @@ int swiglu_mlp(const void *A, const void *W_fused, void *Y, int64_t M, int64_t N
             p.kb_per_split = (int)cdiv(kb, S);
             p.units = p.tiles * S;
             p.group_m = 16;
-            p.idesc = make_idesc(true, false, true, swg::BM, 256);
+            p.idesc = make_idesc(true, false, true, swg::BM, bn);
             p.b_mn_major = 1;
             p.alpha = 1.0f;
             p.D = Y;
             p.ldd = N;
             p.out_kind = swg::OUT_BF16;
             p.err = d->err;
-            if (swg::launch_tc_swiglu_cl(ta, tb, p, p.units, s) != cudaSuccess) return cuda_fail();
+            if (swg::launch_tc_swiglu_cl(bn, ta, tb, p, p.units, s) != cudaSuccess)
+                return cuda_fail();
             g_launches++;
             return SWG_OK;
         }

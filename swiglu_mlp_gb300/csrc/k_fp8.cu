@@ -67,6 +67,16 @@ cudaError_t launch_tc_splitk_cl_fp8(int bn, const CUtensorMap &ta, const CUtenso
     }
 }
 
+int max_active_clusters_splitk_cl_fp8(int bn, int csize, int sms)
+{
+    switch (bn) {
+    case 16: return max_active_clusters_impl<16, EPI_SPLITK_CL, true>(sms, csize);
+    case 32: return max_active_clusters_impl<32, EPI_SPLITK_CL, true>(sms, csize);
+    case 64: return max_active_clusters_impl<64, EPI_SPLITK_CL, true>(sms, csize);
+    default: return 0;
+    }
+}
+
 int max_active_pairs_fp8(int kind, int bn, int sms)
 {
     if (bn != 256) return 0;

@@ -154,6 +154,16 @@ cudaError_t launch_tc_splitk_cl(int bn, const CUtensorMap &ta, const CUtensorMap
     }
 }
 
+int max_active_clusters_splitk_cl(int bn, int csize, int sms)
+{
+    switch (bn) {
+    case 16: return max_active_clusters_impl<16, EPI_SPLITK_CL>(sms, csize);
+    case 32: return max_active_clusters_impl<32, EPI_SPLITK_CL>(sms, csize);
+    case 64: return max_active_clusters_impl<64, EPI_SPLITK_CL>(sms, csize);
+    default: return 0;
+    }
+}
+
 cudaError_t launch_splitk_reduce(const TileParams &p, int sms, cudaStream_t s)
 {
     const long long items = (long long)p.M * ((p.N + 3) / 4);

@@ -42,10 +42,16 @@ cudaError_t launch_tc_swiglu_dual(int bn, bool pair, const CUtensorMap &ta, cons
     }
 }
 
-cudaError_t launch_tc_swiglu_cl(const CUtensorMap &ta, const CUtensorMap &tb, const TileParams &p,
-                                int ctas, cudaStream_t s)
+cudaError_t launch_tc_swiglu_cl(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
+                                const TileParams &p, int ctas, cudaStream_t s)
 {
-    return launch_tc_impl<256, EPI_SWIGLU_CL, false>(ta, tb, p, ctas, s);
+    if (bn != 128) return cudaErrorInvalidValue;
+    return launch_tc_impl<128, EPI_SWIGLU_CL, false>(ta, tb, p, ctas, s);
+}
+
+int max_active_clusters_swiglu_cl(int bn, int csize, int sms)
+{
+    return bn == 128 ? max_active_clusters_impl<128, EPI_SWIGLU_CL>(sms, csize) : 0;
 }
 
 int max_active_pairs_dual(int bn, int sms)

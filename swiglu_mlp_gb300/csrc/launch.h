@@ -57,12 +57,16 @@ cudaError_t launch_tc_splitk_cl(int bn, const CUtensorMap &ta, const CUtensorMap
                                 const TileParams &p, int ctas, cudaStream_t s);
 cudaError_t launch_tc_splitk_cl_fp8(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
                                     const TileParams &p, int ctas, cudaStream_t s);
+// Resident clusters of `csize` CTAs of those kernels (0 if unknown).
+int max_active_clusters_splitk_cl(int bn, int csize, int sms);
+int max_active_clusters_splitk_cl_fp8(int bn, int csize, int sms);
 
 // Fused SwiGLU over W_fused for at most 128 rows with the K ranges of each
-// 128 x 256 tile reduced inside a cluster of p.splits CTAs (EPI_SWIGLU_CL);
-// `ctas` = tiles x splits.
-cudaError_t launch_tc_swiglu_cl(const CUtensorMap &ta, const CUtensorMap &tb, const TileParams &p,
-                                int ctas, cudaStream_t s);
+// 128 x bn tile (bn = 128) reduced inside a cluster of p.splits CTAs
+// (EPI_SWIGLU_CL); `ctas` = tiles x splits.
+cudaError_t launch_tc_swiglu_cl(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
+                                const TileParams &p, int ctas, cudaStream_t s);
+int max_active_clusters_swiglu_cl(int bn, int csize, int sms);
 
 // SwiGLU from separate W1 (tw1) and W2 (tw2), each K x N; BN = 128 or 256
 // (single CTA) or 256 (pair).

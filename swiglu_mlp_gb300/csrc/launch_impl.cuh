@@ -14,7 +14,7 @@ template <int BN, int EPI, bool PAIR, bool FP8 = false>
 cudaError_t launch_tc_impl(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tx,
                            const TileParams &p, int units, cudaStream_t s)
 {
-    using C = Cfg<BN, PAIR>;
+    using C = Cfg<BN, PAIR, EPI>;
     static DeviceOnce configured;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -73,7 +73,7 @@ cudaError_t launch_tc_impl(const CUtensorMap &ta, const CUtensorMap &tb, const T
 template <int BN, int EPI, bool FP8 = false>
 int max_active_pairs_impl(int sms)
 {
-    using C = Cfg<BN, true>;
+    using C = Cfg<BN, true, EPI>;
     auto kernel = tc_gemm_kernel<BN, EPI, true, FP8>;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES) != cudaSuccess)
@@ -85,6 +85,35 @@ int max_active_pairs_impl(int sms)
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+// How many clusters of `csize` single-CTA instances of this kernel can be
+// resident at once (a cluster needs csize free SMs in one GPC); 0 on error.
+template <int BN, int EPI, bool FP8 = false>
+int max_active_clusters_impl(int sms, int csize)
+{
+    using C = Cfg<BN, false, EPI>;
+    auto kernel = tc_gemm_kernel<BN, EPI, false, FP8>;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(csize * (sms / csize));
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;

@@ -118,10 +118,12 @@ __device__ __forceinline__ void bulk_commit_group()
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
-// Waits until every bulk store this thread committed has completed.
-__device__ __forceinline__ void bulk_wait_all()
+// Waits until every bulk store this thread committed has finished reading
+// its shared-memory source (the writes to global memory complete on their
+// own; the grid's completion includes them).
+__device__ __forceinline__ void bulk_wait_read_all()
 {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -383,16 +385,19 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
                  : "memory");
 }
 
-// 16-byte load from the shared memory of a CTA of this cluster
-// (cluster_addr from mapa_shared).
-__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t cluster_addr)
+// Stores to the shared memory of a CTA of this cluster (cluster_addr from
+// mapa_shared); posted, made visible to that CTA by a cluster barrier.
+__device__ __forceinline__ void st_dsmem_f32(uint32_t cluster_addr, float v)
 {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(cluster_addr)
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_dsmem_v4(uint32_t cluster_addr, uint32_t a, uint32_t b,
+                                            uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(a),
+                 "r"(b), "r"(c), "r"(d)
                  : "memory");
-    return v;
 }
 
 // Every thread of every CTA in the cluster arrives, then waits for all.

@@ -142,21 +142,32 @@ struct TileParams {
 // Tile configuration.  BN is the MMA's N (the tile width).  With PAIR, two
 // CTAs of a cluster share one 256-row MMA: each holds its 128 rows of A and
 // BN/2 columns of B per stage and receives its 128 accumulator rows.
-template <int BN, bool PAIR>
+template <int BN, bool PAIR, int EPI = EPI_STORE>
 struct Cfg {
     static constexpr int TILE_M = PAIR ? 2 * BM : BM;
     static constexpr int B_COLS = PAIR ? BN / 2 : BN;     // B columns held per CTA
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = B_COLS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    // Cluster-reduced K ranges: a receive buffer for the partials sent by
+    // every rank, beside the stages, so no rank has to wait for another's
+    // main loop to end before sending (see the cluster epilogues).
+    static constexpr int RECV_BYTES = EPI == EPI_SPLITK_CL   ? BN * BM * 4
+                                      : EPI == EPI_SWIGLU_CL ? BM * (BN + 4 * MAX_CLUSTER_SPLITS) * 4
+                                                             : 0;
     // 192 KB of stages (measured: a seventh 32 KB pair stage did not help
-    // and shrank L1), at most 12.
-    static constexpr int STAGES_RAW = (192 * 1024) / STAGE_BYTES;
+    // and shrank L1), at most 12, within the 227 KB a CTA can have.
+    static constexpr int STAGE_BUDGET_RAW = 232448 - 2048 - RECV_BYTES;
+    static constexpr int STAGE_BUDGET =
+        STAGE_BUDGET_RAW < 192 * 1024 ? STAGE_BUDGET_RAW : 192 * 1024;
+    static constexpr int STAGES_RAW = STAGE_BUDGET / STAGE_BYTES;
     static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
     static constexpr int NUM_BARS = 2 * STAGES + 6;
     static constexpr int TMEM_COLS = (2 * BN) <= 32 ? 32 : (2 * BN) <= 64 ? 64
                                    : (2 * BN) <= 128 ? 128 : (2 * BN) <= 256 ? 256 : 512;
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 64;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + RECV_BYTES + NUM_BARS * 8 + 64;
+    static_assert(STAGES >= 3, "pipeline too shallow");
+    static_assert(SMEM_BYTES <= 232448, "beyond the per-CTA shared memory");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "BN must be a multiple of 16, <= 256");
     static_assert(!PAIR || BN % 128 == 0, "pair tiles split B in 64-column boxes per CTA");
     static_assert(STAGES * STAGE_BYTES >= BM * BN * 4 || BN < 64,
@@ -464,91 +475,73 @@ __device__ __forceinline__ void store_staged(const TileParams &p, const CUtensor
             tma_store_2d(tm, base + b * 16384, x, m0);
     }
     bulk_commit_group();
-    bulk_wait_all();
+    // The staged tile is the CTA's last: only its shared-memory source has to
+    // outlive the copy.
+    bulk_wait_read_all();
 }
 
-// ------------------------------------------------ cluster split-K epilogue
-// EPI_SPLITK_CL, run by the eight epilogue warps of each CTA of a cluster of
-// S = p.splits CTAs (kernel frame: TMEM lane = output column n of the tile,
-// TMEM column j = output row m).
-//   1. Before the accumulator is ready, each thread loads the C values of the
-//      outputs it will produce (beta != 0), so that DRAM read overlaps the
-//      main loop.
-//   2. The accumulator (128 lanes x BN columns, FP32) goes to this CTA's own
-//      shared memory as part[j][lane] (the consumed pipeline stages).
-//   3. Cluster barrier (every thread of every CTA arrives; release/acquire at
-//      cluster scope orders the parked partials before the remote reads).
-//   4. This rank owns output rows [r * BN / S, (r + 1) * BN / S) of the tile:
-//      for each group of four columns it reads the partials of ranks
-//      0, 1, .., S-1 over distributed shared memory, sums them in that
-//      order starting from 0, and stores alpha * sum + beta * C.
-// The teardown's cluster barrier keeps every CTA's shared memory alive until
-// all ranks have read it.
+// ------------------------------------------------ cluster split-K epilogues
+// The K ranges of one tile run on the S = p.splits CTAs of a cluster, one
+// range per rank.  Rank r owns a share of the tile's outputs.  As soon as its
+// accumulator is complete, each CTA pushes every piece of its FP32 partial
+// to the owner's receive buffer recv[source rank][...] (a region of that
+// CTA's shared memory beside its pipeline stages; stores to distributed
+// shared memory are posted, loads from it would wait a round trip each).
+// One cluster barrier (release/acquire at cluster scope; the producer and
+// MMA warps take part too) makes them visible, and the owner sums recv[0],
+// recv[1], .., recv[S-1] from its own shared memory, in that order starting
+// from 0, before the epilogue arithmetic.  After that barrier no CTA touches
+// another's shared memory.
+
+// EPI_SPLITK_CL (swapped-operand frame: TMEM lane = output column n of the
+// tile, TMEM column j = output row m).  Rank r owns output rows
+// [r * BN / S, (r + 1) * BN / S) of the tile; recv[s][n][j - r * BN / S], so
+// each thread pushes four consecutive rows of its column with one 16-byte
+// store.  Before the accumulator is ready each thread loads the C values of
+// the outputs it will produce (beta != 0), so that read overlaps the main
+// loop.
 template <int BN>
 __device__ __forceinline__ void splitk_cluster_epilogue(const TileParams &p, uint32_t tmem_base,
-                                                        uint8_t *smem, uint64_t *acc_full,
+                                                        uint8_t *recv_buf, uint64_t *acc_full,
                                                         volatile int *abort_flag, int unit,
                                                         int krank)
 {
-    constexpr int ITEMS = BN / 8;              // float4 items per thread when S = 1
+    // items (4 rows x 1 column) per thread: (BN / S / 4) * 128 / 256; the
+    // host runs BN = 64 with S >= 2 only
+    constexpr int ITEMS = BN / 8 > 4 ? 4 : BN / 8;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int et = threadIdx.x - EPI_WARP0 * 32;     // 0 .. 255
     const int S = p.splits;
     int mb, nb, split, tile;
     unit_coords(p, unit, mb, nb, split, tile);
-    const int rows = BN / S;                   // output rows this rank reduces
-    const int n_items = rows * (BM / 4);
+    const int rows = BN / S;                   // output rows this rank reduces (>= 4)
+    const int n_items = (rows / 4) * BM;
     const int Mo = p.N, No = p.M;              // output rows / columns
+    // item idx: column n = idx % BM of the tile, rows 4 * (idx / BM) .. + 3 of this rank's share
     float c[ITEMS][4];
 #pragma unroll
     for (int it = 0; it < ITEMS; ++it) {
         c[it][0] = c[it][1] = c[it][2] = c[it][3] = 0.0f;
         const int idx = et + it * NUM_EPI_THREADS;
         if (p.beta == 0.0f || idx >= n_items) continue;
-        const int m = nb * BN + krank * rows + idx / (BM / 4);
-        const int n = mb * BM + (idx % (BM / 4)) * 4;
-        if (m >= Mo || n >= No) continue;
-        const long long off = (long long)m * p.ldd + n;
-        if (No - n >= 4) {
-            if (p.out_kind == OUT_F32) {
-                const float4 v = *reinterpret_cast<const float4 *>(
-                    reinterpret_cast<const float *>(p.D) + off);
-                c[it][0] = v.x;
-                c[it][1] = v.y;
-                c[it][2] = v.z;
-                c[it][3] = v.w;
-            } else {
-                const uint2 w = *reinterpret_cast<const uint2 *>(
-                    reinterpret_cast<const uint16_t *>(p.D) + off);
-                const uint32_t ww[2] = {w.x, w.y};
+        const int n = mb * BM + idx % BM;
+        const int m0 = nb * BN + krank * rows + 4 * (idx / BM);
+        if (n >= No) continue;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    if (p.out_kind == OUT_F16) {
-                        const __half2 c2 = *reinterpret_cast<const __half2 *>(&ww[h]);
-                        c[it][2 * h] = __low2float(c2);
-                        c[it][2 * h + 1] = __high2float(c2);
-                    } else {
-                        const __nv_bfloat162 c2 = *reinterpret_cast<const __nv_bfloat162 *>(&ww[h]);
-                        c[it][2 * h] = __low2float(c2);
-                        c[it][2 * h + 1] = __high2float(c2);
-                    }
-                }
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (j < No - n) c[it][j] = load_out(p.D, off + j, p.out_kind);
-        }
+        for (int i = 0; i < 4; ++i)
+            if (m0 + i < Mo) c[it][i] = load_out(p.D, (long long)(m0 + i) * p.ldd + n, p.out_kind);
     }
 
-    // 2. park the partial: part[j][lane], j < BN, lane < 128
-    float *part = reinterpret_cast<float *>(smem);
+    // push: rows jj .. jj + 3 of this thread's column go to rank jj / rows
+    const uint32_t recv = smem_u32(recv_buf);
+    const uint32_t slice = (uint32_t)(rows * BM * 4);        // bytes of one source's slice
     constexpr int W = BN >= 32 ? 32 : 16;
     const int q = warp & 3;
     const int h = (warp - EPI_WARP0) / 4;
     const bool active = (BN == 64) || h == 0;
     const int j0 = BN == 64 ? h * 32 : 0;
+    const int n_local = q * 32 + lane;
     bool ok = wait_bounded(smem_u32(&acc_full[0]), 0, abort_flag, p.err);
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
@@ -558,140 +551,128 @@ __device__ __forceinline__ void splitk_cluster_epilogue(const TileParams &p, uin
             tmem_ld_cols(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + j0, r);
             tmem_ld_wait(r);
 #pragma unroll
-            for (int j = 0; j < W; ++j) part[(j0 + j) * BM + q * 32 + lane] = __uint_as_float(r[j]);
+            for (int g = 0; g < W / 4; ++g) {
+                const int jj = j0 + 4 * g;
+                if (nb * BN + jj >= Mo) break;     // rows past the output are not sent
+                const int owner = jj / rows;
+                const uint32_t a = recv + (uint32_t)krank * slice +
+                                   (uint32_t)((n_local * rows + jj - owner * rows) * 4);
+                st_dsmem_v4(mapa_shared(a, (uint32_t)owner), r[4 * g], r[4 * g + 1], r[4 * g + 2],
+                            r[4 * g + 3]);
+            }
         }
     }
     tc_fence_before();
-    // 3. every rank's partial is parked
     cluster_sync_all();
-    // 4. reduce this rank's rows in rank order and store D
-    const uint32_t part_addr = smem_u32(part);
+    // reduce this rank's rows from the local receive buffer, sources in order
+    const float *rb = reinterpret_cast<const float *>(recv_buf);
 #pragma unroll
     for (int it = 0; it < ITEMS; ++it) {
         const int idx = et + it * NUM_EPI_THREADS;
         if (idx >= n_items) continue;
-        const int ml = krank * rows + idx / (BM / 4);
-        const int nl = (idx % (BM / 4)) * 4;
-        const int m = nb * BN + ml;
+        const int nl = idx % BM;
+        const int jl = 4 * (idx / BM);
         const int n = mb * BM + nl;
-        if (m >= Mo || n >= No) continue;
-        const uint32_t a = part_addr + (uint32_t)((ml * BM + nl) * 4);
-        float4 v[MAX_CLUSTER_SPLITS];
-#pragma unroll
-        for (int r = 0; r < MAX_CLUSTER_SPLITS; ++r)
-            if (r < S) v[r] = ld_dsmem_f4(mapa_shared(a, (uint32_t)r));
+        const int m0 = nb * BN + krank * rows + jl;
+        if (n >= No) continue;
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int r = 0; r < MAX_CLUSTER_SPLITS; ++r) {
             if (r < S) {
-                acc[0] += v[r].x;
-                acc[1] += v[r].y;
-                acc[2] += v[r].z;
-                acc[3] += v[r].w;
+                const float4 v = *reinterpret_cast<const float4 *>(
+                    rb + (size_t)r * (slice / 4) + nl * rows + jl);
+                acc[0] += v.x;
+                acc[1] += v.y;
+                acc[2] += v.z;
+                acc[3] += v.w;
             }
         }
-        float out[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            out[j] = p.beta != 0.0f ? __fmaf_rn(p.beta, c[it][j], p.alpha * acc[j])
-                                    : p.alpha * acc[j];
-        const long long off = (long long)m * p.ldd + n;
-        if (No - n >= 4) {
-            if (p.out_kind == OUT_F32)
-                *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.D) + off) =
-                    make_float4(out[0], out[1], out[2], out[3]);
-            else
-                *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(p.D) + off) =
-                    make_uint2(pack2(out[0], out[1], p.out_kind), pack2(out[2], out[3], p.out_kind));
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (j < No - n) store_out(p.D, off + j, out[j], p.out_kind);
+        for (int i = 0; i < 4; ++i) {
+            if (m0 + i < Mo) {
+                const float out = p.beta != 0.0f ? __fmaf_rn(p.beta, c[it][i], p.alpha * acc[i])
+                                                 : p.alpha * acc[i];
+                store_out(p.D, (long long)(m0 + i) * p.ldd + n, out, p.out_kind);
+            }
         }
     }
 }
 
-// EPI_SWIGLU_CL, run by the eight epilogue warps of each CTA of a cluster of
-// S = p.splits CTAs, one K range each (output frame: TMEM lane = row of the
-// tile, TMEM column = 2N-space column, Gate at even and Up at odd columns).
-//   1. The accumulator goes to this CTA's own shared memory, row-major with
-//      a row stride of BN + 4 floats (16-byte stores without bank conflicts).
-//   2. Cluster barrier, as in splitk_cluster_epilogue.
-//   3. Rank r owns the tile's 2N-space columns [r * BN / S, (r + 1) * BN / S):
-//      for each row and group of 16 columns (8 outputs) it reads ranks
-//      0, 1, .., S-1 over distributed shared memory, sums in that order from
-//      0, forms y = SiLU(alpha * gate) * (alpha * up) per pair, rounds once to
-//      bf16 and stores 16 bytes of Y.
+// EPI_SWIGLU_CL (output frame: TMEM lane = row of the tile, TMEM column =
+// 2N-space column, Gate at even and Up at odd columns).  Rank r owns the
+// tile's 2N-space columns [r * BN / S, (r + 1) * BN / S);
+// recv[s][row][column - r * BN / S], rows padded by 4 floats (16-byte stores
+// and loads without bank conflicts).  For each row and group of 16 columns
+// (8 outputs) the owner forms y = SiLU(alpha * gate) * (alpha * up) per
+// pair, rounds once to bf16 and stores 16 bytes of Y.
 template <int BN>
 __device__ __forceinline__ void swiglu_cluster_epilogue(const TileParams &p, uint32_t tmem_base,
-                                                        uint8_t *smem, uint64_t *acc_full,
+                                                        uint8_t *recv_buf, uint64_t *acc_full,
                                                         volatile int *abort_flag, int unit,
                                                         int krank)
 {
-    constexpr int LD = BN + 4;
     constexpr int NC = BN / 32;                // 32-column chunks per tile row
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int et = threadIdx.x - EPI_WARP0 * 32;
     const int S = p.splits;
+    const int cols = BN / S;                   // 2N-space columns per rank (>= 32)
+    const int ld = cols + 4;                   // row stride of a receive slice, floats
+    const uint32_t slice = (uint32_t)(BM * ld * 4);
     int mb, nb, split, tile;
     unit_coords(p, unit, mb, nb, split, tile);
-    float *part = reinterpret_cast<float *>(smem);
+    const uint32_t recv = smem_u32(recv_buf);
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const int c_begin = ((warp - EPI_WARP0) / 4) * (NC / 2);
     bool ok = wait_bounded(smem_u32(&acc_full[0]), 0, abort_flag, p.err);
     ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
+    if (ok && __any_sync(0xffffffffu, mb * BM + row < p.M)) {
         tc_fence_after();
         const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        const bool send = mb * BM + row < p.M;  // rows past the output are not sent
 #pragma unroll 1
         for (int c = c_begin; c < c_begin + NC / 2; ++c) {
             uint32_t r[32];
-            tmem_ld_32cols(t_row + c * 32, r);
+            tmem_ld_32cols(t_row + c * 32, r);   // whole warp (.sync.aligned)
             tmem_ld_wait(r);
-            float4 *dst = reinterpret_cast<float4 *>(part + row * LD + c * 32);
+            if (!send) continue;
+            const int owner = (c * 32) / cols;
+            const uint32_t a = mapa_shared(
+                recv + (uint32_t)krank * slice + (uint32_t)((row * ld + c * 32 - owner * cols) * 4),
+                (uint32_t)owner);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                     __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                st_dsmem_v4(a + 16 * j, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
         }
     }
     tc_fence_before();
     cluster_sync_all();
-    const uint32_t part_addr = smem_u32(part);
-    const int cols = BN / S;                   // this rank's 2N-space columns
+    const float *rb = reinterpret_cast<const float *>(recv_buf);
     const int n_items = BM * (cols / 16);
     const int n_out = p.N / 2;                 // output columns (p.N is the 2N-space width)
 #pragma unroll 1
     for (int idx = et; idx < n_items; idx += NUM_EPI_THREADS) {
         const int rr = idx % BM;
-        const int c0 = krank * cols + (idx / BM) * 16;
+        const int cl = (idx / BM) * 16;        // column within this rank's share
         const int m = mb * BM + rr;
-        const int n = (nb * BN + c0) / 2;      // first output column of the item
+        const int n = (nb * BN + krank * cols + cl) / 2;   // first output column
         if (m >= p.M || n >= n_out) continue;
-        const uint32_t a = part_addr + (uint32_t)((rr * LD + c0) * 4);
-        float4 v[MAX_CLUSTER_SPLITS][4];
-#pragma unroll
-        for (int r = 0; r < MAX_CLUSTER_SPLITS; ++r) {
-            if (r < S) {
-                const uint32_t ra = mapa_shared(a, (uint32_t)r);
-#pragma unroll
-                for (int w = 0; w < 4; ++w) v[r][w] = ld_dsmem_f4(ra + 16 * w);
-            }
-        }
         float acc[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
 #pragma unroll
         for (int r = 0; r < MAX_CLUSTER_SPLITS; ++r) {
             if (r < S) {
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    rb + (size_t)r * (slice / 4) + rr * ld + cl);
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
-                    acc[4 * w] += v[r][w].x;
-                    acc[4 * w + 1] += v[r][w].y;
-                    acc[4 * w + 2] += v[r][w].z;
-                    acc[4 * w + 3] += v[r][w].w;
+                    const float4 v = src[w];
+                    acc[4 * w] += v.x;
+                    acc[4 * w + 1] += v.y;
+                    acc[4 * w + 2] += v.z;
+                    acc[4 * w + 3] += v.w;
                 }
             }
         }
@@ -720,7 +701,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmX, const TileParams p)
 {
-    using C = Cfg<BN, PAIR>;
+    using C = Cfg<BN, PAIR, EPI>;
     constexpr int S = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte swizzled stages need 1024-byte alignment.
@@ -728,7 +709,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + S * C::A_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + S * C::B_BYTES);
+    uint8_t *recv = sB + S * C::B_BYTES;     // cluster-reduced K: partials received
+    uint64_t *bars = reinterpret_cast<uint64_t *>(recv + C::RECV_BYTES);
     uint64_t *full = bars;
     uint64_t *empty = bars + S;
     uint64_t *acc_full = bars + 2 * S;
@@ -758,6 +740,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // (griddepcontrol.wait) until this grid has completed and its writes are
     // visible.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // The kernel parameters sit in constant memory, which a CTA's first
+    // access fetches from L2 or DRAM (about half a microsecond measured at
+    // the producer's first unit): touch the scheduling fields now, so that
+    // miss overlaps the set-up instead of delaying the first loads.
+    asm volatile("" ::"r"(p.units), "r"(p.tiles), "r"(p.kb_per_split), "r"(p.k_blocks),
+                 "r"(p.group_m), "r"(p.n_blocks), "r"(p.m_blocks), "r"(p.bk));
 
     if (threadIdx.x == 0) {
         // Tensor maps are fetched from memory on first use: start that now.
@@ -912,7 +900,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
         __syncwarp();
-        if (CLK) cluster_sync_all();   // partials parked (see the epilogue)
+        if (CLK) cluster_sync_all();   // partials pushed (see the cluster epilogues)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && leader) {
@@ -985,11 +973,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             wait_bounded(smem_u32(mma_done), 0, abort_flag, p.err, false, DRAIN_LIMIT_NS);
         }
         __syncwarp();
-        if (CLK) cluster_sync_all();   // partials parked (see the epilogue)
+        if (CLK) cluster_sync_all();   // partials pushed (see the cluster epilogues)
     } else if (EPI == EPI_SPLITK_CL) {
-        splitk_cluster_epilogue<BN>(p, tmem_base, smem, acc_full, abort_flag, first_unit, krank);
+        splitk_cluster_epilogue<BN>(p, tmem_base, recv, acc_full, abort_flag, first_unit, krank);
     } else if (EPI == EPI_SWIGLU_CL) {
-        swiglu_cluster_epilogue<BN>(p, tmem_base, smem, acc_full, abort_flag, first_unit, krank);
+        swiglu_cluster_epilogue<BN>(p, tmem_base, recv, acc_full, abort_flag, first_unit, krank);
     } else if (EPI == EPI_SWIGLU_DUAL) {
         // ------------------------------------------ epilogue (separate W1, W2)
         // Output column j of the tile = SiLU(acc[j]) * acc[BN/2 + j]; warps
@@ -1169,9 +1157,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
     // Pair mode: neither CTA may free its tensor memory or exit while the
-    // leader's MMAs or the peer's arrivals can still reach it.  Cluster
-    // split-K: nor while another rank still reads its parked partial.
-    if (PAIR || CLK)
+    // leader's MMAs or the peer's arrivals can still reach it.  (Cluster-
+    // reduced K: after the cluster barrier of the epilogue nothing reaches
+    // another CTA's shared memory any more.)
+    if (PAIR)
         cluster_sync_all();
     else
         __syncthreads();
