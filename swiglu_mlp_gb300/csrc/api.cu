@@ -272,19 +272,19 @@ bool make_tmap(CUtensorMap *m, const void *ptr, bool bf16, int64_t inner, int64_
 
 // MN-major operand whose MN extent `mn` is a multiple of 64, viewed in 3-D
 // as (64 contiguous MN elements, K rows at the row stride, mn / 64 atoms 128
-// bytes apart): one box of {64, 64, atoms} fills `atoms` consecutive 8 KB
-// swizzle atoms of a stage, the layout two 2-D {64, 64} boxes give, with one
-// TMA instruction.  Rows past K read as zero; with mn a multiple of 64 no box
+// bytes apart): one box of {64, kbox, atoms} fills `atoms` consecutive
+// (kbox x 128-byte) swizzle atoms of a stage, the layout separate 2-D
+// {64, kbox} boxes give, with one TMA instruction.  Rows past K read as zero; with mn a multiple of 64 no box
 // reaches past a row's last element.  Returns false (and the caller keeps the
 // 2-D map) if the driver declines the encoding.
 bool make_tmap_mn3(CUtensorMap *m, const void *ptr, bool bf16, int64_t mn, int64_t k, int64_t ld,
-                   int atoms)
+                   int atoms, int kbox = 64)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn || mn % 64 != 0 || mn_3d_disabled()) return false;
     cuuint64_t dims[3] = {64u, (cuuint64_t)k, (cuuint64_t)(mn / 64)};
     cuuint64_t strides[2] = {(cuuint64_t)ld * 2, 128u};
-    cuuint32_t box[3] = {64u, 64u, (cuuint32_t)atoms};
+    cuuint32_t box[3] = {64u, (cuuint32_t)kbox, (cuuint32_t)atoms};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                     const_cast<void *>(ptr), dims, strides, box, estr,
@@ -491,8 +491,10 @@ bool cluster_splitk_disabled()
 
 // Split-K GEMM with swapped operands for M <= 64: the kernel computes
 // D^T = op(B)^T op(A)^T with op(B)^T (N x K) as its 128-row operand and
-// op(A)^T as its BN-column operand, writes transposed FP32 partials
-// ws[split][m][n], and the usual in-order reduction forms D.
+// op(A)^T as its BN-column operand.  With an automatic split the K ranges of
+// a tile run as one thread-block cluster that reduces them itself (one
+// launch, EPI_SPLITK_CL); otherwise the kernel writes transposed FP32
+// partials ws[split][m][n] and the usual in-order reduction forms D.
 // With fp8 (e4m3 A and B; op(A) = A and op(B) = B^T, both K-major) the
 // K blocks are 128 elements, the same 128-byte rows, and the MMA is
 // kind::f8f6f4; everything else is shared.
@@ -517,6 +519,26 @@ int splitk_swapped(DeviceState *d, const TypeInfo &ti, int transA, int transB, i
     const int kbps = (int)cdiv(kb, splits);
     splits = (int)cdiv(kb, kbps);
 
+    // Automatic split: the K ranges of a tile run as one thread-block cluster
+    // whose CTAs sum their partials through shared memory -- one launch, no
+    // workspace.  Cluster size: the largest of 4, 2, 1 whose clusters are all
+    // resident at once (one per tile) and whose ranges are at least 4 K
+    // blocks.  Used when it gives as many ranges as the workspace path would,
+    // or at least half the SMs; otherwise (small N) the workspace path
+    // splits K further.
+    int cl = 0;
+    if (split_k == 0 && !cluster_splitk_disabled()) {
+        int S = 1;
+        while (S < swg::MAX_CLUSTER_SPLITS && tiles * 2 * S <= d->sms && kb >= 8 * S &&
+               tiles <= max_clusters(d, fp8 ? 1 : 0, bn, 2 * S))
+            S *= 2;
+        // (64-row tiles keep at most 16 rows of the reduction per rank)
+        if ((S == splits || tiles * S * 2 >= d->sms) && S * 32 >= bn) cl = S;
+    }
+    // K atoms (128 bytes of K) per pipeline stage: two on the cluster path
+    // (MN-major boxes then span 128 K rows), one on the workspace path.
+    const int kps = cl > 0 ? 2 : 1;
+
     // op(B)^T is the kernel's A operand: MN-major when B is stored K x N (op N).
     const bool aT_mn = transB == SWG_OP_N;
     CUtensorMap ta, tb;
@@ -524,17 +546,18 @@ int splitk_swapped(DeviceState *d, const TypeInfo &ti, int transA, int transB, i
     if (fp8) {
         ok = make_tmap_u8(&ta, B, K, N, ldb, swg::BM) && make_tmap_u8(&tb, A, K, M, lda, bn);
     } else {
-        ok = aT_mn ? make_tmap(&ta, B, ti.in_bf16, N, K, ldb, 64)
+        ok = aT_mn ? make_tmap(&ta, B, ti.in_bf16, N, K, ldb, 64 * kps)
                    : make_tmap(&ta, B, ti.in_bf16, K, N, ldb, swg::BM);
-        ok = ok && (bT_mn ? make_tmap(&tb, A, ti.in_bf16, M, K, lda, 64)
+        ok = ok && (bT_mn ? make_tmap(&tb, A, ti.in_bf16, M, K, lda, 64 * kps)
                           : make_tmap(&tb, A, ti.in_bf16, K, M, lda, bn));
     }
     if (!ok) return cuda_fail();
     // MN-major operands: one 3-D box per stage where the extent allows.
     CUtensorMap t3;
-    const bool a3 = !fp8 && aT_mn && make_tmap_mn3(&t3, B, ti.in_bf16, N, K, ldb, swg::BM / 64);
+    const bool a3 =
+        !fp8 && aT_mn && make_tmap_mn3(&t3, B, ti.in_bf16, N, K, ldb, swg::BM / 64, 64 * kps);
     if (a3) ta = t3;
-    const bool b3 = !fp8 && bT_mn && make_tmap_mn3(&t3, A, ti.in_bf16, M, K, lda, bn / 64);
+    const bool b3 = !fp8 && bT_mn && make_tmap_mn3(&t3, A, ti.in_bf16, M, K, lda, bn / 64, 64 * kps);
     if (b3) tb = t3;
 
     TileParams p{};           // in the kernel's (transposed) frame
@@ -554,28 +577,15 @@ int splitk_swapped(DeviceState *d, const TypeInfo &ti, int transA, int transB, i
     p.b_mn_major = bT_mn;
     p.err = d->err;
 
-    // Automatic split: the K ranges of a tile run as one thread-block cluster
-    // whose CTAs sum their partials through shared memory -- one launch, no
-    // workspace.  Cluster size: the largest of 4, 2, 1 whose clusters are all
-    // resident at once (one per tile) and whose ranges are at least 4 K
-    // blocks.  Used when it gives as many ranges as the workspace path would,
-    // or at least half the SMs; otherwise (small N) the workspace path
-    // splits K further.
-    int cl = 0;
-    if (split_k == 0 && !cluster_splitk_disabled()) {
-        int S = 1;
-        while (S < swg::MAX_CLUSTER_SPLITS && tiles * 2 * S <= d->sms && kb >= 8 * S &&
-               tiles <= max_clusters(d, fp8 ? 1 : 0, bn, 2 * S))
-            S *= 2;
-        // (64-row tiles keep at most 16 rows of the reduction per rank)
-        if ((S == splits || tiles * S * 2 >= d->sms) && S * 32 >= bn) cl = S;
-    }
     if (cl > 0) {
+        // K is walked in stages of kps atoms: k_blocks counts stages
+        const int64_t ks = cdiv(K, (int64_t)bk * kps);
+        p.k_blocks = (int)ks;
         p.splits = cl;
-        p.kb_per_split = (int)cdiv(kb, cl);
+        p.kb_per_split = (int)cdiv(ks, cl);
         p.units = p.tiles * cl;
-        // every rank has at least one K block (S <= kb / 4 guarantees it)
-        if ((int64_t)(cl - 1) * p.kb_per_split >= kb) return SWG_ERR_UNSUPPORTED;
+        // every rank has at least one stage (ranges of >= 4 atoms guarantee it)
+        if ((int64_t)(cl - 1) * p.kb_per_split >= ks) return SWG_ERR_UNSUPPORTED;
         p.alpha = alpha;
         p.beta = beta;
         p.D = C;

@@ -146,8 +146,13 @@ template <int BN, bool PAIR, int EPI = EPI_STORE>
 struct Cfg {
     static constexpr int TILE_M = PAIR ? 2 * BM : BM;
     static constexpr int B_COLS = PAIR ? BN / 2 : BN;     // B columns held per CTA
-    static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = B_COLS * BK * 2;
+    // 128-byte K atoms per pipeline stage.  The few-rows cluster kernel moves
+    // two per stage (one barrier round and one TMA issue per 32 KB of the
+    // weight instead of per 16 KB): its per-SM rate was bound by the
+    // producer's per-stage latency, not by bytes.
+    static constexpr int KPS = EPI == EPI_SPLITK_CL ? 2 : 1;
+    static constexpr int A_BYTES = BM * BK * 2 * KPS;
+    static constexpr int B_BYTES = B_COLS * BK * 2 * KPS;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     // Cluster-reduced K ranges: a receive buffer for the partials sent by
     // every rank, beside the stages, so no rank has to wait for another's
@@ -829,7 +834,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     const uint32_t a_dst = smem_u32(sA + stage * C::A_BYTES);
                     const uint32_t b_dst = smem_u32(sB + stage * C::B_BYTES);
-                    const int k0 = kb * p.bk;
+                    const int k0 = kb * p.bk * C::KPS;       // first K element of the stage
                     auto load = [&](uint32_t dst, const CUtensorMap *tm, int x, int y) {
                         if (PAIR)
                             tma_load_2d_pair(dst, tm, fb, x, y);
@@ -842,13 +847,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         else
                             tma_load_3d(dst, tm, fb, 0, y, z);
                     };
+                    // (MN-major boxes span all C::KPS atoms of K rows: {64, 64 KPS, ..})
                     if (!p.a_mn_major) {
-                        load(a_dst, &tmA, k0, m0);                          // box {64 K, 128 M}
+#pragma unroll
+                        for (int j = 0; j < C::KPS; ++j)                  // box {64 K, 128 M}
+                            load(a_dst + j * (BM * 128), &tmA, k0 + j * p.bk, m0);
                     } else if (p.a_mn3) {
                         load3(a_dst, &tmA, k0, m0 / 64);                    // box {64 M, 64 K, 2}
                     } else {
                         load(a_dst, &tmA, m0, k0);                          // box {64 M, 64 K}
-                        load(a_dst + 8192, &tmA, m0 + 64, k0);
+                        load(a_dst + 8192 * C::KPS, &tmA, m0 + 64, k0);
                     }
                     if (EPI == EPI_SWIGLU_DUAL) {
                         // W1 / W2 are K x N (N-major), boxes {64 N, 64 K}.  Pair:
@@ -871,13 +879,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             }
                         }
                     } else if (!p.b_mn_major) {
-                        load(b_dst, &tmB, k0, n0);                          // box {64 K, B_COLS N}
+#pragma unroll
+                        for (int j = 0; j < C::KPS; ++j)                  // box {64 K, B_COLS N}
+                            load(b_dst + j * (C::B_COLS * 128), &tmB, k0 + j * p.bk, n0);
                     } else if (p.b_mn3) {
                         load3(b_dst, &tmB, k0, n0 / 64);                    // box {64 N, 64 K, B_COLS / 64}
                     } else {
 #pragma unroll
                         for (int c = 0; c < C::B_COLS / 64; ++c)            // box {64 N, 64 K}
-                            load(b_dst + c * 8192, &tmB, n0 + c * 64, k0);
+                            load(b_dst + c * 8192 * C::KPS, &tmB, n0 + c * 64, k0);
                     }
                     if (++stage == S) {
                         stage = 0;
@@ -906,10 +916,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0 && leader) {
             // K-major operand: next K=16 slice is 32 bytes further in the
             // swizzled row; MN-major: two 8-row K groups (2 x 1024 bytes) further.
+            // With C::KPS > 1 a K-major operand's atoms follow each other
+            // (rows x 128 bytes apart); an MN-major atom holds 64 KPS K rows.
             const uint32_t a_kstep = p.a_mn_major ? 2048u : 32u;
             const uint32_t b_kstep = p.b_mn_major ? 2048u : 32u;
-            const uint32_t a_lbo = p.a_mn_major ? 8192u : 16u;
-            const uint32_t b_lbo = p.b_mn_major ? 8192u : 16u;
+            const uint32_t a_lbo = p.a_mn_major ? 8192u * C::KPS : 16u;
+            const uint32_t b_lbo = p.b_mn_major ? 8192u * C::KPS : 16u;
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -937,9 +949,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t a_base = smem_u32(sA + stage * C::A_BYTES);
                     const uint32_t b_base = smem_u32(sB + stage * C::B_BYTES);
 #pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        const uint64_t ad = smem_desc(a_base + kk * a_kstep, a_lbo, 1024);
-                        const uint64_t bd = smem_desc(b_base + kk * b_kstep, b_lbo, 1024);
+                    for (int kk = 0; kk < C::KPS * (BK / UMMA_K); ++kk) {
+                        const int j = kk / (BK / UMMA_K), kq = kk % (BK / UMMA_K);
+                        const uint32_t a_off = p.a_mn_major ? kk * a_kstep
+                                                            : j * (BM * 128) + kq * a_kstep;
+                        const uint32_t b_off = p.b_mn_major ? kk * b_kstep
+                                                            : j * (C::B_COLS * 128) + kq * b_kstep;
+                        const uint64_t ad = smem_desc(a_base + a_off, a_lbo, 1024);
+                        const uint64_t bd = smem_desc(b_base + b_off, b_lbo, 1024);
                         const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
                         if (PAIR && FP8)
                             tc_mma_f8_pair(d_tmem, ad, bd, p.idesc, accum);
