@@ -512,9 +512,12 @@ def component_cases():
     cases = [(f"swiglu_small_M{m}", "swiglu", m, 896, 4864) for m in (1, 128, 512, 2048)]
     cases += [(f"swiglu_8b_M{m}", "swiglu", m, 4096, 14336) for m in (1, 512, 2048, 8192)]
     cases += [(f"skinny_splitk_M{m}", "skinny", m, 16384, 4096) for m in (16, 32, 64)]
-    # the same call through gemm_splitk_noalloc (partials in the library's
-    # fixed array instead of a cudaMalloc'd workspace)
-    cases += [("skinny_splitk_M16_noalloc", "skinny_noalloc", 16, 16384, 4096)]
+    # four explicit K ranges through gemm_splitk_noalloc (partials in the
+    # library's fixed array instead of a cudaMalloc'd workspace) and, for
+    # comparison, through gemm_ex (the workspace path); the automatic split
+    # of the rows above reduces inside a cluster and needs neither
+    cases += [("skinny_splitk_M16_noalloc_split4", "skinny_noalloc", 16, 16384, 4096),
+              ("skinny_splitk_M16_ws_split4", "skinny_ws4", 16, 16384, 4096)]
     cases += [(f"decode_gemv_M{m}", "gemv", m, 4096, 4096) for m in (1, 8)]
     cases += [("mlp_small_M2048", "mlp", 2048, 896, 4864), ("mlp_8b_M2048", "mlp", 2048, 4096, 14336),
               ("mlp_8b_M1", "mlp", 1, 4096, 14336)]
@@ -548,14 +551,15 @@ def build_case(kind, M, K, N, dev, stream):
         def fn():
             swg.swiglu_mlp(Ad, Wf, Y, M, N, K, stream=stream)
         return fn, None, 2.0 * M * 2 * N * K, (M * K + K * 2 * N + M * N) * 2
-    if kind in ("skinny", "skinny_noalloc"):
+    if kind in ("skinny", "skinny_noalloc", "skinny_ws4"):
         A, B, C = synth.skinny(M, N, K)
         Ad, Bd, C0 = A.to(dev), B.to(dev), C.to(dev)
         Cd = C0.clone()
         call = swg.gemm_splitk_noalloc if kind == "skinny_noalloc" else swg.gemm_ex
+        split = 0 if kind == "skinny" else 4
 
         def fn():
-            call(0, 0, M, N, K, 1.0, Ad, K, Bd, N, 1.0, Cd, N, swg.BF16, 0, stream=stream)
+            call(0, 0, M, N, K, 1.0, Ad, K, Bd, N, 1.0, Cd, N, swg.BF16, split, stream=stream)
 
         def reset():
             Cd.copy_(C0)
@@ -717,7 +721,7 @@ def run_components(args, dev, stream):
         if hot_ms is not None:
             entry["hot_l2"] = {"us_per_call": round(hot_ms * 1e3, 2),
                                "roofline_frac": round(max(t_tensor, t_hbm) / (hot_ms / 1e3), 4)}
-        if kind in ("skinny", "skinny_noalloc", "gemv") or name.startswith(("fp8_decode",
+        if kind in ("skinny", "skinny_noalloc", "skinny_ws4", "gemv") or name.startswith(("fp8_decode",
                                                                              "fp8_skinny")):
             entry["hbm_frac"] = round(byts / med / 1e6 / bw, 4)
         res[name] = entry
