@@ -273,10 +273,12 @@ SWG_API int swiglu_interleave(const void *W1, const void *W2, void *W_fused,
  * Same arguments, rules and results as gemm_ex: for every input it launches
  * the kernels gemm_ex would launch, with the same tiles, split count and
  * fixed-order reduction, so the two give bit-identical D.  The one
- * difference: a split-K call keeps its FP32 partial sums in a fixed array of
- * SWG_NOALLOC_SCRATCH_BYTES (plus two 64 KiB guard bands) that is part of the
- * library's device image, instead of a workspace from cudaMalloc.  The
- * caller still passes A, B and C.
+ * difference: a split-K call that keeps FP32 partial sums in global memory
+ * keeps them in a fixed array of SWG_NOALLOC_SCRATCH_BYTES (plus two 64 KiB
+ * guard bands) that is part of the library's device image, instead of a
+ * workspace from cudaMalloc (few-row calls whose K ranges are reduced inside
+ * a thread-block cluster keep none there).  The caller still passes A, B
+ * and C.
  *
  *   Limit        a split needs splits * M * round_up(N, 4) * 4 bytes of
  *                partials; a call that would need more than

@@ -500,11 +500,18 @@ __device__ __forceinline__ void store_staged(const TileParams &p, const CUtensor
 
 // EPI_SPLITK_CL (swapped-operand frame: TMEM lane = output column n of the
 // tile, TMEM column j = output row m).  Rank r owns output rows
-// [r * BN / S, (r + 1) * BN / S) of the tile; recv[s][n][j - r * BN / S], so
-// each thread pushes four consecutive rows of its column with one 16-byte
-// store.  Before the accumulator is ready each thread loads the C values of
-// the outputs it will produce (beta != 0), so that read overlaps the main
-// loop.
+// [r * BN / S, (r + 1) * BN / S) of the tile.  recv[s] holds, per column n,
+// G = BN / S / 4 groups of four rows; group g of column n sits at 16-byte
+// slot n * G + (g XOR ((n * G / 8) mod G)), so each thread pushes four
+// consecutive rows of its column with one 16-byte store and eight
+// consecutive columns of one group fall in eight different bank groups.
+// Before the accumulator is ready each thread loads the C values of the
+// outputs it will produce (beta != 0), so that read overlaps the main loop.
+__device__ __forceinline__ int recv_slot(int n, int g, int G)
+{
+    return n * G + (g ^ ((n * G / 8) % G));
+}
+
 template <int BN>
 __device__ __forceinline__ void splitk_cluster_epilogue(const TileParams &p, uint32_t tmem_base,
                                                         uint8_t *recv_buf, uint64_t *acc_full,
@@ -520,8 +527,9 @@ __device__ __forceinline__ void splitk_cluster_epilogue(const TileParams &p, uin
     const int S = p.splits;
     int mb, nb, split, tile;
     unit_coords(p, unit, mb, nb, split, tile);
-    const int rows = BN / S;                   // output rows this rank reduces (>= 4)
-    const int n_items = (rows / 4) * BM;
+    const int rows = BN / S;                   // output rows this rank reduces (4 .. 32)
+    const int G = rows / 4;                    // four-row groups per column
+    const int n_items = G * BM;
     const int Mo = p.N, No = p.M;              // output rows / columns
     // item idx: column n = idx % BM of the tile, rows 4 * (idx / BM) .. + 3 of this rank's share
     float c[ITEMS][4];
@@ -561,7 +569,7 @@ __device__ __forceinline__ void splitk_cluster_epilogue(const TileParams &p, uin
                 if (nb * BN + jj >= Mo) break;     // rows past the output are not sent
                 const int owner = jj / rows;
                 const uint32_t a = recv + (uint32_t)krank * slice +
-                                   (uint32_t)((n_local * rows + jj - owner * rows) * 4);
+                                   (uint32_t)(recv_slot(n_local, (jj - owner * rows) / 4, G) * 16);
                 st_dsmem_v4(mapa_shared(a, (uint32_t)owner), r[4 * g], r[4 * g + 1], r[4 * g + 2],
                             r[4 * g + 3]);
             }
@@ -576,16 +584,17 @@ __device__ __forceinline__ void splitk_cluster_epilogue(const TileParams &p, uin
         const int idx = et + it * NUM_EPI_THREADS;
         if (idx >= n_items) continue;
         const int nl = idx % BM;
-        const int jl = 4 * (idx / BM);
+        const int g = idx / BM;
         const int n = mb * BM + nl;
-        const int m0 = nb * BN + krank * rows + jl;
+        const int m0 = nb * BN + krank * rows + 4 * g;
         if (n >= No) continue;
+        const int slot = recv_slot(nl, g, G);
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int r = 0; r < MAX_CLUSTER_SPLITS; ++r) {
             if (r < S) {
                 const float4 v = *reinterpret_cast<const float4 *>(
-                    rb + (size_t)r * (slice / 4) + nl * rows + jl);
+                    rb + (size_t)r * (slice / 4) + slot * 4);
                 acc[0] += v.x;
                 acc[1] += v.y;
                 acc[2] += v.z;
