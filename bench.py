@@ -521,8 +521,13 @@ def component_cases():
     cases += [(f"decode_gemv_M{m}", "gemv", m, 4096, 4096) for m in (1, 8)]
     cases += [("mlp_small_M2048", "mlp", 2048, 896, 4864), ("mlp_8b_M2048", "mlp", 2048, 4096, 14336),
               ("mlp_8b_M1", "mlp", 1, 4096, 14336)]
-    cases += [("swiglu_dual_small_M2048", "dual", 2048, 896, 4864),
-              ("swiglu_dual_8b_M2048", "dual", 2048, 4096, 14336),
+    # SwiGLU from separate W1, W2 at every small-model M of the benchmark and
+    # at M = 1024, beside the interleaved-weight rows (the two forms compared
+    # where the pages' dual-kernel strategy would dispatch by M)
+    cases += [(f"swiglu_dual_small_M{m}", "dual", m, 896, 4864) for m in (128, 512, 2048)]
+    cases += [("swiglu_small_M1024", "swiglu", 1024, 896, 4864),
+              ("swiglu_dual_small_M1024", "dual", 1024, 896, 4864)]
+    cases += [("swiglu_dual_8b_M2048", "dual", 2048, 4096, 14336),
               ("swiglu_dual_8b_M1", "dual", 1, 4096, 14336)]
     cases += [("fp8_decode_gemv_M1", "fp8gemm", 1, 4096, 4096),
               ("fp8_skinny_splitk_M16", "fp8gemm", 16, 16384, 4096)]

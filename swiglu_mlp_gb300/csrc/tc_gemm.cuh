@@ -179,14 +179,40 @@ struct Cfg {
                   "the stage area holds a staged FP32 output tile");
 };
 
+__device__ __forceinline__ void tile_coords(const TileParams &p, int tile, int &mb, int &nb);
+
 // Tile coordinates of work unit u (grouped raster: walk GROUP m-blocks down a
 // column of tiles before moving right, so concurrently running CTAs share A
 // and B panels in L2).
 __device__ __forceinline__ void unit_coords(const TileParams &p, int u, int &mb, int &nb,
                                             int &split, int &tile)
 {
-    split = u / p.tiles;
-    tile = u - split * p.tiles;
+    // Integer division by a runtime value is a chain of tens of dependent
+    // instructions on one thread; the first unit's coordinates sit on the
+    // path to the first load (measured ~0.4 us), so the common shapes skip it.
+    if (p.splits == 1) {
+        split = 0;
+        tile = u;
+    } else {
+        split = u / p.tiles;
+        tile = u - split * p.tiles;
+    }
+    tile_coords(p, tile, mb, nb);
+}
+
+// Block coordinates of tile `tile` in the grouped raster (see unit_coords).
+__device__ __forceinline__ void tile_coords(const TileParams &p, int tile, int &mb, int &nb)
+{
+    if (p.n_blocks == 1) {             // one column of tiles: the raster is the identity
+        mb = tile;
+        nb = 0;
+        return;
+    }
+    if (p.m_blocks == 1) {             // one row of tiles
+        mb = 0;
+        nb = tile;
+        return;
+    }
     const int per_group = p.group_m * p.n_blocks;
     const int group = tile / per_group;
     const int first_m = group * p.group_m;
@@ -743,9 +769,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // Cluster-reduced K: cluster c is tile c, rank r its K range r (unit r * tiles + c).
     constexpr bool CLK = ClusterK<EPI>::value;
     const int krank = CLK ? (int)cluster_ctarank() : 0;
-    const int first_unit = PAIR  ? (int)(blockIdx.x >> 1)
-                           : CLK ? krank * p.tiles + (int)blockIdx.x / p.splits
-                                 : (int)blockIdx.x;
+    const int cid = CLK ? (int)(blockIdx.x >> (p.splits >> 1)) : 0;   // cluster sizes 1, 2, 4
+    const int first_unit = PAIR ? (int)(blockIdx.x >> 1) : CLK ? krank * p.tiles + cid
+                                                               : (int)blockIdx.x;
     const int unit_step = PAIR ? (int)(gridDim.x >> 1) : CLK ? p.units : (int)gridDim.x;
 
     // Programmatic dependent launch: the kernel queued behind this one on the
@@ -819,7 +845,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             for (int u = first_unit; u < p.units && ok; u += unit_step) {
                 int mb, nb, split, tile;
-                unit_coords(p, u, mb, nb, split, tile);
+                if (CLK) {                     // the one unit: K range krank of tile cid
+                    split = krank;
+                    tile = cid;
+                    tile_coords(p, tile, mb, nb);
+                } else {
+                    unit_coords(p, u, mb, nb, split, tile);
+                }
                 const int kb0 = split * p.kb_per_split;
                 int kb1 = kb0 + p.kb_per_split;
                 kb1 = kb1 < p.k_blocks ? kb1 : p.k_blocks;
