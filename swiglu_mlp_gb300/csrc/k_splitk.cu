@@ -16,7 +16,43 @@
 
 namespace swg {
 
-__global__ void __launch_bounds__(256)
+// Four 16-bit or FP32 outputs of C/D as floats (beta != 0 only).
+__device__ __forceinline__ void load_c4(const void *D, long long off, int out_kind, int cnt,
+                                        float (&c)[4])
+{
+    if (cnt == 4 && out_kind == OUT_F32) {
+        const float4 v = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(D) + off);
+        c[0] = v.x;
+        c[1] = v.y;
+        c[2] = v.z;
+        c[3] = v.w;
+    } else if (cnt == 4) {
+        const uint2 w = *reinterpret_cast<const uint2 *>(reinterpret_cast<const uint16_t *>(D) + off);
+        const uint32_t cw[2] = {w.x, w.y};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (out_kind == OUT_F16) {
+                const __half2 c2 = *reinterpret_cast<const __half2 *>(&cw[h]);
+                c[2 * h] = __low2float(c2);
+                c[2 * h + 1] = __high2float(c2);
+            } else {
+                const __nv_bfloat162 c2 = *reinterpret_cast<const __nv_bfloat162 *>(&cw[h]);
+                c[2 * h] = __low2float(c2);
+                c[2 * h + 1] = __high2float(c2);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) c[j] = j < cnt ? load_out(D, off + j, out_kind) : 0.0f;
+    }
+}
+
+// Each thread owns Q groups of four outputs per round (i, i + stride, ..,
+// i + (Q-1) stride) and issues every load of the round -- the S_MAX >=
+// splits partials and, with beta != 0, C -- before the first add, so one
+// memory round trip covers the round.
+template <int S_MAX, int Q>
+__global__ void __launch_bounds__(256, 2)
     splitk_reduce_kernel(const float *__restrict__ ws, long long ld_ws, int splits, int M, int N,
                          float alpha, float beta, void *D, long long ldd, int out_kind)
 {
@@ -27,79 +63,70 @@ __global__ void __launch_bounds__(256)
     const int quads = (N + 3) / 4;
     const long long total = (long long)M * quads;
     const long long split_stride = (long long)M * ld_ws;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        const int m = (int)(i / quads);
-        const int n = (int)(i - (long long)m * quads) * 4;
-        const int cnt = (N - n) < 4 ? (N - n) : 4;
-        const float *src = ws + (long long)m * ld_ws + n;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        if (cnt == 4) {
-            float4 v[MAX_SPLITS];
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i0 = blockIdx.x * (long long)blockDim.x + threadIdx.x; i0 < total;
+         i0 += stride * Q) {
+        float4 v[Q][S_MAX];
+        float c[Q][4];
+        long long off[Q];
+        int cnt[Q];
 #pragma unroll
-            for (int s = 0; s < MAX_SPLITS; ++s)
-                if (s < splits) v[s] = __ldcg(reinterpret_cast<const float4 *>(src + s * split_stride));
+        for (int q = 0; q < Q; ++q) {
+            const long long i = i0 + q * stride;
+            cnt[q] = 0;
+            off[q] = 0;
+            if (i >= total) continue;
+            const int m = (int)(i / quads);
+            const int n = (int)(i - (long long)m * quads) * 4;
+            cnt[q] = (N - n) < 4 ? (N - n) : 4;
+            off[q] = (long long)m * ldd + n;
+            const float *src = ws + (long long)m * ld_ws + n;
+            if (cnt[q] == 4) {
 #pragma unroll
-            for (int s = 0; s < MAX_SPLITS; ++s) {
-                if (s < splits) {
-                    acc[0] += v[s].x;
-                    acc[1] += v[s].y;
-                    acc[2] += v[s].z;
-                    acc[3] += v[s].w;
-                }
-            }
-        } else {
-            for (int s = 0; s < splits; ++s) {
+                for (int sp = 0; sp < S_MAX; ++sp)
+                    if (sp < splits)
+                        v[q][sp] = __ldcg(reinterpret_cast<const float4 *>(src + sp * split_stride));
+            } else {
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (j < cnt) acc[j] += __ldcg(src + s * split_stride + j);
-            }
-        }
-        const long long off = (long long)m * ldd + n;
-        float out[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) out[j] = alpha * acc[j];
-        if (cnt == 4 && out_kind != OUT_F32) {
-            // four 16-bit outputs: one 8-byte load of C (beta != 0), one store
-            uint2 *dst = reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(D) + off);
-            if (beta != 0.0f) {
-                const uint2 c = *dst;
-                uint32_t cw[2] = {c.x, c.y};
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float lo, hi;
-                    if (out_kind == OUT_F16) {
-                        const __half2 c2 = *reinterpret_cast<const __half2 *>(&cw[h]);
-                        lo = __low2float(c2);
-                        hi = __high2float(c2);
-                    } else {
-                        const __nv_bfloat162 c2 = *reinterpret_cast<const __nv_bfloat162 *>(&cw[h]);
-                        lo = __low2float(c2);
-                        hi = __high2float(c2);
+                for (int sp = 0; sp < S_MAX; ++sp) {
+                    if (sp < splits) {
+                        const float *sq = src + sp * split_stride;
+                        v[q][sp] = make_float4(__ldcg(sq), cnt[q] > 1 ? __ldcg(sq + 1) : 0.0f,
+                                               cnt[q] > 2 ? __ldcg(sq + 2) : 0.0f, 0.0f);
                     }
-                    out[2 * h] += beta * lo;
-                    out[2 * h + 1] += beta * hi;
                 }
             }
-            *dst = make_uint2(pack2(out[0], out[1], out_kind), pack2(out[2], out[3], out_kind));
-        } else if (cnt == 4) {
-            float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(D) + off);
-            if (beta != 0.0f) {
-                const float4 c = *dst;
-                out[0] += beta * c.x;
-                out[1] += beta * c.y;
-                out[2] += beta * c.z;
-                out[3] += beta * c.w;
+            if (beta != 0.0f) load_c4(D, off[q], out_kind, cnt[q], c[q]);
+        }
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            if (cnt[q] == 0) continue;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int sp = 0; sp < S_MAX; ++sp) {
+                if (sp < splits) {
+                    acc[0] += v[q][sp].x;
+                    acc[1] += v[q][sp].y;
+                    acc[2] += v[q][sp].z;
+                    acc[3] += v[q][sp].w;
+                }
             }
-            *dst = make_float4(out[0], out[1], out[2], out[3]);
-        } else {
+            float out[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                if (j < cnt) {
-                    float v = out[j];
-                    if (beta != 0.0f) v += beta * load_out(D, off + j, out_kind);
-                    store_out(D, off + j, v, out_kind);
-                }
+                out[j] = alpha * acc[j];
+                if (beta != 0.0f) out[j] += beta * c[q][j];
+            }
+            if (cnt[q] == 4 && out_kind != OUT_F32) {
+                *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(D) + off[q]) =
+                    make_uint2(pack2(out[0], out[1], out_kind), pack2(out[2], out[3], out_kind));
+            } else if (cnt[q] == 4) {
+                *reinterpret_cast<float4 *>(reinterpret_cast<float *>(D) + off[q]) =
+                    make_float4(out[0], out[1], out[2], out[3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (j < cnt[q]) store_out(D, off[q] + j, out[j], out_kind);
             }
         }
     }
@@ -166,6 +193,10 @@ int max_active_clusters_splitk_cl(int bn, int csize, int sms)
 
 cudaError_t launch_splitk_reduce(const TileParams &p, int sms, cudaStream_t s)
 {
+    // Up to eight float4 partial loads in flight per thread (Q = 8 / S_MAX
+    // groups per round), two CTAs per SM; the grid as before: one group per
+    // thread up to four CTAs per SM, so a thread's groups fit in one round.
+    const int smax = p.splits <= 2 ? 2 : p.splits <= 4 ? 4 : p.splits <= 8 ? 8 : 16;
     const long long items = (long long)p.M * ((p.N + 3) / 4);
     long long blocks = (items + 255) / 256;
     const long long cap = (long long)sms * 4;
@@ -181,8 +212,12 @@ cudaError_t launch_splitk_reduce(const TileParams &p, int sms, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, (const float *)p.ws, p.ld_ws, p.splits,
-                              p.M, p.N, p.alpha, p.beta, p.D, p.ldd, p.out_kind);
+    auto kernel = smax == 2   ? splitk_reduce_kernel<2, 4>
+                  : smax == 4 ? splitk_reduce_kernel<4, 2>
+                  : smax == 8 ? splitk_reduce_kernel<8, 1>
+                              : splitk_reduce_kernel<16, 1>;
+    return cudaLaunchKernelEx(&cfg, kernel, (const float *)p.ws, p.ld_ws, p.splits, p.M, p.N,
+                              p.alpha, p.beta, p.D, p.ldd, p.out_kind);
 }
 
 }  // namespace swg
