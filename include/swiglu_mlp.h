@@ -106,8 +106,11 @@ typedef enum {
  *                   to 4 CTAs that sum their FP32 partials through shared
  *                   memory, in range order -- one kernel, no workspace --
  *                   when that occupies at least half of the SMs or splits K
- *                   as often as the workspace path would (SWG_CLUSTER_SPLITK=0
- *                   turns it off).
+ *                   as often as the workspace path would.  More rows with an
+ *                   automatic split: the same over 128 x 256 tiles (2 or 4
+ *                   ranks per tile) when all their clusters are resident at
+ *                   once and fill at least half of the SMs.
+ *                   SWG_CLUSTER_SPLITK=0 turns both off.
  *                   Otherwise the FP32 partials live
  *                   in a library-owned workspace, allocated (cudaMalloc) on
  *                   first use per (device, stream) and replaced by a larger

@@ -400,8 +400,8 @@ int max_pairs(DeviceState *d, int kind, int bn)
 }
 
 // Resident clusters of `csize` CTAs of a cluster-reduced split kernel
-// (kind 0 = few-rows GEMM, 1 = the same with e4m3, 2 = SwiGLU), cached per
-// device like max_pairs.
+// (kind 0 = few-rows GEMM, 1 = the same with e4m3, 2 = SwiGLU, 3 = GEMM
+// tiles of 128 x 256), cached per device like max_pairs.
 int max_clusters(DeviceState *d, int kind, int bn, int csize)
 {
     const int key = (16 + kind) * 65536 + bn * 16 + csize;
@@ -412,7 +412,8 @@ int max_clusters(DeviceState *d, int kind, int bn, int csize)
     }
     const int n = kind == 0   ? swg::max_active_clusters_splitk_cl(bn, csize, d->sms)
                   : kind == 1 ? swg::max_active_clusters_splitk_cl_fp8(bn, csize, d->sms)
-                              : swg::max_active_clusters_swiglu_cl(bn, csize, d->sms);
+                  : kind == 2 ? swg::max_active_clusters_swiglu_cl(bn, csize, d->sms)
+                              : swg::max_active_clusters_store_cl(csize, d->sms);
     std::lock_guard<std::mutex> lk(g_mu);
     d->max_pairs[key] = n;
     return n;
@@ -627,6 +628,55 @@ int splitk_swapped(DeviceState *d, const TypeInfo &ti, int transA, int transB, i
     r.ws = p.ws;
     r.ld_ws = ld_ws;
     if (swg::launch_splitk_reduce(r, d->sms, s) != cudaSuccess) return cuda_fail();
+    g_launches++;
+    return SWG_OK;
+}
+
+// GEMM over 128 x 256 tiles with the K range of each tile split over a
+// cluster of S CTAs (EPI_STORE_CL): the ranks exchange their FP32 partials
+// through shared memory and each stores alpha * sum + beta * C for its share
+// of the tile's columns, summed in rank order.
+int gemm_store_cluster(DeviceState *d, const TypeInfo &ti, int transA, int transB, int64_t M,
+                       int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
+                       const void *B, int64_t ldb, float beta, void *C, int64_t ldc, int S,
+                       cudaStream_t s)
+{
+    const bool a_mn = transA == SWG_OP_T;
+    const bool b_mn = transB == SWG_OP_N;
+    CUtensorMap ta, tb, t3;
+    bool ok = a_mn ? make_tmap(&ta, A, ti.in_bf16, M, K, lda, 64)
+                   : make_tmap(&ta, A, ti.in_bf16, K, M, lda, swg::BM);
+    ok = ok && (b_mn ? make_tmap(&tb, B, ti.in_bf16, N, K, ldb, 64)
+                     : make_tmap(&tb, B, ti.in_bf16, K, N, ldb, 256));
+    if (!ok) return cuda_fail();
+    TileParams p{};
+    p.a_mn3 = a_mn && make_tmap_mn3(&t3, A, ti.in_bf16, M, K, lda, swg::BM / 64);
+    if (p.a_mn3) ta = t3;
+    p.b_mn3 = b_mn && make_tmap_mn3(&t3, B, ti.in_bf16, N, K, ldb, 256 / 64);
+    if (p.b_mn3) tb = t3;
+    const int64_t kb = cdiv(K, swg::BK);
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.m_blocks = (int)cdiv(M, swg::BM);
+    p.n_blocks = (int)cdiv(N, 256);
+    p.k_blocks = (int)kb;
+    p.bk = swg::BK;
+    p.tiles = p.m_blocks * p.n_blocks;
+    p.splits = S;
+    p.kb_per_split = (int)cdiv(kb, S);
+    p.units = p.tiles * S;
+    p.group_m = 16;
+    p.idesc = make_idesc(ti.in_bf16, a_mn, b_mn, swg::BM, 256);
+    p.a_mn_major = a_mn;
+    p.b_mn_major = b_mn;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.D = C;
+    p.ldd = ldc;
+    p.out_kind = ti.out_kind;
+    p.err = d->err;
+    if (swg::launch_tc_store_cl(ta, tb, p, p.units, s) != cudaSuccess) return cuda_fail();
     g_launches++;
     return SWG_OK;
 }
@@ -1033,6 +1083,21 @@ static int gemm_impl(int transA, int transB, int64_t M, int64_t N, int64_t K, fl
         splits = (int)std::min<int64_t>(split_k, kb);
     }
     splits = std::min(splits, swg::MAX_SPLITS);
+    // More rows and an automatic split: 128 x 256 tiles whose K ranges run as
+    // one cluster of S CTAs that sum their partials through shared memory
+    // (one launch, no workspace), when S clusters per tile are resident at
+    // once and fill at least half of the SMs.
+    if (split_k == 0 && splits > 1 && M > 64 && !cluster_splitk_disabled() &&
+        forced_tile_mode(&forced_bn) == 0) {
+        const int64_t t1 = cdiv(M, swg::BM) * cdiv(N, 256);
+        int S = 0;
+        for (int s_c = 2; s_c <= swg::MAX_CLUSTER_SPLITS; s_c *= 2)
+            if (t1 * s_c <= d->sms && kb >= 4 * s_c && t1 <= max_clusters(d, 3, 256, s_c))
+                S = s_c;
+        if (S > 0 && t1 * S * 2 >= d->sms && (int64_t)(S - 1) * cdiv(kb, S) < kb)
+            return gemm_store_cluster(d, ti, transA, transB, M, N, K, alpha, A, lda, B, ldb,
+                                      beta, C, ldc, S, static_cast<cudaStream_t>(stream));
+    }
     // Few rows and a split K: compute the transposed product instead, so the
     // large operand fills the MMA's 128 rows and the <= 64 rows of op(A)
     // become its N (smaller stages, deeper pipeline, fewer partials).

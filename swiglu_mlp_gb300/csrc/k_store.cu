@@ -22,6 +22,17 @@ cudaError_t launch_tc_store(int bn, bool pair, const CUtensorMap &ta, const CUte
     }
 }
 
+cudaError_t launch_tc_store_cl(const CUtensorMap &ta, const CUtensorMap &tb, const TileParams &p,
+                               int ctas, cudaStream_t s)
+{
+    return launch_tc_impl<256, EPI_STORE_CL, false>(ta, tb, p, ctas, s);
+}
+
+int max_active_clusters_store_cl(int csize, int sms)
+{
+    return max_active_clusters_impl<256, EPI_STORE_CL>(sms, csize);
+}
+
 int max_active_pairs_store(int bn, int sms)
 {
     switch (bn) {

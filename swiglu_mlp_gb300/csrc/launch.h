@@ -45,6 +45,13 @@ cudaError_t launch_tc_splitk(int bn, bool pair, const CUtensorMap &ta, const CUt
                              const TileParams &p, int units, cudaStream_t s,
                              const CUtensorMap *tout = nullptr);
 
+// GEMM tiles of 128 x 256 with the K range split over a cluster of p.splits
+// (2 or 4) CTAs that reduce through shared memory (EPI_STORE_CL); `ctas` =
+// tiles x splits.
+cudaError_t launch_tc_store_cl(const CUtensorMap &ta, const CUtensorMap &tb, const TileParams &p,
+                               int ctas, cudaStream_t s);
+int max_active_clusters_store_cl(int csize, int sms);
+
 // Split-K with swapped operands (the kernel computes the transposed product;
 // `bn` 16, 32 or 64 is the width of the original rows it covers).
 cudaError_t launch_tc_splitk_t(int bn, const CUtensorMap &ta, const CUtensorMap &tb,

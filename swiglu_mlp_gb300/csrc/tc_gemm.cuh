@@ -80,6 +80,8 @@ namespace swg {
 // output's own frame (rows = rows of A, columns = the 2N-space of W_fused):
 // rank r sums its share of the tile's column pairs over the S ranks and
 // stores SiLU(alpha * gate) * (alpha * up).
+// EPI_STORE_CL: the same for a plain GEMM tile (128 x BN, output frame):
+// rank r stores alpha * sum + beta * C for its share of the tile's columns.
 enum EpiKind {
     EPI_STORE = 0,
     EPI_SWIGLU = 1,
@@ -87,13 +89,18 @@ enum EpiKind {
     EPI_SPLITK_T = 3,
     EPI_SWIGLU_DUAL = 4,
     EPI_SPLITK_CL = 5,
-    EPI_SWIGLU_CL = 6
+    EPI_SWIGLU_CL = 6,
+    EPI_STORE_CL = 7
 };
 
 // The epilogues whose K ranges are reduced inside a cluster (one unit per CTA).
 template <int EPI>
 struct ClusterK {
-    static constexpr bool value = EPI == EPI_SPLITK_CL || EPI == EPI_SWIGLU_CL;
+    static constexpr bool value =
+        EPI == EPI_SPLITK_CL || EPI == EPI_SWIGLU_CL || EPI == EPI_STORE_CL;
+    // EPI_STORE_CL receives the partials in its consumed pipeline stages, so
+    // its ranks first wait for every rank's main loop (one more barrier).
+    static constexpr int barriers = EPI == EPI_STORE_CL ? 2 : 1;
 };
 enum OutKind { OUT_BF16 = 0, OUT_F16 = 1, OUT_F32 = 2 };
 
@@ -733,6 +740,147 @@ __device__ __forceinline__ void swiglu_cluster_epilogue(const TileParams &p, uin
     }
 }
 
+// EPI_STORE_CL (output frame, 128 x BN tile, TMEM lane = row).  Rank r owns
+// the tile's columns [r * BN / S, (r + 1) * BN / S); recv[s][row][column -
+// r * BN / S] with rows padded by 4 floats sits in the consumed stages, so the
+// ranks first pass a cluster barrier once every main loop has finished.  C
+// for this rank's outputs is loaded (beta != 0) before the accumulator is
+// ready.  For each row and group of 8 columns the owner stores
+// alpha * (recv[0] + .. + recv[S-1]) + beta * C, summed in rank order from 0.
+template <int BN>
+__device__ __forceinline__ void store_cluster_epilogue(const TileParams &p, uint32_t tmem_base,
+                                                       uint8_t *recv_buf, uint64_t *acc_full,
+                                                       volatile int *abort_flag, int krank, int cid)
+{
+    constexpr int NC = BN / 32;
+    // items per thread with S >= 2 (instantiated for BN = 256 only; the
+    // floor of one keeps other instantiations of the kernel compilable)
+    constexpr int ITEMS_RAW = BM * (BN / 2) / 8 / NUM_EPI_THREADS;
+    constexpr int ITEMS = ITEMS_RAW > 0 ? ITEMS_RAW : 1;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int et = threadIdx.x - EPI_WARP0 * 32;
+    const int S = p.splits;
+    const int cols = BN / S;                   // this rank's columns (>= 64)
+    const int ld = cols + 4;
+    const uint32_t slice = (uint32_t)(BM * ld * 4);
+    int mb, nb;
+    tile_coords(p, cid, mb, nb);
+    const int n_items = BM * (cols / 8);
+    // 1. C of this rank's outputs
+    float c[ITEMS][8];
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) c[it][j] = 0.0f;
+        const int idx = et + it * NUM_EPI_THREADS;
+        if (p.beta == 0.0f || idx >= n_items) continue;
+        const int m = mb * BM + idx % BM;
+        const int n = nb * BN + krank * cols + (idx / BM) * 8;
+        if (m >= p.M || n >= p.N) continue;
+        const long long off = (long long)m * p.ldd + n;
+        if (p.N - n >= 8 && p.out_kind != OUT_F32) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(
+                reinterpret_cast<const uint16_t *>(p.D) + off);
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                if (p.out_kind == OUT_F16) {
+                    const __half2 c2 = *reinterpret_cast<const __half2 *>(&ww[h]);
+                    c[it][2 * h] = __low2float(c2);
+                    c[it][2 * h + 1] = __high2float(c2);
+                } else {
+                    const __nv_bfloat162 c2 = *reinterpret_cast<const __nv_bfloat162 *>(&ww[h]);
+                    c[it][2 * h] = __low2float(c2);
+                    c[it][2 * h + 1] = __high2float(c2);
+                }
+            }
+        } else if (p.N - n >= 8) {
+            const float4 *src = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(p.D) + off);
+            const float4 a = src[0], b = src[1];
+            c[it][0] = a.x; c[it][1] = a.y; c[it][2] = a.z; c[it][3] = a.w;
+            c[it][4] = b.x; c[it][5] = b.y; c[it][6] = b.z; c[it][7] = b.w;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (j < p.N - n) c[it][j] = load_out(p.D, off + j, p.out_kind);
+        }
+    }
+    // 2. every rank's main loop is over: its stages may receive partials
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int c_begin = ((warp - EPI_WARP0) / 4) * (NC / 2);
+    bool ok = wait_bounded(smem_u32(&acc_full[0]), 0, abort_flag, p.err);
+    ok = __all_sync(0xffffffffu, ok);
+    cluster_sync_all();
+    const uint32_t recv = smem_u32(recv_buf);
+    if (ok && __any_sync(0xffffffffu, mb * BM + row < p.M)) {
+        tc_fence_after();
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        const bool send = mb * BM + row < p.M;  // rows past the output are not sent
+#pragma unroll 1
+        for (int cc = c_begin; cc < c_begin + NC / 2; ++cc) {
+            uint32_t r[32];
+            tmem_ld_32cols(t_row + cc * 32, r);  // whole warp (.sync.aligned)
+            tmem_ld_wait(r);
+            if (!send) continue;
+            const int owner = (cc * 32) / cols;
+            const uint32_t a = mapa_shared(
+                recv + (uint32_t)krank * slice + (uint32_t)((row * ld + cc * 32 - owner * cols) * 4),
+                (uint32_t)owner);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                st_dsmem_v4(a + 16 * j, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+        }
+    }
+    tc_fence_before();
+    cluster_sync_all();
+    // 3. reduce this rank's columns from the local receive buffer
+    const float *rb = reinterpret_cast<const float *>(recv_buf);
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const int idx = et + it * NUM_EPI_THREADS;
+        if (idx >= n_items) continue;
+        const int rr = idx % BM;
+        const int cl = (idx / BM) * 8;
+        const int m = mb * BM + rr;
+        const int n = nb * BN + krank * cols + cl;
+        if (m >= p.M || n >= p.N) continue;
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+#pragma unroll
+        for (int r = 0; r < MAX_CLUSTER_SPLITS; ++r) {
+            if (r < S) {
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    rb + (size_t)r * (slice / 4) + rr * ld + cl);
+                const float4 a = src[0], b = src[1];
+                acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+                acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+            }
+        }
+        float out[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            out[j] = p.beta != 0.0f ? __fmaf_rn(p.beta, c[it][j], p.alpha * acc[j])
+                                    : p.alpha * acc[j];
+        const long long off = (long long)m * p.ldd + n;
+        if (p.N - n >= 8 && p.out_kind != OUT_F32) {
+            *reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.D) + off) =
+                make_uint4(pack2(out[0], out[1], p.out_kind), pack2(out[2], out[3], p.out_kind),
+                           pack2(out[4], out[5], p.out_kind), pack2(out[6], out[7], p.out_kind));
+        } else if (p.N - n >= 8) {
+            float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.D) + off);
+            dst[0] = make_float4(out[0], out[1], out[2], out[3]);
+            dst[1] = make_float4(out[4], out[5], out[6], out[7]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (j < p.N - n) store_out(p.D, off + j, out[j], p.out_kind);
+        }
+    }
+}
+
 // FP8: operands are 8-bit (e4m3/e5m2) and the MMA is kind::f8f6f4.  In bytes
 // nothing else changes: a 128-byte swizzled stage row holds 128 elements and
 // each MMA (K = 32) consumes 32 bytes of it, as a kind::f16 MMA (K = 16) does.
@@ -951,7 +1099,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
         __syncwarp();
-        if (CLK) cluster_sync_all();   // partials pushed (see the cluster epilogues)
+        if (CLK) {                     // (see the cluster epilogues)
+            for (int b = 0; b < ClusterK<EPI>::barriers; ++b) cluster_sync_all();
+        }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && leader) {
@@ -1031,11 +1181,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             wait_bounded(smem_u32(mma_done), 0, abort_flag, p.err, false, DRAIN_LIMIT_NS);
         }
         __syncwarp();
-        if (CLK) cluster_sync_all();   // partials pushed (see the cluster epilogues)
+        if (CLK) {                     // (see the cluster epilogues)
+            for (int b = 0; b < ClusterK<EPI>::barriers; ++b) cluster_sync_all();
+        }
     } else if (EPI == EPI_SPLITK_CL) {
         splitk_cluster_epilogue<BN>(p, tmem_base, recv, acc_full, abort_flag, first_unit, krank);
     } else if (EPI == EPI_SWIGLU_CL) {
         swiglu_cluster_epilogue<BN>(p, tmem_base, recv, acc_full, abort_flag, first_unit, krank);
+    } else if (EPI == EPI_STORE_CL) {
+        // the partials go to the consumed stages (at most 139 KB of 192 KB)
+        store_cluster_epilogue<BN>(p, tmem_base, smem, acc_full, abort_flag, krank, cid);
     } else if (EPI == EPI_SWIGLU_DUAL) {
         // ------------------------------------------ epilogue (separate W1, W2)
         // Output column j of the tile = SiLU(acc[j]) * acc[BN/2 + j]; warps

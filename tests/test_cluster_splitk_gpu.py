@@ -122,3 +122,58 @@ def test_graph_capture_without_warm_up():
     assert swg.get_device_error() == 0
     yhat = oracle.gemm(0, 0, M, N, K, 2.0, A, K, B, N, 0.0)
     check_half(to_f64(D.cpu("graph")), yhat, "cluster graph replay")
+
+
+# ---------------------------------------------------------------- M > 64
+# With more rows an automatic split runs 128 x 256 tiles whose K ranges form
+# one cluster of 2 or 4 CTAs; the partials are exchanged in the consumed
+# pipeline stages and each rank stores alpha * sum + beta * C for its share of
+# the tile's columns.
+
+@pytest.mark.parametrize("M,N,K", [(2048, 896, 4864),      # the small MLP's down projection, 2 ranks
+                                   (1024, 1024, 8192),     # 32 tiles, 4 ranks
+                                   (600, 1200, 4000)])     # ragged M, N and K, 4 ranks
+@pytest.mark.parametrize("tA,tB", [(0, 0), (1, 1), (0, 1), (1, 0)])
+def test_tiles_with_cluster_split_every_output(M, N, K, tA, tB):
+    g = synth.generator(600 + M + 2 * tA + tB)
+    A = synth.normal(synth.stored_shape(tA, M, K), g)
+    B = synth.normal(synth.stored_shape(tB, K, N), g, std=0.05)
+    C = synth.normal((M, N), g)
+    D = Guarded(M, N, torch.bfloat16, init=C)
+    swg.gemm(tA, tB, M, N, K, 1.0, A.cuda(), A.shape[1], B.cuda(), B.shape[1], 1.0, D.view, D.ld,
+             swg.BF16)
+    assert swg.get_device_error() == 0
+    yhat = oracle.gemm(tA, tB, M, N, K, 1.0, A, A.shape[1], B, B.shape[1], 1.0, C, N)
+    check_half(to_f64(D.cpu(f"cluster tiles {M}x{N}x{K}")), yhat,
+               f"cluster tiles {M}x{N}x{K} tA={tA} tB={tB}")
+
+
+def test_tiles_with_cluster_split_f32_out_nan_c():
+    M, N, K = 1024, 1024, 8192
+    A, B, _ = synth.gemm_bf16(M, N, K, seed=67)
+    D = Guarded(M, N, torch.float32, fill=float("nan"))
+    swg.gemm(0, 0, M, N, K, 0.5, A.cuda(), K, B.cuda(), N, 0.0, D.view, D.ld, swg.BF16_F32OUT)
+    assert swg.get_device_error() == 0
+    rows = sorted({0, 127, 128, 511, 512, M - 1})
+    yhat = oracle.gemm(0, 0, M, N, K, 0.5, A, K, B, N, 0.0, rows=rows)
+    out = to_f64(D.cpu("cluster tiles f32"))
+    assert np.isfinite(out).all()
+    check_f32(out[rows], yhat, K, "cluster tiles f32 out")
+
+
+def test_tiles_with_cluster_split_match_workspace_and_repeat(monkeypatch):
+    M, N, K = 2048, 896, 4864
+    A, B, C = synth.gemm_bf16(M, N, K, seed=68, c=True)
+    Ad, Bd = A.cuda(), B.cuda()
+    outs = []
+    for flag in ("1", "1", "0"):
+        monkeypatch.setenv("SWG_CLUSTER_SPLITK", flag)
+        D = Guarded(M, N, torch.bfloat16, init=C, ld=N)
+        swg.gemm(0, 0, M, N, K, 1.0, Ad, K, Bd, N, 1.0, D.view, N, swg.BF16)
+        outs.append(D.cpu(f"cluster={flag}"))
+    assert swg.get_device_error() == 0
+    assert torch.equal(outs[0], outs[1])
+    rows = sorted({0, 127, 128, 1023, 1024, M - 1})
+    yhat = oracle.gemm(0, 0, M, N, K, 1.0, A, K, B, N, 1.0, C, N, rows=rows)
+    check_half(to_f64(outs[0])[rows], yhat, "cluster tiles")
+    check_half(to_f64(outs[2])[rows], yhat, "workspace tiles")
