@@ -603,8 +603,11 @@ __device__ __forceinline__ void splitk_cluster_epilogue(const TileParams &p, uin
                 const int owner = jj / rows;
                 const uint32_t a = recv + (uint32_t)krank * slice +
                                    (uint32_t)(recv_slot(n_local, (jj - owner * rows) / 4, G) * 16);
-                st_dsmem_v4(mapa_shared(a, (uint32_t)owner), r[4 * g], r[4 * g + 1], r[4 * g + 2],
-                            r[4 * g + 3]);
+                if (owner == krank)                // own share: a local store
+                    st_shared_v4(a, make_uint4(r[4 * g], r[4 * g + 1], r[4 * g + 2], r[4 * g + 3]));
+                else
+                    st_dsmem_v4(mapa_shared(a, (uint32_t)owner), r[4 * g], r[4 * g + 1],
+                                r[4 * g + 2], r[4 * g + 3]);
             }
         }
     }
@@ -685,12 +688,19 @@ __device__ __forceinline__ void swiglu_cluster_epilogue(const TileParams &p, uin
             tmem_ld_wait(r);
             if (!send) continue;
             const int owner = (c * 32) / cols;
-            const uint32_t a = mapa_shared(
-                recv + (uint32_t)krank * slice + (uint32_t)((row * ld + c * 32 - owner * cols) * 4),
-                (uint32_t)owner);
+            const uint32_t al =
+                recv + (uint32_t)krank * slice + (uint32_t)((row * ld + c * 32 - owner * cols) * 4);
+            if (owner == krank) {                 // own share: local stores
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                st_dsmem_v4(a + 16 * j, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+                for (int j = 0; j < 8; ++j)
+                    st_shared_v4(al + 16 * j,
+                                 make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]));
+            } else {
+                const uint32_t a = mapa_shared(al, (uint32_t)owner);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    st_dsmem_v4(a + 16 * j, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+            }
         }
     }
     tc_fence_before();
@@ -700,8 +710,9 @@ __device__ __forceinline__ void swiglu_cluster_epilogue(const TileParams &p, uin
     const int n_out = p.N / 2;                 // output columns (p.N is the 2N-space width)
 #pragma unroll 1
     for (int idx = et; idx < n_items; idx += NUM_EPI_THREADS) {
-        const int rr = idx % BM;
-        const int cl = (idx / BM) * 16;        // column within this rank's share
+        // consecutive threads take consecutive groups of a row (wider stores)
+        const int rr = idx / (cols / 16);
+        const int cl = (idx % (cols / 16)) * 16;   // column within this rank's share
         const int m = mb * BM + rr;
         const int n = (nb * BN + krank * cols + cl) / 2;   // first output column
         if (m >= p.M || n >= n_out) continue;
@@ -775,8 +786,9 @@ __device__ __forceinline__ void store_cluster_epilogue(const TileParams &p, uint
         for (int j = 0; j < 8; ++j) c[it][j] = 0.0f;
         const int idx = et + it * NUM_EPI_THREADS;
         if (p.beta == 0.0f || idx >= n_items) continue;
-        const int m = mb * BM + idx % BM;
-        const int n = nb * BN + krank * cols + (idx / BM) * 8;
+        // consecutive threads take consecutive groups of a row: whole lines
+        const int m = mb * BM + idx / (cols / 8);
+        const int n = nb * BN + krank * cols + (idx % (cols / 8)) * 8;
         if (m >= p.M || n >= p.N) continue;
         const long long off = (long long)m * p.ldd + n;
         if (p.N - n >= 8 && p.out_kind != OUT_F32) {
@@ -825,12 +837,19 @@ __device__ __forceinline__ void store_cluster_epilogue(const TileParams &p, uint
             tmem_ld_wait(r);
             if (!send) continue;
             const int owner = (cc * 32) / cols;
-            const uint32_t a = mapa_shared(
-                recv + (uint32_t)krank * slice + (uint32_t)((row * ld + cc * 32 - owner * cols) * 4),
-                (uint32_t)owner);
+            const uint32_t al =
+                recv + (uint32_t)krank * slice + (uint32_t)((row * ld + cc * 32 - owner * cols) * 4);
+            if (owner == krank) {                 // own share: local stores
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                st_dsmem_v4(a + 16 * j, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+                for (int j = 0; j < 8; ++j)
+                    st_shared_v4(al + 16 * j,
+                                 make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]));
+            } else {
+                const uint32_t a = mapa_shared(al, (uint32_t)owner);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    st_dsmem_v4(a + 16 * j, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+            }
         }
     }
     tc_fence_before();
@@ -841,8 +860,8 @@ __device__ __forceinline__ void store_cluster_epilogue(const TileParams &p, uint
     for (int it = 0; it < ITEMS; ++it) {
         const int idx = et + it * NUM_EPI_THREADS;
         if (idx >= n_items) continue;
-        const int rr = idx % BM;
-        const int cl = (idx / BM) * 8;
+        const int rr = idx / (cols / 8);
+        const int cl = (idx % (cols / 8)) * 8;
         const int m = mb * BM + rr;
         const int n = nb * BN + krank * cols + cl;
         if (m >= p.M || n >= p.N) continue;
