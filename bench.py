@@ -540,18 +540,23 @@ def component_cases():
     return cases
 
 
-def build_case(kind, M, K, N, dev, stream):
+def build_case(kind, M, K, N, dev, stream, keep=None):
     """Returns (fn, reset, flops, algorithmic_bytes) for one workload; `reset`
-    restores C between repetitions (beta = 1) and is run outside the events."""
+    restores C between repetitions (beta = 1) and is run outside the events.
+    `keep` (a dict), if given, receives the host inputs and the device output
+    of the call, so that a test can check exactly what is timed here."""
     import torch
 
     import swiglu_mlp_gb300 as swg
     import synth
+    if keep is None:
+        keep = {}
     if kind == "swiglu":
         A, W1, W2 = synth.swiglu(M, K, N, seed=3)
         Ad = A.to(dev)
         Wf = swg.interleave_weights(W1.to(dev), W2.to(dev), stream=stream)
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        keep.update(A=A, W1=W1, W2=W2, out=Y)
 
         def fn():
             swg.swiglu_mlp(Ad, Wf, Y, M, N, K, stream=stream)
@@ -562,6 +567,7 @@ def build_case(kind, M, K, N, dev, stream):
         Cd = C0.clone()
         call = swg.gemm_splitk_noalloc if kind == "skinny_noalloc" else swg.gemm_ex
         split = 0 if kind == "skinny" else 4
+        keep.update(A=A, B=B, C=C, out=Cd)
 
         def fn():
             call(0, 0, M, N, K, 1.0, Ad, K, Bd, N, 1.0, Cd, N, swg.BF16, split, stream=stream)
@@ -574,6 +580,7 @@ def build_case(kind, M, K, N, dev, stream):
         A = torch.randn(M, K, generator=g).to(torch.float8_e4m3fn).to(dev)
         Bt = torch.randn(N, K, generator=g).to(torch.float8_e4m3fn).to(dev)
         D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        keep.update(A=A.cpu(), Bt=Bt.cpu(), out=D)
 
         def fn():
             swg.gemm(0, 1, M, N, K, 1.0 / 64, A, K, Bt, K, 0.0, D, N, swg.E4M3_BF16OUT,
@@ -586,6 +593,7 @@ def build_case(kind, M, K, N, dev, stream):
         Wt[1::2] = W2.t()
         Ad, Wtd = A.to(dev), Wt.to(dev)
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        keep.update(A=A, W1=W1, W2=W2, scale=sw, out=Y)
 
         def fn():
             swg.swiglu_mlp_fp8(Ad, Wtd, Y, M, N, K, sw, stream=stream)
@@ -594,6 +602,7 @@ def build_case(kind, M, K, N, dev, stream):
         A, W1, W2 = synth.swiglu(M, K, N, seed=3)
         Ad, W1d, W2d = A.to(dev), W1.to(dev), W2.to(dev)
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        keep.update(A=A, W1=W1, W2=W2, out=Y)
 
         def fn():
             swg.swiglu_mlp_dual(Ad, W1d, W2d, Y, M, N, K, stream=stream)
@@ -601,12 +610,15 @@ def build_case(kind, M, K, N, dev, stream):
     if kind == "mlp":
         # Out = (SiLU(A W1) (.) (A W2)) W_down + Out (residual, beta = 1)
         A, W1, W2 = synth.swiglu(M, K, N, seed=3)
-        Wd = synth.normal((N, K), synth.generator(6), std=0.02).to(dev)
+        Wd_h = synth.normal((N, K), synth.generator(6), std=0.02)
+        R_h = synth.normal((M, K), synth.generator(7))
+        Wd = Wd_h.to(dev)
         Ad = A.to(dev)
         Wf = swg.interleave_weights(W1.to(dev), W2.to(dev), stream=stream)
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        R = synth.normal((M, K), synth.generator(7)).to(dev)
+        R = R_h.to(dev)
         Out = R.clone()
+        keep.update(A=A, W1=W1, W2=W2, Wd=Wd_h, R=R_h, Y=Y, out=Out)
 
         def fn():
             swg.swiglu_mlp_forward(Ad, Wf, Wd, Y, Out, M, N, K, 1.0, stream=stream)
@@ -619,6 +631,7 @@ def build_case(kind, M, K, N, dev, stream):
         A = synth.normal((M, K), g).to(dev)
         B = synth.normal((K, N), g).to(dev)
         D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        keep.update(A=A.cpu(), B=B.cpu(), out=D)
 
         def fn():
             swg.gemm(0, 0, M, N, K, 1.0, A, K, B, N, 0.0, D, N, swg.BF16, stream=stream)
@@ -628,6 +641,7 @@ def build_case(kind, M, K, N, dev, stream):
         A, B, C = synth.gemm_f16_small(seed=0, M=M, N=N, K=K)
         Ad, Bd, C0 = A.to(dev), B.to(dev), C.to(dev)
         Cd = C0.clone()
+        keep.update(A=A, B=B, C=C, out=Cd)
 
         def fn():
             swg.gemm(0, 0, M, N, K, 1.5, Ad, K, Bd, N, 0.5, Cd, N, swg.F16_F32OUT, stream=stream)
@@ -641,6 +655,7 @@ def build_case(kind, M, K, N, dev, stream):
         A, B, _ = synth.gemm_bf16(M, N, K, tA, tB, seed=1)
         Ad, Bd = A.to(dev), B.to(dev)
         D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        keep.update(A=A, B=B, trans=(tA, tB), out=D)
 
         def fn():
             swg.gemm(tA, tB, M, N, K, 1.0, Ad, A.shape[1], Bd, B.shape[1], 0.0, D, N, swg.BF16,
