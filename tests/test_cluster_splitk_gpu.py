@@ -177,3 +177,38 @@ def test_tiles_with_cluster_split_match_workspace_and_repeat(monkeypatch):
     yhat = oracle.gemm(0, 0, M, N, K, 1.0, A, K, B, N, 1.0, C, N, rows=rows)
     check_half(to_f64(outs[0])[rows], yhat, "cluster tiles")
     check_half(to_f64(outs[2])[rows], yhat, "workspace tiles")
+
+
+# Ragged edges of the 128 x 256 cluster tiles: M past the last full 128-row
+# block, N past the last full 256-column block (a rank's share cut short), K
+# not a multiple of the two ranges.
+@pytest.mark.parametrize("M,N,K", [(2000, 904, 4000),      # 64 tiles x 2 ranks
+                                   (1800, 1000, 3000)])    # 60 tiles x 2 ranks
+@pytest.mark.parametrize("tA,tB", [(0, 0), (1, 1), (0, 1), (1, 0)])
+def test_cluster_tiles_ragged_every_output(M, N, K, tA, tB):
+    g = synth.generator(700 + M + 2 * tA + tB)
+    A = synth.normal(synth.stored_shape(tA, M, K), g)
+    B = synth.normal(synth.stored_shape(tB, K, N), g, std=0.05)
+    C = synth.normal((M, N), g)
+    D = Guarded(M, N, torch.bfloat16, init=C)
+    n0 = swg.launch_count()
+    swg.gemm(tA, tB, M, N, K, 1.0, A.cuda(), A.shape[1], B.cuda(), B.shape[1], 1.0, D.view, D.ld,
+             swg.BF16)
+    assert swg.launch_count() - n0 == 1
+    assert swg.get_device_error() == 0
+    yhat = oracle.gemm(tA, tB, M, N, K, 1.0, A, A.shape[1], B, B.shape[1], 1.0, C, N)
+    check_half(to_f64(D.cpu(f"cluster tiles {M}x{N}x{K}")), yhat,
+               f"cluster tiles {M}x{N}x{K} tA={tA} tB={tB}")
+
+
+def test_cluster_tiles_two_ranks_f32_out_nan_c():
+    M, N, K = 2048, 896, 4864
+    A, B, _ = synth.gemm_bf16(M, N, K, seed=69)
+    D = Guarded(M, N, torch.float32, fill=float("nan"))
+    swg.gemm(0, 0, M, N, K, 0.5, A.cuda(), K, B.cuda(), N, 0.0, D.view, D.ld, swg.BF16_F32OUT)
+    assert swg.get_device_error() == 0
+    rows = sorted({0, 127, 128, 255, 256, 1023, 1024, M - 129, M - 128, M - 1})
+    yhat = oracle.gemm(0, 0, M, N, K, 0.5, A, K, B, N, 0.0, rows=rows)
+    out = to_f64(D.cpu("cluster tiles f32, two ranks"))
+    assert np.isfinite(out).all()
+    check_f32(out[rows], yhat, K, "cluster tiles f32 out, two ranks")
