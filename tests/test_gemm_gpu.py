@@ -165,6 +165,37 @@ def test_alpha_linearity_power_of_two_exact():
     assert torch.equal(D4.cpu("alpha 4"), 4.0 * D1.cpu("alpha 1"))
 
 
+# alpha = 0 and alpha < 0 on every path a product can take: 128 x 256 pair
+# tiles, the few-rows cluster kernel, the 128 x 256 cluster tiles, the explicit
+# split with its reduction kernel, and the one-row FP32-pipe kernel.
+_ALPHA_SHAPES = [(300, 264, 200, 0), (16, 4096, 4096, 0), (2048, 896, 4864, 0),
+                 (200, 1024, 2048, 3), (1, 520, 1000, 0)]
+
+
+@pytest.mark.parametrize("M,N,K,split", _ALPHA_SHAPES)
+def test_alpha_zero_gives_beta_c_exactly(M, N, K, split):
+    """With finite operands and alpha = 0 every product is scaled to zero, so
+    D = beta * C with one rounding; beta = 1/2 halves a bf16 value exactly."""
+    A, B, C = synth.gemm_bf16(M, N, K, seed=M + N, c=True)
+    D = Guarded(M, N, torch.bfloat16, init=C)
+    swg.gemm_ex(0, 0, M, N, K, 0.0, A.cuda(), K, B.cuda(), N, 0.5, D.view, D.ld, swg.BF16, split)
+    assert swg.get_device_error() == 0
+    assert torch.equal(D.cpu("alpha 0"), (0.5 * C.float()).to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("M,N,K,split", _ALPHA_SHAPES)
+def test_negative_alpha(M, N, K, split):
+    A, B, C = synth.gemm_bf16(M, N, K, seed=2 * M + N, c=True)
+    D = Guarded(M, N, torch.bfloat16, init=C)
+    swg.gemm_ex(0, 0, M, N, K, -0.75, A.cuda(), K, B.cuda(), N, 1.0, D.view, D.ld, swg.BF16,
+                split)
+    assert swg.get_device_error() == 0
+    rows = None if M <= 300 else [0, 1, 127, 128, 255, 256, M // 2, M - 1]
+    yhat = oracle.gemm(0, 0, M, N, K, -0.75, A, K, B, N, 1.0, C, N, rows=rows)
+    out = to_f64(D.cpu("alpha < 0"))
+    check_half(out if rows is None else out[rows], yhat, f"alpha -0.75 {M}x{N}x{K}")
+
+
 def test_beta_one_accumulates_twice():
     """gemm with beta = 1 run twice over the same C adds A B twice."""
     M, N, K = 128, 256, 128
